@@ -1,0 +1,194 @@
+/*
+ * mxfp4.h — C ABI of the GB300 (sm_103a) MXFP4 block-scaled dense linear.
+ *
+ * The library implements the hot path of the MXFP4 dense linear described in
+ * sglang PR #39598 "[AMD] Add opt-in AITER ASM FP4 GEMM for Quark dense
+ * linear" (and its blog analysis, section 2, the diff of
+ * quark_w4a4_mxfp4.py) and the A16WFP4 absorbed BMM of sglang PR #34317
+ * "[AMD] [GLM5] use tuned MXFP4 kernels for MLA absorbed BMM".
+ *
+ * Formats.  An MXFP4 matrix of R rows and K elements (K even) is
+ *   - codes:  E2M1 4-bit values, two per byte, element 2j in the low nibble
+ *             of byte j, row-major [R][K/2];
+ *   - scales: E8M0 bytes (value 2^(e-127), 0xFF = NaN), one per 32
+ *             consecutive elements of a row, row-major [R][ceil(K/32)]
+ *             (shapes of the pages' per_1x32_f4_quant fake implementation).
+ *
+ * The TILED layout (MXFP4_LAYOUT_TILED) is this library's repacked form,
+ * the layout the tcgen05 block-scaled MMA consumes: rows padded to
+ * Rp = ceil(R/128)*128 and elements to Kp = ceil(K/256)*256;
+ *   codes region (Rp*Kp/2 bytes): 16 KiB tiles of 128 rows x 128 bytes,
+ *     tile (rt,kt) at ((rt*Kp/256)+kt)*16384, byte j of tile row i at
+ *     i*128 + ((j/16) ^ (i%8))*16 + j%16 (128-byte swizzle);
+ *   scales region (Rp*Kp/32 bytes): 512-byte atoms of 128 rows x 4 scales,
+ *     atom (rt,g) at ((rt*Kp/128)+g)*512, scale of atom row i, block b at
+ *     16*(i%32) + 4*(i/32) + b%4.
+ *   Padding codes are 0 and padding scales 0x7F (E8M0 1.0; the pages pad
+ *   with 1.0 because 0xFF is NaN).
+ *
+ * Conventions.
+ *   - Pointers named *_dev are device pointers; the caller owns all memory.
+ *     Except for the workspace the caller passes, the library allocates
+ *     nothing and frees nothing.
+ *   - stream is a cudaStream_t (NULL = legacy default stream).  Every call is
+ *     asynchronous and stream-ordered; argument checks run on the host before
+ *     any launch and return their status synchronously.
+ *   - Data pointers must be 16-byte aligned (MXFP4_ERR_MISALIGNED).
+ *   - No call falls back to another implementation: a shape the kernels do
+ *     not support returns MXFP4_ERR_UNSUPPORTED_SHAPE.
+ *   - Device-side waits are bounded; a wait that gives up records an error
+ *     word that mxfp4_get_device_error() returns as MXFP4_ERR_TIMEOUT.
+ */
+#ifndef MXFP4_GB300_H
+#define MXFP4_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MXFP4_API __attribute__((visibility("default")))
+#else
+#define MXFP4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MXFP4_OK = 0,
+    MXFP4_ERR_INVALID_ARG = 1,        /* null pointer, non-positive size, bad enum  */
+    MXFP4_ERR_UNSUPPORTED_SHAPE = 2,  /* e.g. odd K, leading dimension too small    */
+    MXFP4_ERR_MISALIGNED = 3,         /* pointer or leading dimension not 16-B aligned */
+    MXFP4_ERR_WORKSPACE = 4,          /* workspace missing or smaller than required */
+    MXFP4_ERR_CUDA = 5,               /* a CUDA runtime call or launch failed       */
+    MXFP4_ERR_TIMEOUT = 6,            /* a device-side wait gave up                 */
+    MXFP4_ERR_NO_DEVICE = 7           /* no usable sm_103 device is current         */
+} mxfp4_status;
+
+typedef enum {
+    MXFP4_LAYOUT_ROWMAJOR = 0,  /* codes [R][K/2], scales [R][ceil(K/32)] */
+    MXFP4_LAYOUT_TILED = 1      /* the tcgen05 tile layout described above */
+} mxfp4_layout;
+
+typedef enum {
+    MXFP4_OUT_BMN = 0,  /* out[b][m][n]  (K-up projection)                    */
+    MXFP4_OUT_MBN = 1   /* out[m][b][n]  (V-up projection, batch-major write) */
+} mxfp4_bmm_out_layout;
+
+/* Version of this ABI (increments on incompatible change). */
+MXFP4_API int mxfp4_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+MXFP4_API const char* mxfp4_status_string(mxfp4_status status);
+
+/*
+ * Bytes of the packed weight buffer for `batch` matrices of N rows x K
+ * elements: batch * (Np*Kp/2 + Np*Kp/32).  Returns 0 when an argument is
+ * not positive or K is odd.
+ */
+MXFP4_API size_t mxfp4_packed_weight_bytes(int batch, int N, int K);
+
+/*
+ * One-time repack of FP4 weights into the TILED layout — the counterpart of
+ * the pages' process_weights_after_loading step, which swizzles the E8M0
+ * weight scales into AITER's tile order and preshuffles the FP4 weights
+ * (PR #39598 blog analysis, section 2: _swizzle_asm_fp4_scale,
+ * shuffle_weight).  Unlike the pages' gate (rows % 32, scale cols % 8,
+ * N > 128) every shape is accepted: rows and K are padded instead.
+ *
+ *   w_codes_dev   [batch][N][K/2] uint8, row-major, contiguous
+ *   w_scales_dev  [batch][N][ceil(K/32)] uint8, row-major, contiguous
+ *   packed_dev    mxfp4_packed_weight_bytes(batch, N, K) bytes (output)
+ * Deterministic and idempotent.  Errors: INVALID_ARG, UNSUPPORTED_SHAPE
+ * (odd K), MISALIGNED, CUDA.
+ */
+MXFP4_API mxfp4_status mxfp4_pack_weights(const uint8_t* w_codes_dev, const uint8_t* w_scales_dev,
+                                int batch, int N, int K, void* packed_dev, void* stream);
+
+/* Bytes of the activation codes / scales buffers for M rows x K elements. */
+MXFP4_API size_t mxfp4_act_code_bytes(int M, int K, mxfp4_layout layout);
+MXFP4_API size_t mxfp4_act_scale_bytes(int M, int K, mxfp4_layout layout);
+
+/*
+ * Per-1x32 MXFP4 quantization of bf16 activations — the pages'
+ * per_1x32_f4_quant (PR #39598 blog analysis, section 2,
+ * _aiter_per_1x32_f4_quant and its fake implementation for shapes).
+ * For each block of 32 elements of a row: amax = max|x|; scale byte =
+ * max(biased_exponent(amax) - 2, 0), i.e. the OCP MX exponent
+ * floor(log2 amax) - 2 clamped to E8M0; each element is divided by the scale
+ * and rounded to the nearest E2M1 value, ties to even, saturating at +-6,
+ * keeping the input's sign bit (so -0 encodes as 0x8).  A block holding
+ * Inf/NaN gets scale 0xFF and codes 0.  No flush of subnormal inputs.
+ *
+ *   x_dev       bf16 [M][ldx], ldx >= K (elements)
+ *   codes_dev   mxfp4_act_code_bytes(M, K, layout) bytes (output)
+ *   scales_dev  mxfp4_act_scale_bytes(M, K, layout) bytes (output)
+ * K must be even.  Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA.
+ */
+MXFP4_API mxfp4_status mxfp4_quant_act(const void* x_dev, int M, int K, int ldx,
+                             uint8_t* codes_dev, uint8_t* scales_dev,
+                             mxfp4_layout layout, void* stream);
+
+/* Workspace bytes mxfp4_gemm needs for this problem (any input form). */
+MXFP4_API size_t mxfp4_gemm_workspace_bytes(int M, int N, int K);
+
+/*
+ * W4A4 MXFP4 GEMM with fused bias — the pages' gemm_a4w4 followed by
+ * `y + bias` (PR #39598 blog analysis, section 2, apply_weights):
+ *   out[m][n] = bf16_RNE( sum_k deq(A)[m][k] * deq(W)[n][k] + bias[n] )
+ * with deq(c, s) = e2m1(c) * 2^(s-127), fp32 accumulation on the tcgen05
+ * block-scaled tensor cores, one rounding to bf16.
+ *
+ * Activation input, exactly one of:
+ *   a_bf16_dev != NULL: bf16 [M][lda] (lda >= K), quantized inside the call
+ *                       (the pages' apply_weights path); a_codes/a_scales NULL;
+ *   a_bf16_dev == NULL: pre-quantized codes/scales in `a_layout` (the pages'
+ *                       (x_fp4, x_scales) tuple input); ROWMAJOR scales are
+ *                       re-laid out inside the call.
+ *   w_packed_dev   output of mxfp4_pack_weights(batch = 1, N, K)
+ *   bias_dev       bf16 [N] or NULL
+ *   out_dev        bf16 [M][ldo], ldo >= N
+ *   workspace_dev  >= mxfp4_gemm_workspace_bytes(M, N, K) bytes of device
+ *                  scratch owned by the caller; contents need not be
+ *                  initialised and are clobbered.
+ * Calls sharing one workspace must be ordered on the GPU.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, WORKSPACE, CUDA.
+ */
+MXFP4_API mxfp4_status mxfp4_gemm(const void* a_bf16_dev, int lda,
+                        const uint8_t* a_codes_dev, const uint8_t* a_scales_dev,
+                        mxfp4_layout a_layout,
+                        const void* w_packed_dev, const void* bias_dev,
+                        void* out_dev, int ldo, int M, int N, int K,
+                        void* workspace_dev, size_t workspace_bytes, void* stream);
+
+/*
+ * A16WFP4 batched matmul for the MLA absorbed K-up / V-up projections
+ * (PR #34317, Modifications): bf16 activations against FP4 weights with E8M0
+ * scales, no activation quantization:
+ *   r[b][m][n] = bf16_RNE( sum_k x[b][m][k] * deq(W_b)[n][k] ), fp32 accumulation
+ *   out_layout BMN: out[b][m][n] = r;  MBN: out[m][b][n] = r (V-up written
+ *   batch-major directly, no separate transpose).
+ *
+ *   x_dev         bf16 [B][M][K], contiguous
+ *   w_packed_dev  output of mxfp4_pack_weights(B, N, K)
+ *   out_dev       bf16, B*M*N elements in out_layout order
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA.
+ */
+MXFP4_API mxfp4_status a16wfp4_bmm(const void* x_dev, const void* w_packed_dev, void* out_dev,
+                         int B, int M, int N, int K, mxfp4_bmm_out_layout out_layout,
+                         void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device error
+ * words on the current device.  Returns MXFP4_ERR_TIMEOUT if a kernel gave
+ * up a bounded wait since the last call, MXFP4_OK otherwise (or
+ * MXFP4_ERR_CUDA if the synchronisation itself failed).
+ */
+MXFP4_API mxfp4_status mxfp4_get_device_error(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP4_GB300_H */

@@ -1,0 +1,127 @@
+"""ctypes binding of ``libmxfp4_gb300.so`` (declared in ``include/mxfp4.h``).
+
+Argument marshalling only: every computation runs in the library's CUDA
+kernels.  Arguments that are device buffers accept a torch tensor (its
+``data_ptr()``) or a raw integer address; ``stream`` accepts a
+``torch.cuda.Stream``, a raw ``cudaStream_t`` integer, or ``None`` for torch's
+current stream on the current device.  A non-OK status raises
+``Mxfp4Error``.  Importing this module fails loudly when the library has not
+been built (``python -m mxfp4_quantized_gemm_gb300.build``).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmxfp4_gb300.so")
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(
+        f"{_LIB_PATH} is missing: build it with `python -m mxfp4_quantized_gemm_gb300.build` "
+        "(there is no CPU fallback)")
+lib = ctypes.CDLL(_LIB_PATH)
+
+# status codes (mxfp4_status)
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT, \
+    ERR_NO_DEVICE = range(8)
+LAYOUT_ROWMAJOR, LAYOUT_TILED = 0, 1
+OUT_BMN, OUT_MBN = 0, 1
+
+_p, _i, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+
+_SIGNATURES = {
+    "mxfp4_abi_version": (_i, []),
+    "mxfp4_status_string": (ctypes.c_char_p, [_i]),
+    "mxfp4_packed_weight_bytes": (_sz, [_i, _i, _i]),
+    "mxfp4_pack_weights": (_i, [_p, _p, _i, _i, _i, _p, _p]),
+    "mxfp4_act_code_bytes": (_sz, [_i, _i, _i]),
+    "mxfp4_act_scale_bytes": (_sz, [_i, _i, _i]),
+    "mxfp4_quant_act": (_i, [_p, _i, _i, _i, _p, _p, _i, _p]),
+    "mxfp4_gemm_workspace_bytes": (_sz, [_i, _i, _i]),
+    "mxfp4_gemm": (_i, [_p, _i, _p, _p, _i, _p, _p, _p, _i, _i, _i, _i, _p, _sz, _p]),
+    "a16wfp4_bmm": (_i, [_p, _p, _p, _i, _i, _i, _i, _i, _p]),
+    "mxfp4_get_device_error": (_i, [_p]),
+}
+for _name, (_res, _args) in _SIGNATURES.items():
+    _fn = getattr(lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+class Mxfp4Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {lib.mxfp4_status_string(status).decode()}")
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(status: int, where: str) -> None:
+    if status != OK:
+        raise Mxfp4Error(status, where)
+
+
+def mxfp4_abi_version() -> int:
+    return lib.mxfp4_abi_version()
+
+
+def mxfp4_status_string(status: int) -> str:
+    return lib.mxfp4_status_string(status).decode()
+
+
+def mxfp4_packed_weight_bytes(batch: int, N: int, K: int) -> int:
+    return lib.mxfp4_packed_weight_bytes(batch, N, K)
+
+
+def mxfp4_act_code_bytes(M: int, K: int, layout: int) -> int:
+    return lib.mxfp4_act_code_bytes(M, K, layout)
+
+
+def mxfp4_act_scale_bytes(M: int, K: int, layout: int) -> int:
+    return lib.mxfp4_act_scale_bytes(M, K, layout)
+
+
+def mxfp4_gemm_workspace_bytes(M: int, N: int, K: int) -> int:
+    return lib.mxfp4_gemm_workspace_bytes(M, N, K)
+
+
+def mxfp4_pack_weights(w_codes, w_scales, batch: int, N: int, K: int, packed, stream=None) -> None:
+    _check(lib.mxfp4_pack_weights(_ptr(w_codes), _ptr(w_scales), batch, N, K, _ptr(packed), _stream(stream)),
+           "mxfp4_pack_weights")
+
+
+def mxfp4_quant_act(x, M: int, K: int, ldx: int, codes, scales, layout: int, stream=None) -> None:
+    _check(lib.mxfp4_quant_act(_ptr(x), M, K, ldx, _ptr(codes), _ptr(scales), layout, _stream(stream)),
+           "mxfp4_quant_act")
+
+
+def mxfp4_gemm(a_bf16, lda: int, a_codes, a_scales, a_layout: int, w_packed, bias, out, ldo: int,
+               M: int, N: int, K: int, workspace, workspace_bytes: int, stream=None) -> None:
+    _check(lib.mxfp4_gemm(_ptr(a_bf16), lda, _ptr(a_codes), _ptr(a_scales), a_layout, _ptr(w_packed),
+                          _ptr(bias), _ptr(out), ldo, M, N, K, _ptr(workspace), workspace_bytes,
+                          _stream(stream)),
+           "mxfp4_gemm")
+
+
+def a16wfp4_bmm(x, w_packed, out, B: int, M: int, N: int, K: int, out_layout: int, stream=None) -> None:
+    _check(lib.a16wfp4_bmm(_ptr(x), _ptr(w_packed), _ptr(out), B, M, N, K, out_layout, _stream(stream)),
+           "a16wfp4_bmm")
+
+
+def mxfp4_get_device_error(stream=None) -> int:
+    return lib.mxfp4_get_device_error(_stream(stream))

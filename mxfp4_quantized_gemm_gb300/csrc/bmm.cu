@@ -1,0 +1,308 @@
+// A16WFP4 batched matmul for the MLA absorbed K-up / V-up projections of
+// sglang PR #34317 "[AMD] [GLM5] use tuned MXFP4 kernels for MLA absorbed
+// BMM" (Modifications): bf16 activations against FP4 weights with E8M0
+// scales, the V-up result written batch-major [M, B, N] directly.
+//
+//   r[b][m][n] = bf16_RNE( sum_k x[b][m][k] * deq(W_b)[n][k] )
+//
+// One CTA owns (batch b, a tile of BN weight rows) and loops over the M
+// tiles.  Its weight tile is dequantized once into shared memory as bf16 in
+// the 128-byte-swizzled K-major operand image (e2m1 * 2^(s-127) is exact in
+// bf16 for every scale the format can hold except the extreme subnormals),
+// and stays resident; activations stream through a ring of 128 x 64 bf16
+// slabs fed by TMA tensor loads; one thread issues tcgen05.mma.kind::f16
+// (bf16 x bf16 -> fp32 TMEM); four warps drain the double-buffered
+// accumulator while the next M tile is multiplied.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "internal.h"
+#include "layout.cuh"
+#include "ptx.cuh"
+
+namespace mx {
+
+static __device__ uint32_t g_bmm_error;
+
+constexpr int kBmmStages = 4;
+constexpr int kSlabBytes = 128 * 128;      // 128 rows x 64 bf16
+
+struct BmmArgs {
+  const uint8_t* w_packed;
+  __nv_bfloat16* out;
+  int B, M, N, K, KS;        // KS = K / 64 slabs
+  int BN, n_tiles, m_tiles, m_per_cta;
+  size_t w_batch_bytes, w_code_bytes;
+  int KT;                    // Kp / 256 of the packed weights
+  bool batch_major;
+};
+
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Magnitude of the E2M1 code index 0..7 ({0, .5, 1, 1.5, 2, 3, 4, 6}) built
+// from its exponent and mantissa bits.
+__device__ __forceinline__ float e2m1_mag(uint32_t idx) {
+  if (idx < 2) return idx == 0 ? 0.f : 0.5f;
+  return __uint_as_float(((126u + (idx >> 1)) << 23) | ((idx & 1u) << 22));
+}
+
+// 2^(s-127) as a float for an E8M0 byte (0xFF -> NaN).
+__device__ __forceinline__ float e8m0_to_float(uint32_t s) {
+  if (s == 0xFF) return __uint_as_float(0x7FC00000u);
+  if (s == 0) return __uint_as_float(0x00400000u);   // 2^-127, a float subnormal
+  return __uint_as_float(s << 23);
+}
+
+__global__ void __launch_bounds__(192, 1) a16wfp4_bmm_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                             const BmmArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int BN = g.BN;
+  uint8_t* wsm = smem;                                       // KS slabs of BN rows x 128 B
+  uint8_t* xsm = smem + static_cast<size_t>(g.KS) * BN * 128; // ring of x slabs
+  uint64_t* full = reinterpret_cast<uint64_t*>(xsm + kBmmStages * kSlabBytes);
+  uint64_t* empty = full + kBmmStages;
+  uint64_t* acc_full = empty + kBmmStages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt = blockIdx.x % g.n_tiles;
+  const int b = blockIdx.x / g.n_tiles;
+  const int mt0 = blockIdx.y * g.m_per_cta;
+  const int mt1 = min(g.m_tiles, mt0 + g.m_per_cta);
+  const uint32_t tmem_cols = 2 * BN;
+  bool abort = false;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kBmmStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 128);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, tmem_cols);
+    tmem_relinquish();
+  }
+
+  // ---- dequantize this CTA's weight tile into the swizzled bf16 image
+  {
+    const uint8_t* wc = g.w_packed + static_cast<size_t>(b) * g.w_batch_bytes;
+    const uint8_t* ws = wc + g.w_code_bytes;
+    const int nblk = g.K >> 5;
+    const int items = BN * nblk;
+    for (int it = threadIdx.x; it < items; it += blockDim.x) {
+      const int nl = it / nblk, blk = it - nl * nblk;
+      const int n = nt * BN + nl;
+      const uint4 c = *reinterpret_cast<const uint4*>(wc + tiled_code_offset(n, blk * 16, g.KT));
+      const float sc = e8m0_to_float(ws[tiled_scale_offset(n, blk, g.KT)]);
+      const uint32_t w32[4] = {c.x, c.y, c.z, c.w};
+      uint32_t o[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const uint32_t byte = (w32[q >> 2] >> (8 * (q & 3))) & 0xFF;
+        const uint32_t lo = byte & 0xF, hi = byte >> 4;
+        const float vlo = (lo & 8) ? -(e2m1_mag(lo & 7) * sc) : e2m1_mag(lo & 7) * sc;
+        const float vhi = (hi & 8) ? -(e2m1_mag(hi & 7) * sc) : e2m1_mag(hi & 7) * sc;
+        o[q] = pack_bf16x2(vlo, vhi);
+      }
+      // 32 elements = 4 swizzled 16-byte chunks of one slab row
+      const int k0 = blk * 32;
+      const int slab = k0 >> 6;
+      const int chunk0 = (k0 & 63) >> 3;
+      uint8_t* row = wsm + static_cast<size_t>(slab) * BN * 128 + nl * 128;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const int phys = (chunk0 + cc) ^ (nl & 7);
+        *reinterpret_cast<uint4*>(row + phys * 16) = make_uint4(o[4 * cc], o[4 * cc + 1], o[4 * cc + 2], o[4 * cc + 3]);
+      }
+    }
+    fence_proxy_async_smem();   // generic-proxy writes -> visible to the tensor core
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---- producer: x slabs by TMA
+    uint32_t ls = 0;
+    for (int mt = mt0; mt < mt1; ++mt) {
+      for (int ks = 0; ks < g.KS; ++ks, ++ls) {
+        const int s = ls % kBmmStages;
+        const uint32_t ph = (ls / kBmmStages) & 1;
+        if (!mbar_wait(&empty[s], ph ^ 1, abort)) break;
+        mbar_arrive_expect_tx(&full[s], kSlabBytes);
+        tma_load_3d(xsm + s * kSlabBytes, &xmap, ks * 64, mt * 128, b, &full[s]);
+      }
+      if (abort) break;
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA issuer
+    uint32_t ls = 0;
+    const uint32_t idesc = idesc_bf16(128, BN);
+    const uint32_t wbase = smem_u32(wsm);
+    for (int mt = mt0, i = 0; mt < mt1 && !abort; ++mt, ++i) {
+      const int buf = i & 1;
+      const uint32_t use = i >> 1;
+      if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort)) break;
+      tc_fence_after();
+      const uint32_t acc = tmem + buf * BN;
+      for (int ks = 0; ks < g.KS; ++ks, ++ls) {
+        const int s = ls % kBmmStages;
+        const uint32_t ph = (ls / kBmmStages) & 1;
+        if (!mbar_wait(&full[s], ph, abort)) break;
+        tc_fence_after();
+        const uint32_t xs = smem_u32(xsm + s * kSlabBytes);
+        const uint32_t wsl = wbase + static_cast<uint32_t>(ks) * BN * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          mma_bf16(acc, sdesc_sw128(xs + 32 * j), sdesc_sw128(wsl + 32 * j), idesc, (ks | j) != 0);
+        mma_commit(&empty[s]);
+      }
+      mma_commit(&acc_full[buf]);
+    }
+  } else if (warp >= 2) {
+    // ---- epilogue
+    const int q = warp & 3;
+    for (int mt = mt0, i = 0; mt < mt1; ++mt, ++i) {
+      const int buf = i & 1;
+      const uint32_t use = i >> 1;
+      const bool ok = mbar_wait(&acc_full[buf], use & 1, abort);
+      tc_fence_after();
+      const int m = mt * 128 + q * 32 + lane;
+      __nv_bfloat16* dst_row =
+          g.batch_major ? g.out + (static_cast<size_t>(m) * g.B + b) * g.N + nt * BN
+                        : g.out + (static_cast<size_t>(b) * g.M + m) * g.N + nt * BN;
+      if (ok) {
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          uint32_t r[16];
+          tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + c0, r);
+          tmem_wait_ld();
+          const int n0 = nt * BN + c0;
+          if (m < g.M && n0 < g.N) {
+            __nv_bfloat16* dst = dst_row + c0;
+            if (n0 + 16 <= g.N && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+              uint4 w0, w1;
+              w0.x = pack_bf16x2(__uint_as_float(r[0]), __uint_as_float(r[1]));
+              w0.y = pack_bf16x2(__uint_as_float(r[2]), __uint_as_float(r[3]));
+              w0.z = pack_bf16x2(__uint_as_float(r[4]), __uint_as_float(r[5]));
+              w0.w = pack_bf16x2(__uint_as_float(r[6]), __uint_as_float(r[7]));
+              w1.x = pack_bf16x2(__uint_as_float(r[8]), __uint_as_float(r[9]));
+              w1.y = pack_bf16x2(__uint_as_float(r[10]), __uint_as_float(r[11]));
+              w1.z = pack_bf16x2(__uint_as_float(r[12]), __uint_as_float(r[13]));
+              w1.w = pack_bf16x2(__uint_as_float(r[14]), __uint_as_float(r[15]));
+              reinterpret_cast<uint4*>(dst)[0] = w0;
+              reinterpret_cast<uint4*>(dst)[1] = w1;
+            } else {
+              for (int e = 0; e < 16; ++e)
+                if (n0 + e < g.N) dst[e] = __float2bfloat16_rn(__uint_as_float(r[e]));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[buf]);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tmem_cols);
+  }
+  if (abort) atomicOr(&g_bmm_error, kErrTimeout);
+}
+
+// ------------------------------------------------------------------ host
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+static bool g_bmm_attr[64];
+
+cudaError_t launch_bmm(const void* x, const uint8_t* w_packed, void* out, int B, int M, int N, int K,
+                       bool batch_major, const DeviceInfo& dev, cudaStream_t s) {
+  auto encode = tensor_map_encoder();
+  if (encode == nullptr) return cudaErrorNotSupported;
+
+  BmmArgs a{};
+  a.w_packed = w_packed;
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.B = B;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.KS = K / 64;
+  const int64_t Np = padded_rows(N), Kp = padded_k(K);
+  a.KT = static_cast<int>(Kp / kKTile);
+  a.w_code_bytes = static_cast<size_t>(Np * Kp / 2);
+  a.w_batch_bytes = a.w_code_bytes + static_cast<size_t>(Np * Kp / 32);
+  // widest weight tile whose bf16 image fits in 128 KiB (and divides Np)
+  int BN = 256;
+  while (BN > 64 && (static_cast<int64_t>(BN) * K * 2 > 128 * 1024 || Np % BN != 0)) BN /= 2;
+  a.BN = BN;
+  a.n_tiles = static_cast<int>(Np / BN);
+  a.m_tiles = static_cast<int>(ceil_div(M, 128));
+  const int pairs = B * a.n_tiles;
+  int m_groups = dev.sm_count / pairs;
+  if (m_groups < 1) m_groups = 1;
+  if (m_groups > a.m_tiles) m_groups = a.m_tiles;
+  a.m_per_cta = static_cast<int>(ceil_div(a.m_tiles, m_groups));
+  m_groups = static_cast<int>(ceil_div(a.m_tiles, a.m_per_cta));
+  a.batch_major = batch_major;
+
+  CUtensorMap map;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(M) * K * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(x), dims, strides, box, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+
+  const int smem = a.KS * BN * 128 + kBmmStages * kSlabBytes + 1024 + 256;
+  if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+  if (!g_bmm_attr[dev.device]) {
+    cudaError_t e = cudaFuncSetAttribute(a16wfp4_bmm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         227 * 1024);
+    if (e != cudaSuccess) return e;
+    g_bmm_attr[dev.device] = true;
+  }
+  dim3 grid(static_cast<unsigned>(pairs), static_cast<unsigned>(m_groups));
+  a16wfp4_bmm_kernel<<<grid, 192, smem, s>>>(map, a);
+  return cudaGetLastError();
+}
+
+uint32_t bmm_read_clear_error() {
+  uint32_t v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_bmm_error, sizeof(v)) != cudaSuccess) return 0;
+  cudaMemcpyToSymbol(g_bmm_error, &zero, sizeof(zero));
+  return v;
+}
+
+}  // namespace mx

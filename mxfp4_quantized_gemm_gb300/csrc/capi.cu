@@ -1,0 +1,214 @@
+// C ABI of the library (declared in include/mxfp4.h): argument checks on
+// the host, workspace carving, dispatch to the kernels of quant.cu, gemm.cu
+// and bmm.cu.  No entry point allocates device memory.
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "../../include/mxfp4.h"
+#include "internal.h"
+
+namespace mx {
+
+static DeviceInfo g_dev_cache[64];
+static bool g_dev_cached[64];
+
+cudaError_t current_device_info(DeviceInfo* out) {
+  int d = -1;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return e;
+  if (d < 0 || d >= 64) return cudaErrorInvalidDevice;
+  if (!g_dev_cached[d]) {
+    DeviceInfo info{d, 0, false};
+    int major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&info.sm_count, cudaDevAttrMultiProcessorCount, d)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, d)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, d)) != cudaSuccess) return e;
+    info.ok = (major == 10 && minor == 3);
+    g_dev_cache[d] = info;
+    g_dev_cached[d] = true;
+  }
+  *out = g_dev_cache[d];
+  return cudaSuccess;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+static size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Device check shared by every compute entry point.
+static mxfp4_status device_ready(DeviceInfo* dev) {
+  cudaError_t e = current_device_info(dev);
+  if (e == cudaErrorNoDevice || e == cudaErrorInsufficientDriver) return MXFP4_ERR_NO_DEVICE;
+  if (e != cudaSuccess) return MXFP4_ERR_CUDA;
+  return dev->ok ? MXFP4_OK : MXFP4_ERR_NO_DEVICE;
+}
+
+static mxfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA; }
+
+// Workspace carve-up of mxfp4_gemm: tiled activation codes, tiled scales,
+// stream-K partial sums and tickets, each 1 KiB aligned.
+struct GemmWorkspace {
+  size_t codes_off, scales_off, streamk_off, total;
+};
+static GemmWorkspace gemm_workspace_layout(int M, int N, int K) {
+  GemmWorkspace w{};
+  w.codes_off = 0;
+  w.scales_off = round_up(static_cast<size_t>(tiled_code_bytes(M, K)), 1024);
+  w.streamk_off = w.scales_off + round_up(static_cast<size_t>(tiled_scale_bytes(M, K)), 1024);
+  w.total = w.streamk_off + round_up(gemm_streamk_workspace_bytes(M, N, K), 1024);
+  return w;
+}
+
+}  // namespace mx
+
+using namespace mx;
+
+extern "C" {
+
+int mxfp4_abi_version(void) { return 1; }
+
+const char* mxfp4_status_string(mxfp4_status s) {
+  switch (s) {
+    case MXFP4_OK: return "MXFP4_OK";
+    case MXFP4_ERR_INVALID_ARG: return "MXFP4_ERR_INVALID_ARG";
+    case MXFP4_ERR_UNSUPPORTED_SHAPE: return "MXFP4_ERR_UNSUPPORTED_SHAPE";
+    case MXFP4_ERR_MISALIGNED: return "MXFP4_ERR_MISALIGNED";
+    case MXFP4_ERR_WORKSPACE: return "MXFP4_ERR_WORKSPACE";
+    case MXFP4_ERR_CUDA: return "MXFP4_ERR_CUDA";
+    case MXFP4_ERR_TIMEOUT: return "MXFP4_ERR_TIMEOUT";
+    case MXFP4_ERR_NO_DEVICE: return "MXFP4_ERR_NO_DEVICE";
+  }
+  return "MXFP4_ERR_UNKNOWN";
+}
+
+size_t mxfp4_packed_weight_bytes(int batch, int N, int K) {
+  if (batch <= 0 || N <= 0 || K <= 0 || (K & 1)) return 0;
+  return static_cast<size_t>(batch) *
+         static_cast<size_t>(tiled_code_bytes(N, K) + tiled_scale_bytes(N, K));
+}
+
+size_t mxfp4_act_code_bytes(int M, int K, mxfp4_layout layout) {
+  if (M <= 0 || K <= 0 || (K & 1)) return 0;
+  if (layout == MXFP4_LAYOUT_ROWMAJOR) return static_cast<size_t>(M) * (K / 2);
+  if (layout == MXFP4_LAYOUT_TILED) return static_cast<size_t>(tiled_code_bytes(M, K));
+  return 0;
+}
+
+size_t mxfp4_act_scale_bytes(int M, int K, mxfp4_layout layout) {
+  if (M <= 0 || K <= 0 || (K & 1)) return 0;
+  if (layout == MXFP4_LAYOUT_ROWMAJOR) return static_cast<size_t>(M) * static_cast<size_t>(ceil_div(K, 32));
+  if (layout == MXFP4_LAYOUT_TILED) return static_cast<size_t>(tiled_scale_bytes(M, K));
+  return 0;
+}
+
+mxfp4_status mxfp4_pack_weights(const uint8_t* w_codes, const uint8_t* w_scales, int batch, int N, int K,
+                                void* packed, void* stream) {
+  if (w_codes == nullptr || w_scales == nullptr || packed == nullptr) return MXFP4_ERR_INVALID_ARG;
+  if (batch <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_INVALID_ARG;
+  if (K & 1) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(packed)) return MXFP4_ERR_MISALIGNED;
+  DeviceInfo dev;
+  mxfp4_status st = device_ready(&dev);
+  if (st != MXFP4_OK) return st;
+  return from_cuda(launch_pack(w_codes, w_scales, batch, N, K, static_cast<uint8_t*>(packed), dev,
+                               static_cast<cudaStream_t>(stream)));
+}
+
+mxfp4_status mxfp4_quant_act(const void* x, int M, int K, int ldx, uint8_t* codes, uint8_t* scales,
+                             mxfp4_layout layout, void* stream) {
+  if (x == nullptr || codes == nullptr || scales == nullptr) return MXFP4_ERR_INVALID_ARG;
+  if (M <= 0 || K <= 0) return MXFP4_ERR_INVALID_ARG;
+  if (layout != MXFP4_LAYOUT_ROWMAJOR && layout != MXFP4_LAYOUT_TILED) return MXFP4_ERR_INVALID_ARG;
+  if ((K & 1) || ldx < K) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(x) & 1) != 0) return MXFP4_ERR_MISALIGNED;
+  if (layout == MXFP4_LAYOUT_TILED && (!aligned16(codes) || !aligned16(scales))) return MXFP4_ERR_MISALIGNED;
+  DeviceInfo dev;
+  mxfp4_status st = device_ready(&dev);
+  if (st != MXFP4_OK) return st;
+  return from_cuda(launch_quant(x, M, K, ldx, codes, scales, layout == MXFP4_LAYOUT_TILED, dev,
+                                static_cast<cudaStream_t>(stream)));
+}
+
+size_t mxfp4_gemm_workspace_bytes(int M, int N, int K) {
+  if (M <= 0 || N <= 0 || K <= 0 || (K & 1)) return 0;
+  return gemm_workspace_layout(M, N, K).total;
+}
+
+mxfp4_status mxfp4_gemm(const void* a_bf16, int lda, const uint8_t* a_codes, const uint8_t* a_scales,
+                        mxfp4_layout a_layout, const void* w_packed, const void* bias, void* out, int ldo, int M,
+                        int N, int K, void* workspace, size_t workspace_bytes, void* stream) {
+  if (w_packed == nullptr || out == nullptr) return MXFP4_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_INVALID_ARG;
+  const bool from_bf16 = a_bf16 != nullptr;
+  if (from_bf16 && (a_codes != nullptr || a_scales != nullptr)) return MXFP4_ERR_INVALID_ARG;
+  if (!from_bf16 && (a_codes == nullptr || a_scales == nullptr)) return MXFP4_ERR_INVALID_ARG;
+  if (!from_bf16 && a_layout != MXFP4_LAYOUT_ROWMAJOR && a_layout != MXFP4_LAYOUT_TILED)
+    return MXFP4_ERR_INVALID_ARG;
+  if ((K & 1) || ldo < N || (from_bf16 && lda < K)) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(w_packed) || !aligned16(out) || (bias != nullptr && (reinterpret_cast<uintptr_t>(bias) & 1)))
+    return MXFP4_ERR_MISALIGNED;
+  if (from_bf16 && (reinterpret_cast<uintptr_t>(a_bf16) & 1)) return MXFP4_ERR_MISALIGNED;
+  if (!from_bf16 && a_layout == MXFP4_LAYOUT_TILED && (!aligned16(a_codes) || !aligned16(a_scales)))
+    return MXFP4_ERR_MISALIGNED;
+  const GemmWorkspace wl = gemm_workspace_layout(M, N, K);
+  if (workspace == nullptr || workspace_bytes < wl.total) return MXFP4_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return MXFP4_ERR_MISALIGNED;
+
+  DeviceInfo dev;
+  mxfp4_status st = device_ready(&dev);
+  if (st != MXFP4_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+
+  GemmProblem p{};
+  if (from_bf16) {
+    p.a_codes = ws + wl.codes_off;
+    p.a_scales = ws + wl.scales_off;
+    cudaError_t e = launch_quant(a_bf16, M, K, lda, ws + wl.codes_off, ws + wl.scales_off, true, dev, s);
+    if (e != cudaSuccess) return MXFP4_ERR_CUDA;
+  } else if (a_layout == MXFP4_LAYOUT_ROWMAJOR) {
+    // the pages' pre-quantized (x_fp4, x_scales) input: re-lay out, pad scales with 0x7F
+    cudaError_t e = launch_pack(a_codes, a_scales, 1, M, K, ws + wl.codes_off, dev, s);
+    if (e != cudaSuccess) return MXFP4_ERR_CUDA;
+    p.a_codes = ws + wl.codes_off;
+    p.a_scales = ws + wl.codes_off + tiled_code_bytes(M, K);
+  } else {
+    p.a_codes = a_codes;
+    p.a_scales = a_scales;
+  }
+  p.w_packed = static_cast<const uint8_t*>(w_packed);
+  p.bias = bias;
+  p.out = out;
+  p.ldo = ldo;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.workspace = ws + wl.streamk_off;
+  p.workspace_bytes = wl.total - wl.streamk_off;
+  return from_cuda(launch_gemm(p, dev, s));
+}
+
+mxfp4_status a16wfp4_bmm(const void* x, const void* w_packed, void* out, int B, int M, int N, int K,
+                         mxfp4_bmm_out_layout out_layout, void* stream) {
+  if (x == nullptr || w_packed == nullptr || out == nullptr) return MXFP4_ERR_INVALID_ARG;
+  if (B <= 0 || M <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_INVALID_ARG;
+  if (out_layout != MXFP4_OUT_BMN && out_layout != MXFP4_OUT_MBN) return MXFP4_ERR_INVALID_ARG;
+  if (K % 64 != 0) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || !aligned16(w_packed) || !aligned16(out)) return MXFP4_ERR_MISALIGNED;
+  DeviceInfo dev;
+  mxfp4_status st = device_ready(&dev);
+  if (st != MXFP4_OK) return st;
+  return from_cuda(launch_bmm(x, static_cast<const uint8_t*>(w_packed), out, B, M, N, K,
+                              out_layout == MXFP4_OUT_MBN, dev, static_cast<cudaStream_t>(stream)));
+}
+
+mxfp4_status mxfp4_get_device_error(void* stream) {
+  DeviceInfo dev;
+  mxfp4_status st = device_ready(&dev);
+  if (st != MXFP4_OK) return st;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MXFP4_ERR_CUDA;
+  const uint32_t err = quant_read_clear_error() | gemm_read_clear_error() | bmm_read_clear_error();
+  return (err & kErrTimeout) ? MXFP4_ERR_TIMEOUT : MXFP4_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mx {
+
+// Tile geometry of the TILED layout (see include/mxfp4.h).
+constexpr int kRowTile = 128;   // rows per tile / scale atom
+constexpr int kKTile = 256;     // elements per tile along K (128 bytes of codes)
+constexpr int kTileBytes = kRowTile * kKTile / 2;   // 16384
+constexpr int kAtomBytes = 512;                     // 128 rows x 4 scales
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t padded_rows(int64_t R) { return ceil_div(R, kRowTile) * kRowTile; }
+inline int64_t padded_k(int64_t K) { return ceil_div(K, kKTile) * kKTile; }
+inline int64_t tiled_code_bytes(int64_t R, int64_t K) { return padded_rows(R) * padded_k(K) / 2; }
+inline int64_t tiled_scale_bytes(int64_t R, int64_t K) { return padded_rows(R) * padded_k(K) / 32; }
+
+// Error bits recorded in a translation unit's device error word.
+constexpr uint32_t kErrTimeout = 1u;
+
+// Largest stream-K grid the decode GEMM uses; sizes its partial-sum slots.
+constexpr int kMaxStreamKCtas = 256;
+// Largest activation row count served by the swap-AB decode kernel.
+constexpr int kDecodeMaxM = 64;
+
+struct DeviceInfo {
+  int device;
+  int sm_count;
+  bool ok;   // an sm_103 device
+};
+// Properties of the current device, cached per device.
+cudaError_t current_device_info(DeviceInfo* out);
+
+// quant.cu
+cudaError_t launch_quant(const void* x, int M, int K, int ldx, uint8_t* codes, uint8_t* scales, bool tiled,
+                         const DeviceInfo& dev, cudaStream_t s);
+cudaError_t launch_pack(const uint8_t* codes, const uint8_t* scales, int batch, int R, int K, uint8_t* packed,
+                        const DeviceInfo& dev, cudaStream_t s);
+uint32_t quant_read_clear_error();
+
+// gemm.cu
+struct GemmProblem {
+  const uint8_t* a_codes;   // TILED activation codes
+  const uint8_t* a_scales;  // TILED activation scales
+  const uint8_t* w_packed;  // packed weights (codes region then scales region)
+  const void* bias;         // bf16 [N] or null
+  void* out;                // bf16 [M][ldo]
+  int ldo, M, N, K;
+  void* workspace;          // stream-K partials + tickets
+  size_t workspace_bytes;
+};
+size_t gemm_streamk_workspace_bytes(int M, int N, int K);
+cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_t s);
+uint32_t gemm_read_clear_error();
+
+// bmm.cu
+cudaError_t launch_bmm(const void* x, const uint8_t* w_packed, void* out, int B, int M, int N, int K,
+                       bool batch_major, const DeviceInfo& dev, cudaStream_t s);
+uint32_t bmm_read_clear_error();
+
+}  // namespace mx

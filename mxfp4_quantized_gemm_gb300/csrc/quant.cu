@@ -1,0 +1,211 @@
+// Per-1x32 MXFP4 activation quantization and the one-time tile repack.
+//
+// Quantization follows the OCP MX conversion the pages' per_1x32_f4_quant
+// implements (sglang PR #39598 blog analysis, section 2): one E8M0 scale per
+// 32 K-elements with exponent floor(log2 amax) - 2, elements rounded to the
+// nearest E2M1 value (ties to even) and saturated at +-6.  The repack is the
+// Blackwell counterpart of the pages' load-time weight preshuffle and scale
+// swizzle (same section: process_weights_after_loading).
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "internal.h"
+#include "layout.cuh"
+#include "ptx.cuh"
+
+namespace mx {
+
+static __device__ uint32_t g_quant_error;
+
+// E2M1 magnitude index of a non-negative float by round-to-nearest-even on
+// the grid {0, .5, 1, 1.5, 2, 3, 4, 6}, saturating at 6.  Each comparison is
+// one midpoint of the grid; a value exactly on a midpoint goes to the
+// neighbour with the even code (the comparison is strict towards the odd
+// code: 0.25 -> 0, 0.75 -> 2, 1.25 -> 2, 1.75 -> 4, 2.5 -> 4, 3.5 -> 6, 5 -> 6).
+__device__ __forceinline__ uint32_t e2m1_magnitude(float a) {
+  return static_cast<uint32_t>(a > 0.25f) + static_cast<uint32_t>(a >= 0.75f) +
+         static_cast<uint32_t>(a > 1.25f) + static_cast<uint32_t>(a >= 1.75f) +
+         static_cast<uint32_t>(a > 2.5f) + static_cast<uint32_t>(a >= 3.5f) + static_cast<uint32_t>(a > 5.0f);
+}
+
+// One warp per unit of (row, 256 consecutive elements): lane l holds
+// elements 8l..8l+7, four lanes form one 32-element block.
+template <bool kTiled>
+__global__ void __launch_bounds__(256) quant_kernel(const uint16_t* __restrict__ x, int M, int K, int ldx,
+                                                    uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                                                    int rows, int KT, bool vec_ok) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t units = static_cast<int64_t>(rows) * KT;
+  const int nb = (K + 31) >> 5;   // scale blocks per row
+
+  for (int64_t u = warp; u < units; u += nwarps) {
+    const int r = static_cast<int>(u / KT);
+    const int kt = static_cast<int>(u - static_cast<int64_t>(r) * KT);
+    const int e0 = kt * 256 + lane * 8;
+
+    uint16_t v[8];
+    if (r < M && vec_ok && e0 + 8 <= K) {
+      const uint4 q = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(r) * ldx + e0));
+      v[0] = q.x & 0xFFFF; v[1] = q.x >> 16; v[2] = q.y & 0xFFFF; v[3] = q.y >> 16;
+      v[4] = q.z & 0xFFFF; v[5] = q.z >> 16; v[6] = q.w & 0xFFFF; v[7] = q.w >> 16;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        v[i] = (r < M && e0 + i < K) ? x[static_cast<size_t>(r) * ldx + e0 + i] : static_cast<uint16_t>(0);
+    }
+
+    // Block amax on the magnitude bits (bf16 magnitudes order like integers;
+    // Inf and NaN sort above every finite value).
+    uint32_t am = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) am = max(am, static_cast<uint32_t>(v[i] & 0x7FFF));
+    am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+    am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+
+    const uint32_t ef = am >> 7;                 // biased exponent field of amax
+    const bool nonfinite = ef == 0xFF;
+    // floor(log2 amax) - 2 as an E8M0 byte, clamped at 0 (zero / subnormal amax)
+    const uint32_t sbyte = nonfinite ? 0xFFu : (ef > 2 ? ef - 2 : 0u);
+    const float inv = __uint_as_float((254u - (nonfinite ? 0u : sbyte)) << 23);   // 2^(127 - sbyte)
+
+    uint32_t packed = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float a = __uint_as_float(static_cast<uint32_t>(v[i] & 0x7FFF) << 16) * inv;
+      uint32_t c = e2m1_magnitude(a) | ((v[i] >> 12) & 8u);
+      if (nonfinite) c = 0;
+      packed |= c << (4 * i);
+    }
+
+    const int blk = kt * 8 + (lane >> 2);
+    const bool blk_real = r < M && blk < nb;
+    const int j0 = kt * 128 + lane * 4;   // first code byte of this lane in the row
+    if (kTiled) {
+      *reinterpret_cast<uint32_t*>(codes + tiled_code_offset(r, j0, KT)) = packed;
+      if ((lane & 3) == 0) scales[tiled_scale_offset(r, blk, KT)] = blk_real ? static_cast<uint8_t>(sbyte) : 0x7F;
+    } else {
+      if (r < M) {
+        const int row_bytes = K >> 1;
+        uint8_t* dst = codes + static_cast<size_t>(r) * row_bytes + j0;
+        if (e0 + 8 <= K && (reinterpret_cast<uintptr_t>(dst) & 3) == 0) {
+          *reinterpret_cast<uint32_t*>(dst) = packed;
+        } else {
+#pragma unroll
+          for (int b = 0; b < 4; ++b)
+            if (j0 + b < row_bytes) dst[b] = static_cast<uint8_t>(packed >> (8 * b));
+        }
+        if ((lane & 3) == 0 && blk_real) scales[static_cast<size_t>(r) * nb + blk] = static_cast<uint8_t>(sbyte);
+      }
+    }
+  }
+}
+
+// Repack row-major codes into the TILED codes region: one thread per
+// 16-byte output chunk, written in storage order.
+__global__ void __launch_bounds__(256) pack_codes_kernel(const uint8_t* __restrict__ codes, int batch, int R,
+                                                         int K, uint8_t* __restrict__ packed,
+                                                         size_t per_batch, int KT, int64_t chunks_per_batch) {
+  const int row_bytes = K >> 1;
+  const int64_t total = chunks_per_batch * batch;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int b = static_cast<int>(t / chunks_per_batch);
+    const int64_t c = t - static_cast<int64_t>(b) * chunks_per_batch;
+    const int64_t tile = c >> 10;            // 128 rows x 8 chunks per tile
+    const int rem = static_cast<int>(c & 1023);
+    const int i = rem >> 3, p = rem & 7;
+    const int rt = static_cast<int>(tile / KT), kt = static_cast<int>(tile - static_cast<int64_t>(rt) * KT);
+    const int r = rt * 128 + i;
+    const int j = kt * 128 + ((p ^ (i & 7)) << 4);
+    uint4 val = make_uint4(0, 0, 0, 0);
+    if (r < R && j < row_bytes) {
+      const uint8_t* src = codes + (static_cast<size_t>(b) * R + r) * row_bytes + j;
+      if (j + 16 <= row_bytes && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+        val = __ldg(reinterpret_cast<const uint4*>(src));
+      } else {
+        uint8_t tmp[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) tmp[q] = (j + q < row_bytes) ? src[q] : static_cast<uint8_t>(0);
+        val.x = tmp[0] | (tmp[1] << 8) | (tmp[2] << 16) | (static_cast<uint32_t>(tmp[3]) << 24);
+        val.y = tmp[4] | (tmp[5] << 8) | (tmp[6] << 16) | (static_cast<uint32_t>(tmp[7]) << 24);
+        val.z = tmp[8] | (tmp[9] << 8) | (tmp[10] << 16) | (static_cast<uint32_t>(tmp[11]) << 24);
+        val.w = tmp[12] | (tmp[13] << 8) | (tmp[14] << 16) | (static_cast<uint32_t>(tmp[15]) << 24);
+      }
+    }
+    *reinterpret_cast<uint4*>(packed + static_cast<size_t>(b) * per_batch + static_cast<size_t>(c) * 16) = val;
+  }
+}
+
+// Repack row-major scales into the TILED scales region: one thread per
+// output byte, in storage order; padding gets 0x7F.
+__global__ void __launch_bounds__(256) pack_scales_kernel(const uint8_t* __restrict__ scales, int batch, int R,
+                                                          int K, uint8_t* __restrict__ packed, size_t per_batch,
+                                                          size_t code_bytes, int KT, int64_t bytes_per_batch) {
+  const int nb = (K + 31) >> 5;
+  const int64_t total = bytes_per_batch * batch;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int b = static_cast<int>(t / bytes_per_batch);
+    const int64_t o = t - static_cast<int64_t>(b) * bytes_per_batch;
+    const int64_t atom = o >> 9;
+    const int w = static_cast<int>(o & 511);
+    const int i = (w >> 4) + 32 * ((w >> 2) & 3);
+    const int rt = static_cast<int>(atom / (2 * KT));
+    const int g = static_cast<int>(atom - static_cast<int64_t>(rt) * 2 * KT);
+    const int r = rt * 128 + i, blk = g * 4 + (w & 3);
+    const uint8_t val = (r < R && blk < nb) ? scales[(static_cast<size_t>(b) * R + r) * nb + blk] : 0x7F;
+    packed[static_cast<size_t>(b) * per_batch + code_bytes + static_cast<size_t>(o)] = val;
+  }
+}
+
+static int grid_for(int64_t work_items, int per_block, const DeviceInfo& dev) {
+  int64_t blocks = (work_items + per_block - 1) / per_block;
+  const int64_t cap = static_cast<int64_t>(dev.sm_count) * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return static_cast<int>(blocks);
+}
+
+cudaError_t launch_quant(const void* x, int M, int K, int ldx, uint8_t* codes, uint8_t* scales, bool tiled,
+                         const DeviceInfo& dev, cudaStream_t s) {
+  const bool vec_ok = (reinterpret_cast<uintptr_t>(x) & 15) == 0 && (ldx % 8) == 0;
+  if (tiled) {
+    const int rows = static_cast<int>(padded_rows(M));
+    const int KT = static_cast<int>(padded_k(K) / kKTile);
+    const int grid = grid_for(static_cast<int64_t>(rows) * KT, 8, dev);
+    quant_kernel<true><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x), M, K, ldx, codes, scales, rows, KT,
+                                            vec_ok);
+  } else {
+    const int KT = static_cast<int>(ceil_div(K, kKTile));
+    const int grid = grid_for(static_cast<int64_t>(M) * KT, 8, dev);
+    quant_kernel<false><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x), M, K, ldx, codes, scales, M, KT,
+                                             vec_ok);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack(const uint8_t* codes, const uint8_t* scales, int batch, int R, int K, uint8_t* packed,
+                        const DeviceInfo& dev, cudaStream_t s) {
+  const int64_t cb = tiled_code_bytes(R, K), sb = tiled_scale_bytes(R, K);
+  const size_t per_batch = static_cast<size_t>(cb + sb);
+  const int KT = static_cast<int>(padded_k(K) / kKTile);
+  const int64_t chunks = cb / 16;
+  pack_codes_kernel<<<grid_for(chunks * batch, 256, dev), 256, 0, s>>>(codes, batch, R, K, packed, per_batch, KT,
+                                                                       chunks);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  pack_scales_kernel<<<grid_for(sb * batch, 256, dev), 256, 0, s>>>(scales, batch, R, K, packed, per_batch,
+                                                                    static_cast<size_t>(cb), KT, sb);
+  return cudaGetLastError();
+}
+
+uint32_t quant_read_clear_error() {
+  uint32_t v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_quant_error, sizeof(v)) != cudaSuccess) return 0;
+  cudaMemcpyToSymbol(g_quant_error, &zero, sizeof(zero));
+  return v;
+}
+
+}  // namespace mx

@@ -1,0 +1,101 @@
+"""The C-ABI library builds, loads, exports every declared symbol, and checks
+its arguments on the host (CPU only: no compute call is made)."""
+
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mxfp4.h")
+
+
+@pytest.fixture(scope="module")
+def capi():
+    from mxfp4_quantized_gemm_gb300 import build
+    build.build()
+    from mxfp4_quantized_gemm_gb300 import capi as c
+    return c
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b((?:mxfp4|a16wfp4)_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_path(capi):
+    names = declared_functions()
+    for must in ("mxfp4_pack_weights", "mxfp4_quant_act", "mxfp4_gemm", "a16wfp4_bmm"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(capi):
+    for name in declared_functions():
+        assert hasattr(capi.lib, name), name
+
+
+def test_abi_version_and_status_strings(capi):
+    assert capi.mxfp4_abi_version() == 1
+    for s in range(8):
+        assert capi.mxfp4_status_string(s).startswith("MXFP4_")
+    assert capi.mxfp4_status_string(99) == "MXFP4_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("B,N,K", [(1, 1024, 5120), (1, 1000, 5152), (64, 512, 192), (3, 5, 40)])
+def test_packed_size_matches_layout_statement(capi, B, N, K):
+    from oracle import tile_layout as tl
+    assert capi.mxfp4_packed_weight_bytes(B, N, K) == B * tl.packed_bytes(N, K)
+
+
+def test_size_queries(capi):
+    from oracle import tile_layout as tl
+    assert capi.mxfp4_act_code_bytes(16, 5120, capi.LAYOUT_ROWMAJOR) == 16 * 2560
+    assert capi.mxfp4_act_scale_bytes(16, 5120, capi.LAYOUT_ROWMAJOR) == 16 * 160
+    assert capi.mxfp4_act_scale_bytes(3, 5152, capi.LAYOUT_ROWMAJOR) == 3 * 161
+    assert capi.mxfp4_act_code_bytes(17, 5152, capi.LAYOUT_TILED) == tl.code_bytes(17, 5152)
+    assert capi.mxfp4_act_scale_bytes(17, 5152, capi.LAYOUT_TILED) == tl.scale_bytes(17, 5152)
+    for bad in [(0, 32), (4, 0), (4, 33), (-1, 32)]:
+        assert capi.mxfp4_act_code_bytes(*bad, capi.LAYOUT_ROWMAJOR) == 0
+    assert capi.mxfp4_act_code_bytes(4, 32, 7) == 0
+    assert capi.mxfp4_packed_weight_bytes(0, 4, 32) == 0
+    assert capi.mxfp4_packed_weight_bytes(1, 4, 31) == 0
+    assert capi.mxfp4_gemm_workspace_bytes(16, 1024, 5120) >= tl.code_bytes(16, 5120) + tl.scale_bytes(16, 5120)
+    assert capi.mxfp4_gemm_workspace_bytes(0, 1, 32) == 0
+
+
+def test_argument_checks_precede_any_launch(capi):
+    lib = capi.lib
+    A = 1 << 20   # a 16-byte aligned fake address: never dereferenced, checks fail first
+    # null pointers
+    assert lib.mxfp4_pack_weights(None, A, 1, 4, 32, A, None) == capi.ERR_INVALID_ARG
+    assert lib.mxfp4_quant_act(None, 4, 32, 32, A, A, 0, None) == capi.ERR_INVALID_ARG
+    assert lib.a16wfp4_bmm(A, None, A, 1, 1, 1, 64, 0, None) == capi.ERR_INVALID_ARG
+    # non-positive sizes, bad enums
+    assert lib.mxfp4_quant_act(A, 0, 32, 32, A, A, 0, None) == capi.ERR_INVALID_ARG
+    assert lib.mxfp4_quant_act(A, 4, 32, 32, A, A, 5, None) == capi.ERR_INVALID_ARG
+    assert lib.a16wfp4_bmm(A, A, A, 1, 1, 1, 64, 3, None) == capi.ERR_INVALID_ARG
+    # odd K, ld too small, K not a multiple of 64 for the BMM
+    assert lib.mxfp4_pack_weights(A, A, 1, 4, 33, A, None) == capi.ERR_UNSUPPORTED_SHAPE
+    assert lib.mxfp4_quant_act(A, 4, 32, 16, A, A, 0, None) == capi.ERR_UNSUPPORTED_SHAPE
+    assert lib.a16wfp4_bmm(A, A, A, 1, 1, 1, 96, 0, None) == capi.ERR_UNSUPPORTED_SHAPE
+    # misaligned
+    assert lib.mxfp4_pack_weights(A, A, 1, 4, 32, A + 8, None) == capi.ERR_MISALIGNED
+    assert lib.a16wfp4_bmm(A + 4, A, A, 1, 1, 1, 64, 0, None) == capi.ERR_MISALIGNED
+    # gemm: both or neither activation forms, workspace too small
+    ws = capi.mxfp4_gemm_workspace_bytes(4, 8, 64)
+    assert lib.mxfp4_gemm(A, 64, A, A, 0, A, None, A, 8, 4, 8, 64, A, ws, None) == capi.ERR_INVALID_ARG
+    assert lib.mxfp4_gemm(None, 0, None, None, 0, A, None, A, 8, 4, 8, 64, A, ws, None) == capi.ERR_INVALID_ARG
+    assert lib.mxfp4_gemm(A, 64, None, None, 0, A, None, A, 8, 4, 8, 64, A, ws - 1, None) == capi.ERR_WORKSPACE
+    assert lib.mxfp4_gemm(A, 64, None, None, 0, A, None, A, 8, 4, 8, 64, None, ws, None) == capi.ERR_WORKSPACE
+    assert lib.mxfp4_gemm(A, 64, None, None, 0, A, None, A, 4, 4, 8, 64, A, ws, None) == capi.ERR_UNSUPPORTED_SHAPE
+    assert lib.mxfp4_gemm(A, 64, None, None, 0, A + 2, None, A, 8, 4, 8, 64, A, ws, None) == capi.ERR_MISALIGNED
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device answer")
+def test_valid_call_without_device_reports_no_device(capi):
+    A = 1 << 20
+    st = capi.lib.mxfp4_quant_act(A, 4, 32, 32, A, A, 0, None)
+    assert st in (capi.ERR_NO_DEVICE, capi.ERR_CUDA)
