@@ -1,0 +1,555 @@
+#!/usr/bin/env python3
+"""Benchmark of the MXFP4 dense linear on GB300.
+
+Headline workload (the decode sweep): M in {1, 4, 16, 32, 64} x (N, K) in
+{(14336, 5120), (5120, 14336), (34816, 5120)}: bf16 activations ~N(0,1) with
+1% outlier channels (x20), FP4 weights with E8M0 scales 2^U{-8..2}, bf16 out.
+One step runs the whole path once per case: per-1x32 activation quantization
+then the W4A4 GEMM (weights repacked once at load time, off the clock).
+
+Metric: weight-stream GB/s = algorithmic bytes (packed weights + bf16
+activations + bf16 outputs) / time.  Every case of a step reads its own
+copy of the packed weights (15 distinct buffers, 0.87 GB), so no weight is
+re-read from L2 between uses.
+
+The timed region is the replay of CUDA graphs holding the steps; external
+CUDA events around every GEMM launch give the GEMM kernel's own duration for
+the roofline.  `e2e` repeats the step through the public API with the
+activations copied from pinned host memory and the outputs read back.
+Secondary lines: prefill TFLOPS (M in {2048, 8192}, with bias) and the
+A16WFP4 BMM.  `--impl reference` times the CPU oracle on the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DECODE_MS = (1, 4, 16, 32, 64)
+DECODE_NK = ((14336, 5120), (5120, 14336), (34816, 5120))
+PREFILL_MS = (2048, 8192)
+W_SCALE_DECODE = (-8, 2)
+W_SCALE_PREFILL = (-6, 0)
+FP4_OVER_BF16 = 6.0            # nominal dense FP4 / BF16 tensor throughput on GB300 (13.5 / 2.25 PF)
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+METRIC = "MXFP4 GEMM TFLOPS (prefill) & weight-stream GB/s (decode M<=64), 1xGB300"
+
+
+def ceil_div(a, b):
+    return -(-a // b)
+
+
+def linear_bytes(M, N, K):
+    """Algorithmic bytes of one dense-linear call fed bf16 activations."""
+    return N * K // 2 + N * ceil_div(K, 32) + M * K * 2 + M * N * 2
+
+
+def gemm_kernel_bytes(M, N, K):
+    """Algorithmic bytes of the GEMM kernel alone (activations already quantized)."""
+    return N * K // 2 + N * ceil_div(K, 32) + M * K // 2 + M * ceil_div(K, 32) + M * N * 2
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("gemm.cu", "ptx.cuh", "internal.h"):
+        h.update(open(os.path.join(ROOT, "mxfp4_quantized_gemm_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per GEMM launch from the committed ncu summary, if taken on this source."""
+    p = os.path.join(ROOT, "profiles", "decode_gemm_traffic.txt")
+    try:
+        fields = {}
+        for line in open(p):
+            if "=" in line and not line.startswith("#"):
+                k, v = line.split("=", 1)
+                fields[k.strip()] = v.strip()
+        if fields.get("source_hash") == kernel_source_hash():
+            return float(fields["dram_bytes_per_step_gemm"])
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        self.proc.wait()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [v for v in sm if v > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ dist
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def dist_max(value: float, world: int) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ ours
+def make_event(torch, external):
+    try:
+        return torch.cuda.Event(enable_timing=True, external=external)
+    except TypeError:
+        return torch.cuda.Event(enable_timing=True)
+
+
+def run_ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from mxfp4_quantized_gemm_gb300 import capi, synth
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    hbm_peak, bf16_peak, bf16_sust, peak_src = load_peaks()
+
+    def to_dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    # ---- packed weights: one distinct copy per case (15 buffers)
+    cases = []
+    for M in DECODE_MS:
+        for (N, K) in DECODE_NK:
+            cases.append((M, N, K))
+    packed_master = {}
+    for (N, K) in DECODE_NK:
+        wc = synth.weight_codes(N, K, seed=0, tensor_id=2)
+        ws = synth.weight_scales(N, K, *W_SCALE_DECODE, seed=0, tensor_id=3)
+        buf = torch.empty(capi.mxfp4_packed_weight_bytes(1, N, K), dtype=torch.uint8, device=dev)
+        capi.mxfp4_pack_weights(to_dev(wc), to_dev(ws), 1, N, K, buf)
+        packed_master[(N, K)] = buf
+    torch.cuda.synchronize()
+
+    state = []
+    for i, (M, N, K) in enumerate(cases):
+        x_bits = synth.activations(M, K, seed=1 + i, tensor_id=1, outlier_frac=0.01)
+        ws_bytes = capi.mxfp4_gemm_workspace_bytes(M, N, K)
+        state.append({
+            "M": M, "N": N, "K": K,
+            "packed": packed_master[(N, K)].clone(),
+            "x": synth.bf16_tensor(x_bits).to(dev),
+            "x_host": synth.bf16_tensor(x_bits).pin_memory(),
+            "codes": torch.empty(capi.mxfp4_act_code_bytes(M, K, capi.LAYOUT_TILED), dtype=torch.uint8, device=dev),
+            "scales": torch.empty(capi.mxfp4_act_scale_bytes(M, K, capi.LAYOUT_TILED), dtype=torch.uint8, device=dev),
+            "out": torch.empty(M, N, dtype=torch.bfloat16, device=dev),
+            "out_host": torch.empty(M, N, dtype=torch.bfloat16).pin_memory(),
+            "ws": torch.empty(ws_bytes, dtype=torch.uint8, device=dev),
+            "ws_bytes": ws_bytes,
+        })
+    del packed_master
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.Stream(device=dev)
+    sptr = stream.cuda_stream
+
+    def step(events=None):
+        for j, c in enumerate(state):
+            capi.mxfp4_quant_act(c["x"], c["M"], c["K"], c["K"], c["codes"], c["scales"], capi.LAYOUT_TILED, sptr)
+            if events is not None:
+                events[j][0].record(stream)
+            capi.mxfp4_gemm(None, 0, c["codes"], c["scales"], capi.LAYOUT_TILED, c["packed"], None, c["out"],
+                            c["N"], c["M"], c["N"], c["K"], c["ws"], c["ws_bytes"], sptr)
+            if events is not None:
+                events[j][1].record(stream)
+
+    # eager warm-up (sets kernel attributes, checks for device errors)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    stream.synchronize()
+    assert capi.mxfp4_get_device_error(sptr) == capi.OK
+
+    # graph of G steps with timing events around every GEMM launch
+    K_steps, W_steps = args.steps, args.warmup
+    G = max(g for g in range(1, min(K_steps, 50) + 1) if K_steps % g == 0)
+    ev = [[[make_event(torch, True), make_event(torch, True)] for _ in state] for _ in range(G)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for g in range(G):
+                step(ev[g])
+    stream.synchronize()
+    replays = K_steps // G
+    warm_replays = max(1, ceil_div(W_steps, G))
+    with torch.cuda.stream(stream):
+        for _ in range(warm_replays):
+            graph.replay()
+    stream.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    t0, t1 = make_event(torch, False), make_event(torch, False)
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for _ in range(replays):
+            graph.replay()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    dist_barrier(world)
+    clk = clocks.stop()
+    assert capi.mxfp4_get_device_error(sptr) == capi.OK
+    ms_total = t0.elapsed_time(t1)
+    ms_total = dist_max(ms_total, world)
+
+    bytes_step = sum(linear_bytes(c["M"], c["N"], c["K"]) for c in state)
+    value = bytes_step * K_steps * world / (ms_total * 1e-3) / 1e9
+
+    # GEMM kernel durations: events of the last replay (inside the timed region)
+    gemm_ms = [[ev[g][j][0].elapsed_time(ev[g][j][1]) for j in range(len(state))] for g in range(G)]
+    per_case_ms = [statistics.median(gemm_ms[g][j] for g in range(G)) for j in range(len(state))]
+    kbytes = [gemm_kernel_bytes(c["M"], c["N"], c["K"]) for c in state]
+    tot_gemm_ms = sum(sum(row) for row in gemm_ms)
+    achieved = sum(kbytes) * G / (tot_gemm_ms * 1e-3) / 1e9
+    traffic = recorded_traffic()
+
+    # ---- e2e through the public API: H2D inputs, fused quant+GEMM call, D2H outputs
+    e2e_steps = max(3, min(args.e2e_steps, K_steps))
+    h2d = sum(c["M"] * c["K"] * 2 for c in state)
+    d2h = sum(c["M"] * c["N"] * 2 for c in state)
+
+    def e2e_step():
+        for c in state:
+            c["x"].copy_(c["x_host"], non_blocking=True)
+            capi.mxfp4_gemm(c["x"], c["K"], None, None, 0, c["packed"], None, c["out"], c["N"], c["M"], c["N"],
+                            c["K"], c["ws"], c["ws_bytes"], sptr)
+            c["out_host"].copy_(c["out"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+    stream.synchronize()
+    e0, e1 = make_event(torch, False), make_event(torch, False)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    stream.synchronize()
+    e2e_ms = dist_max(e0.elapsed_time(e1), world)
+    e2e_value = bytes_step * e2e_steps * world / (e2e_ms * 1e-3) / 1e9
+
+    extra = {}
+    if not args.no_secondary:
+        extra["prefill"] = run_prefill(args, torch, np, capi, synth, dev, stream, bf16_peak, peak_src)
+        extra["bmm"] = run_bmm(args, torch, np, capi, synth, dev, stream, hbm_peak, bf16_sust)
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K_steps,
+        "warmup": W_steps,
+        "ms_per_step": round(ms_total / K_steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e2m1xe2m1->f32 (bf16 out)",
+        "data": "synthetic",
+        "config": {
+            "workload": "decode W4A4 sweep: M in {1,4,16,32,64} x (N,K) in {(14336,5120),(5120,14336),(34816,5120)}; "
+                        "bf16 activations N(0,1) with 1% outlier channels x20, quantized per call; FP4 weights, "
+                        "E8M0 scales 2^U{-8..2}; bf16 out, no bias",
+            "cases_per_step": len(state),
+            "l2": "inputs larger than L2: each case reads its own packed-weight copy (15 buffers, "
+                  f"{sum(c['packed'].numel() for c in state) / 1e9:.2f} GB per step)",
+            "timing": f"CUDA graph of {G} steps replayed {replays}x; external events around each GEMM launch",
+            "parallelism": f"replicas x{world}",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "kernel": "gemm_decode_kernel (swap-AB stream-K, tcgen05 kind::mxf4)",
+            "achieved": round(achieved, 1),
+            "peak": hbm_peak,
+            "peak_source": f"{peak_src} hbm_gbs",
+            "unit": "GB/s",
+            "frac": round(achieved / hbm_peak, 4),
+            "traffic": traffic,
+            "per_case_us": {f"M{c['M']}_N{c['N']}_K{c['K']}": round(ms * 1e3, 2) for c, ms in zip(state, per_case_ms)},
+        },
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps},
+        "gpu_launches": 2 * len(state) * K_steps,
+        "clocks": clk,
+    }
+    line.update(extra)
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return line, rank
+
+
+def run_prefill(args, torch, np, capi, synth, dev, stream, bf16_peak, peak_src):
+    sptr = stream.cuda_stream
+    fp4_peak = bf16_peak * FP4_OVER_BF16
+    results = {}
+    tot_flop, tot_ms = 0.0, 0.0
+    for (N, K) in DECODE_NK:
+        wc = synth.weight_codes(N, K, seed=0, tensor_id=2)
+        ws = synth.weight_scales(N, K, *W_SCALE_PREFILL, seed=0, tensor_id=3)
+        packed = torch.empty(capi.mxfp4_packed_weight_bytes(1, N, K), dtype=torch.uint8, device=dev)
+        capi.mxfp4_pack_weights(torch.from_numpy(wc).to(dev), torch.from_numpy(ws).to(dev), 1, N, K, packed)
+        bias = synth.bf16_tensor(synth.bias(N, seed=0)).to(dev)
+        for M in PREFILL_MS:
+            x = synth.bf16_tensor(synth.activations(M, K, seed=M, tensor_id=1)).to(dev)
+            out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            wsb = capi.mxfp4_gemm_workspace_bytes(M, N, K)
+            work = torch.empty(wsb, dtype=torch.uint8, device=dev)
+
+            def call():
+                capi.mxfp4_gemm(x, K, None, None, 0, packed, bias, out, N, M, N, K, work, wsb, sptr)
+
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    call()
+            stream.synchronize()
+            reps = 20
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                for _ in range(reps):
+                    call()
+                b.record(stream)
+            stream.synchronize()
+            ms = a.elapsed_time(b) / reps
+            flop = 2.0 * M * N * K
+            results[f"M{M}_N{N}_K{K}"] = {"us": round(ms * 1e3, 1), "tflops": round(flop / (ms * 1e-3) / 1e12, 1)}
+            tot_flop += flop
+            tot_ms += ms
+        del packed
+    tflops = tot_flop / (tot_ms * 1e-3) / 1e12
+    return {"metric": "prefill W4A4 TFLOPS (quant + GEMM + bias), M in {2048, 8192}", "value": round(tflops, 1),
+            "unit": "TFLOP/s", "peak": round(fp4_peak, 1),
+            "peak_source": f"{peak_src} bf16_tflops x {FP4_OVER_BF16} (nominal dense FP4/BF16)",
+            "frac": round(tflops / fp4_peak, 4), "cases": results,
+            "l2": "back-to-back calls on one weight copy (compute-bound)"}
+
+
+def run_bmm(args, torch, np, capi, synth, dev, stream, hbm_peak, bf16_sust):
+    sptr = stream.cuda_stream
+    B = 64
+    res = {}
+    tot_bytes, tot_ms = 0.0, 0.0
+    for name, N, K, layout in (("kup", 512, 192, capi.OUT_BMN), ("vup", 256, 512, capi.OUT_MBN)):
+        wc = synth.weight_codes(N, K, seed=1, batch=B)
+        ws = synth.weight_scales(N, K, -6, 0, seed=1, batch=B)
+        packed = torch.empty(capi.mxfp4_packed_weight_bytes(B, N, K), dtype=torch.uint8, device=dev)
+        capi.mxfp4_pack_weights(torch.from_numpy(wc).to(dev), torch.from_numpy(ws).to(dev), B, N, K, packed)
+        for M in (16, 4096):
+            x = synth.bf16_tensor(synth.bmm_activations(B, M, K, seed=M)).to(dev)
+            out = torch.empty(B * M * N, dtype=torch.bfloat16, device=dev)
+
+            def call():
+                capi.a16wfp4_bmm(x, packed, out, B, M, N, K, layout, sptr)
+
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    call()
+            stream.synchronize()
+            reps = 20
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                for _ in range(reps):
+                    call()
+                b.record(stream)
+            stream.synchronize()
+            ms = a.elapsed_time(b) / reps
+            nbytes = B * M * K * 2 + B * N * K * (0.5 + 1 / 32) + B * M * N * 2
+            res[f"{name}_M{M}"] = {"us": round(ms * 1e3, 1), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                                   "tflops": round(2.0 * B * M * N * K / (ms * 1e-3) / 1e12, 1)}
+            tot_bytes += nbytes
+            tot_ms += ms
+    gbs = tot_bytes / (tot_ms * 1e-3) / 1e9
+    return {"metric": "A16WFP4 MLA absorbed BMM GB/s, B=64, M in {16, 4096}", "value": round(gbs, 1),
+            "unit": "GB/s", "peak": hbm_peak, "frac": round(gbs / hbm_peak, 4), "cases": res,
+            "l2": "back-to-back calls; x and out exceed L2 at M=4096"}
+
+
+# ------------------------------------------------------------------ oracle timing
+def oracle_sample_step(ref, synth, np, M, N, K, rows_w):
+    """The oracle's dense linear on M activation rows against a `rows_w`-row slice of the weights."""
+    x = ref.bf16_bits_to_f64(synth.activations(M, K, seed=5, outlier_frac=0.01))
+    wc = synth.weight_codes(rows_w, K, seed=N)
+    ws = synth.weight_scales(rows_w, K, *W_SCALE_DECODE, seed=N)
+    t = time.perf_counter()
+    ref.quant_then_gemm(x, wc, ws, K)
+    return time.perf_counter() - t, linear_bytes(M, rows_w, K)
+
+
+def cpu_baseline(seconds: float):
+    import numpy as np
+
+    from mxfp4_quantized_gemm_gb300 import synth
+    from oracle import mxfp4_ref as ref
+    rows_w = 2048
+    tot_t, tot_b, n = 0.0, 0, 0
+    deadline = time.perf_counter() + seconds
+    while time.perf_counter() < deadline or n < 3:
+        M = DECODE_MS[n % len(DECODE_MS)]
+        N, K = DECODE_NK[(n // len(DECODE_MS)) % len(DECODE_NK)]
+        t, b = oracle_sample_step(ref, synth, np, M, N, K, rows_w)
+        tot_t += t
+        tot_b += b
+        n += 1
+    return {"value": round(tot_b / tot_t / 1e9, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} decode-sweep cases, each the oracle's quantize + dequantized fp64 matmul of all "
+                      f"M rows against a {rows_w}-row slice of the weights (numpy/BLAS, default threads)"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None, rank
+    import numpy as np
+
+    from mxfp4_quantized_gemm_gb300 import synth
+    from oracle import mxfp4_ref as ref
+    rows_w = 64
+    cases = [(M, N, K) for M in DECODE_MS for (N, K) in DECODE_NK]
+    for i in range(args.warmup):
+        M, N, K = cases[i % len(cases)]
+        oracle_sample_step(ref, synth, np, M, N, K, rows_w)
+    tot_t, tot_b = 0.0, 0
+    for i in range(args.steps):
+        M, N, K = cases[i % len(cases)]
+        t, b = oracle_sample_step(ref, synth, np, M, N, K, rows_w)
+        tot_t += t
+        tot_b += b
+    value = tot_b / tot_t / 1e9
+    sample = (f"each step: one decode-sweep case (cycling the 15), the oracle's quantize + dequantized fp64 "
+              f"matmul against a {rows_w}-row slice of the weights")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_t / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "decode W4A4 sweep (sampled weight rows), CPU oracle"},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line, rank
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        # rank 0 alone times the oracle on the host cores; other ranks exit at once
+        world, rank = int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
+        line, rank = run_reference(args, world, rank)
+        if rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    world, rank, local = dist_init()
+    if True:
+        line, rank = run_ours(args, world, rank, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -21,6 +21,7 @@
 //    summation order, no waiting).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstdint>
 
 #include "internal.h"
@@ -41,7 +42,8 @@ struct GemmArgs {
   int w_tiles;          // Np / 128
   // stream-K (decode)
   float* partials;
-  uint32_t* tickets;
+  unsigned long long* tickets;   // per weight tile: (call tag << 16) | arrivals
+  unsigned long long tag;        // 48-bit tag of this call
   int grid;
   int64_t total_iters;
 };
@@ -96,24 +98,38 @@ __global__ void __launch_bounds__(192, 1) gemm_prefill_kernel(const GemmArgs g) 
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    // ---- producer: bulk copies of one k-tile per stage
+    // ---- producer: bulk copies of one k-tile per stage.  The weight tiles
+    // of the first stages are requested before waiting on the kernel that
+    // produces the activations (programmatic dependent launch).
     const int nsub = min(2, g.w_tiles - nt * 2);   // weight row tiles that exist
     const uint32_t bytes = kPfA + kPfSA + nsub * (kTileBytes + 1024);
-    for (int kt = 0; kt < KT; ++kt) {
+    auto load_w = [&](int kt, uint8_t* st, uint64_t* bar) {
+      for (int q = 0; q < nsub; ++q) {
+        const int rt = nt * 2 + q;
+        bulk_g2s(st + kPfA + q * kTileBytes, g.w_codes + (static_cast<size_t>(rt * KT + kt) << 14), kTileBytes, bar);
+        bulk_g2s(st + kPfA + kPfB + kPfSA + q * 1024, g.w_scales + (static_cast<size_t>(rt * 2 * KT + 2 * kt) << 9),
+                 1024, bar);
+      }
+    };
+    auto load_a = [&](int kt, uint8_t* st, uint64_t* bar) {
+      bulk_g2s(st, g.a_codes + (static_cast<size_t>(mt * KT + kt) << 14), kTileBytes, bar);
+      bulk_g2s(st + kPfA + kPfB, g.a_scales + (static_cast<size_t>(mt * 2 * KT + 2 * kt) << 9), 1024, bar);
+    };
+    const int npre = min(kPfStages, KT);
+    for (int kt = 0; kt < npre; ++kt) {
+      mbar_arrive_expect_tx(&full[kt], bytes);
+      load_w(kt, smem + kt * kPfStageBytes, &full[kt]);
+    }
+    griddep_wait();
+    for (int kt = 0; kt < npre; ++kt) load_a(kt, smem + kt * kPfStageBytes, &full[kt]);
+    for (int kt = npre; kt < KT; ++kt) {
       const int s = kt % kPfStages;
       const uint32_t ph = (kt / kPfStages) & 1;
       if (!mbar_wait(&empty[s], ph ^ 1, abort)) break;
       uint8_t* st = smem + s * kPfStageBytes;
       mbar_arrive_expect_tx(&full[s], bytes);
-      bulk_g2s(st, g.a_codes + (static_cast<size_t>(mt * KT + kt) << 14), kTileBytes, &full[s]);
-      bulk_g2s(st + kPfA + kPfB, g.a_scales + (static_cast<size_t>(mt * 2 * KT + 2 * kt) << 9), 1024, &full[s]);
-      for (int q = 0; q < nsub; ++q) {
-        const int rt = nt * 2 + q;
-        bulk_g2s(st + kPfA + q * kTileBytes, g.w_codes + (static_cast<size_t>(rt * KT + kt) << 14), kTileBytes,
-                 &full[s]);
-        bulk_g2s(st + kPfA + kPfB + kPfSA + q * 1024, g.w_scales + (static_cast<size_t>(rt * 2 * KT + 2 * kt) << 9),
-                 1024, &full[s]);
-      }
+      load_w(kt, st, &full[s]);
+      load_a(kt, st, &full[s]);
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer
@@ -144,6 +160,7 @@ __global__ void __launch_bounds__(192, 1) gemm_prefill_kernel(const GemmArgs g) 
     mma_commit(done);
   } else if (warp >= 2) {
     // ---- epilogue: TMEM -> registers -> + bias -> bf16 -> global
+    griddep_wait();
     const bool ok = mbar_wait(done, 0, abort);
     tc_fence_after();
     const int q = warp & 3;                 // TMEM lane quarter this warp may access
@@ -262,21 +279,36 @@ __global__ void __launch_bounds__(192, 1) gemm_decode_kernel(const GemmArgs g) {
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    // ---- producer
+    // ---- producer.  Weight tiles of the first stages are requested before
+    // waiting on the activation-producing kernel (programmatic dependent launch).
     const uint32_t bytes = C::kStageBytes;
-    uint32_t ls = 0;
-    for (int64_t it = it0; it < it1; ++it, ++ls) {
+    auto load_w = [&](int64_t it, uint8_t* st, uint64_t* bar) {
       const int t = static_cast<int>(it / KT);
       const int kt = static_cast<int>(it - static_cast<int64_t>(t) * KT);
+      bulk_g2s(st, g.w_codes + (static_cast<size_t>(t * KT + kt) << 14), kTileBytes, bar);
+      bulk_g2s(st + C::kW, g.w_scales + (static_cast<size_t>(t * 2 * KT + 2 * kt) << 9), 1024, bar);
+    };
+    auto load_a = [&](int64_t it, uint8_t* st, uint64_t* bar) {
+      const int kt = static_cast<int>(it % KT);
+      bulk_g2s(st + C::kW + C::kSW, g.a_codes + (static_cast<size_t>(kt) << 14), C::kA, bar);
+      bulk_g2s(st + C::kW + C::kSW + C::kA, g.a_scales + (static_cast<size_t>(2 * kt) << 9), 1024, bar);
+    };
+    const int npre = static_cast<int>((it1 - it0) < C::kStages ? (it1 - it0) : C::kStages);
+    for (int i = 0; i < npre; ++i) {
+      mbar_arrive_expect_tx(&full[i], bytes);
+      load_w(it0 + i, smem + i * C::kStageBytes, &full[i]);
+    }
+    griddep_wait();
+    for (int i = 0; i < npre; ++i) load_a(it0 + i, smem + i * C::kStageBytes, &full[i]);
+    uint32_t ls = npre;
+    for (int64_t it = it0 + npre; it < it1; ++it, ++ls) {
       const int s = ls % C::kStages;
       const uint32_t ph = (ls / C::kStages) & 1;
       if (!mbar_wait(&empty[s], ph ^ 1, abort)) break;
       uint8_t* st = smem + s * C::kStageBytes;
       mbar_arrive_expect_tx(&full[s], bytes);
-      bulk_g2s(st, g.w_codes + (static_cast<size_t>(t * KT + kt) << 14), kTileBytes, &full[s]);
-      bulk_g2s(st + C::kW, g.w_scales + (static_cast<size_t>(t * 2 * KT + 2 * kt) << 9), 1024, &full[s]);
-      bulk_g2s(st + C::kW + C::kSW, g.a_codes + (static_cast<size_t>(kt) << 14), C::kA, &full[s]);
-      bulk_g2s(st + C::kW + C::kSW + C::kA, g.a_scales + (static_cast<size_t>(2 * kt) << 9), 1024, &full[s]);
+      load_w(it, st, &full[s]);
+      load_a(it, st, &full[s]);
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA issuer: one accumulator per tile segment, double-buffered
@@ -317,6 +349,7 @@ __global__ void __launch_bounds__(192, 1) gemm_decode_kernel(const GemmArgs g) {
     }
   } else if (warp >= 2) {
     // ---- epilogue (128 threads): lane = weight row n, columns = activation rows m
+    griddep_wait();
     const int q = warp & 3;
     const int rl = q * 32 + lane;            // row inside the 128-row weight tile
     int seg = 0;
@@ -368,8 +401,19 @@ __global__ void __launch_bounds__(192, 1) gemm_decode_kernel(const GemmArgs g) {
         const int c_lo = sk_owner(tb, g.total_iters, g.grid);
         const int c_hi = sk_owner(tb + KT - 1, g.total_iters, g.grid);
         if (threadIdx.x == 64) {
-          const uint32_t prev = atomicAdd(&g.tickets[t], 1u);
-          *last_flag = (prev == static_cast<uint32_t>(c_hi - c_lo)) ? 1u : 0u;
+          // Arrival count of this call on tile t.  A word whose tag is not this
+          // call's counts as zero, so the workspace needs no initialisation.
+          unsigned long long* tk = &g.tickets[t];
+          unsigned long long cur = atomicAdd(tk, 0ull);
+          unsigned long long before;
+          while (true) {
+            before = ((cur >> 16) == g.tag) ? (cur & 0xFFFFull) : 0ull;
+            const unsigned long long want = (g.tag << 16) | (before + 1);
+            const unsigned long long seen = atomicCAS(tk, cur, want);
+            if (seen == cur) break;
+            cur = seen;
+          }
+          *last_flag = (before == static_cast<unsigned long long>(c_hi - c_lo)) ? 1u : 0u;
         }
         named_barrier(1, 128);
         if (*last_flag) {
@@ -390,7 +434,7 @@ __global__ void __launch_bounds__(192, 1) gemm_decode_kernel(const GemmArgs g) {
             for (int m = 0; m < BN; ++m)
               if (m < g.M) g.out[static_cast<size_t>(m) * g.ldo + n] = __float2bfloat16_rn(sum[m] + b);
           }
-          if (threadIdx.x == 64) g.tickets[t] = 0;   // leave the ticket clean
+          if (threadIdx.x == 64) atomicExch(&g.tickets[t], 0ull);   // leave the ticket clean
         }
         named_barrier(1, 128);
       }
@@ -423,8 +467,26 @@ size_t gemm_streamk_workspace_bytes(int M, int N, int K) {
   (void)M;
   (void)K;
   const size_t partials = static_cast<size_t>(2) * kMaxStreamKCtas * kDecodeMaxM * 128 * sizeof(float);
-  const size_t tickets = static_cast<size_t>(ceil_div(N, 128)) * sizeof(uint32_t);
+  const size_t tickets = static_cast<size_t>(ceil_div(N, 128)) * sizeof(unsigned long long);
   return partials + ((tickets + 255) & ~static_cast<size_t>(255));
+}
+
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel in the stream (the activation quantizer) is finishing;
+// it waits on it with griddepcontrol.wait before reading activations.
+template <typename Kern>
+static cudaError_t launch_pdl(Kern k, dim3 grid, int smem, cudaStream_t s, const GemmArgs& a) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, a);
 }
 
 template <int BN>
@@ -432,8 +494,18 @@ static cudaError_t launch_decode(GemmArgs& a, const DeviceInfo& dev, cudaStream_
   using C = DecodeCfg<BN>;
   cudaError_t e = ensure_smem(gemm_decode_kernel<BN>, C::kSmem, dev.device, which);
   if (e != cudaSuccess) return e;
-  gemm_decode_kernel<BN><<<a.grid, 192, C::kSmem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(gemm_decode_kernel<BN>, dim3(a.grid), C::kSmem, s, a);
+}
+
+// 48-bit tag distinguishing this call's stream-K tickets from stale words.
+static unsigned long long next_call_tag() {
+  static std::atomic<unsigned long long> seq{0};
+  unsigned long long x = seq.fetch_add(1, std::memory_order_relaxed) + 0x632BE59BD9B4E019ull;
+  x ^= x >> 31;
+  x *= 0x9E3779B97F4A7C15ull;
+  x ^= x >> 29;
+  x &= 0xFFFFFFFFFFFFull;
+  return x == 0 ? 1 : x;
 }
 
 cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_t s) {
@@ -459,9 +531,8 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
     a.grid = grid;
     a.partials = static_cast<float*>(p.workspace);
     const size_t partial_bytes = static_cast<size_t>(2) * kMaxStreamKCtas * kDecodeMaxM * 128 * sizeof(float);
-    a.tickets = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(p.workspace) + partial_bytes);
-    cudaError_t e = cudaMemsetAsync(a.tickets, 0, static_cast<size_t>(a.w_tiles) * sizeof(uint32_t), s);
-    if (e != cudaSuccess) return e;
+    a.tickets = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(p.workspace) + partial_bytes);
+    a.tag = next_call_tag();
     if (p.M <= 16) return launch_decode<16>(a, dev, s, 1);
     if (p.M <= 32) return launch_decode<32>(a, dev, s, 2);
     return launch_decode<64>(a, dev, s, 3);
@@ -469,8 +540,7 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
   cudaError_t e = ensure_smem(gemm_prefill_kernel, kPfSmem, dev.device, 0);
   if (e != cudaSuccess) return e;
   dim3 grid(static_cast<unsigned>(ceil_div(p.N, kPfBN)), static_cast<unsigned>(ceil_div(p.M, 128)));
-  gemm_prefill_kernel<<<grid, 192, kPfSmem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(gemm_prefill_kernel, grid, kPfSmem, s, a);
 }
 
 uint32_t gemm_read_clear_error() {

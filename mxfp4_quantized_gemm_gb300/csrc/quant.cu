@@ -39,6 +39,8 @@ __global__ void __launch_bounds__(256) quant_kernel(const uint16_t* __restrict__
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int64_t units = static_cast<int64_t>(rows) * KT;
   const int nb = (K + 31) >> 5;   // scale blocks per row
+  // let a GEMM launched behind this kernel set up and prefetch weights now
+  griddep_launch_dependents();
 
   for (int64_t u = warp; u < units; u += nwarps) {
     const int r = static_cast<int>(u / KT);

@@ -60,19 +60,17 @@ def full_check(capi, M, N, K, seed, **kw):
     packed = pack_weights(capi, wc, ws, K)
     got = run_gemm(capi, x, packed, b, M, N, K)
     acc, mag = oracle_gemm_rows(x, np.arange(M), wc, ws, K, b)
-    return check_close(got, acc, mag, n_acc(K), max_allowance=None, what=f"M={M} N={N} K={K}")
+    return check_close(got, acc, mag, n_acc(K), what=f"M={M} N={N} K={K}")
 
 
 def test_synthetic_16x1024x5120(capi):
-    st = full_check(capi, 16, 1024, 5120, seed=0)
-    assert st["n_allowance"] <= 2
+    full_check(capi, 16, 1024, 5120, seed=0)
 
 
 @pytest.mark.parametrize("M", [2, 3, 17, 64])
 def test_small_n_rows_all_correct(capi, M):
     # the pages' gfx950 heuristic returned wrong rows 1..M-1 for N <= 128, 2 <= M <= 64
-    st = full_check(capi, M, 128, 5120, seed=M, edge=True)
-    assert st["n_allowance"] <= 1
+    full_check(capi, M, 128, 5120, seed=M, edge=True)
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 1024, 5120), (16, 1000, 5152)])
@@ -84,8 +82,7 @@ def test_tail_shapes_small_m(capi, M, N, K):
 @pytest.mark.parametrize("M", [1, 4, 16, 32, 64])
 def test_decode_sweep(capi, M, NK):
     N, K = NK
-    st = full_check(capi, M, N, K, seed=M * 7 + N, w_lo=-8, w_hi=2, outliers=0.01)
-    assert st["n_allowance"] <= max(2, M * N // 20000)
+    full_check(capi, M, N, K, seed=M * 7 + N, w_lo=-8, w_hi=2, outliers=0.01)
 
 
 @pytest.mark.parametrize("M,N,K", [(8193, 1024, 5120), (8193, 1000, 5152)])
@@ -95,7 +92,7 @@ def test_tail_shapes_large_m(capi, M, N, K):
     got = run_gemm(capi, x, packed, b, M, N, K)
     rows = sample_rows(M, seed=1)
     acc, mag = oracle_gemm_rows(x, rows, wc, ws, K, b)
-    check_close(got[rows], acc, mag, n_acc(K), max_allowance=None, what=f"M={M}")
+    check_close(got[rows], acc, mag, n_acc(K), what=f"M={M}")
 
 
 @pytest.mark.parametrize("NK", [(14336, 5120), (5120, 14336), (34816, 5120)])
@@ -107,7 +104,7 @@ def test_prefill_with_bias(capi, M, NK):
     got = run_gemm(capi, x, packed, b, M, N, K)
     rows = sample_rows(M, seed=2, n_random=24, boundary_stride=8)
     acc, mag = oracle_gemm_rows(x, rows, wc, ws, K, b)
-    check_close(got[rows], acc, mag, n_acc(K), max_allowance=None, what=f"prefill M={M} N={N} K={K}")
+    check_close(got[rows], acc, mag, n_acc(K), what=f"prefill M={M} N={N} K={K}")
 
 
 @pytest.mark.parametrize("M", [16, 300])
@@ -159,7 +156,7 @@ def test_leading_dimension_of_output(capi):
     packed = pack_weights(capi, wc, ws, K)
     got = run_gemm(capi, x, packed, b, M, N, K, ldo=N + 40)
     acc, mag = oracle_gemm_rows(x, np.arange(M), wc, ws, K, b)
-    check_close(got, acc, mag, n_acc(K), max_allowance=0)
+    check_close(got, acc, mag, n_acc(K))
 
 
 TINY = [(m, n, k) for m in (1, 2, 7, 16, 33, 64, 65, 129)
@@ -174,7 +171,7 @@ def test_tiny_shape_sweep(capi):
         got = run_gemm(capi, x, packed, b, M, N, K)
         acc, mag = oracle_gemm_rows(x, np.arange(M), wc, ws, K, b)
         try:
-            check_close(got, acc, mag, n_acc(K), max_allowance=0, what=f"{(M, N, K)}")
+            check_close(got, acc, mag, n_acc(K), what=f"{(M, N, K)}")
         except AssertionError as e:
             bad.append(str(e)[:200])
     assert not bad, f"{len(bad)} of {len(TINY)} shapes failed: {bad[:4]}"
