@@ -15,6 +15,7 @@ import sys
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG_DIR, "csrc")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
+INCLUDE_DIR = os.path.join(os.path.dirname(PKG_DIR), "include")
 LIB_NAME = "libmxfp4_gb300.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 SOURCES = ("quant.cu", "gemm.cu", "bmm.cu", "capi.cu")
@@ -51,7 +52,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
         s = os.path.join(CSRC, src)
         obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
         if force or _stale(obj, [s] + headers):
-            cmd = [nvcc, *NVCC_FLAGS, "-c", s, "-o", obj]
+            cmd = [nvcc, *NVCC_FLAGS, "-I", INCLUDE_DIR, "-c", s, "-o", obj]
             if verbose:
                 print(" ".join(cmd), flush=True)
             res = subprocess.run(cmd, capture_output=True, text=True)

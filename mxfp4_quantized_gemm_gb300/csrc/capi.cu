@@ -4,7 +4,7 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
-#include "../../include/mxfp4.h"
+#include "mxfp4.h"
 #include "internal.h"
 
 namespace mx {
