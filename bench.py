@@ -521,6 +521,30 @@ def run_reference(args, world, rank):
     return line, rank
 
 
+def run_single(args):
+    """Run one dense-linear shape `calls` times over `copies` weight copies (for ncu captures)."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from mxfp4_quantized_gemm_gb300 import capi, synth
+    M, N, K = (int(v) for v in args.single.split(","))
+    wc = synth.weight_codes(N, K, seed=0)
+    ws = synth.weight_scales(N, K, *W_SCALE_DECODE, seed=0)
+    pk = torch.empty(capi.mxfp4_packed_weight_bytes(1, N, K), dtype=torch.uint8, device="cuda")
+    capi.mxfp4_pack_weights(torch.from_numpy(wc).cuda(), torch.from_numpy(ws).cuda(), 1, N, K, pk)
+    pks = [pk] + [pk.clone() for _ in range(args.copies - 1)]
+    x = synth.bf16_tensor(synth.activations(M, K, seed=1, outlier_frac=0.01)).cuda()
+    out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    wsb = capi.mxfp4_gemm_workspace_bytes(M, N, K)
+    work = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    for i in range(args.calls):
+        capi.mxfp4_gemm(x, K, None, None, 0, pks[i % len(pks)], None, out, N, M, N, K, work, wsb)
+    torch.cuda.synchronize()
+    assert capi.mxfp4_get_device_error() == capi.OK
+    print(f"single {M},{N},{K}: {args.calls} calls ok")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -531,7 +555,14 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--single", type=str, default=None,
+                    help="profiling mode: M,N,K of one dense-linear call (bf16 input), no JSON line")
+    ap.add_argument("--calls", type=int, default=6)
+    ap.add_argument("--copies", type=int, default=4)
     args = ap.parse_args()
+    if args.single:
+        run_single(args)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
