@@ -139,45 +139,51 @@ __global__ void __launch_bounds__(192, 1) a16wfp4_bmm_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0 && lane == 0) {
-    // ---- producer: x slabs by TMA
-    uint32_t ls = 0;
-    for (int mt = mt0; mt < mt1; ++mt) {
-      for (int ks = 0; ks < g.KS; ++ks, ++ls) {
-        const int s = ls % kBmmStages;
-        const uint32_t ph = (ls / kBmmStages) & 1;
-        if (!mbar_wait(&empty[s], ph ^ 1, abort)) break;
-        mbar_arrive_expect_tx(&full[s], kSlabBytes);
-        tma_load_3d(xsm + s * kSlabBytes, &xmap, ks * 64, mt * 128, b, &full[s]);
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- producer: x slabs by TMA
+      uint32_t ls = 0;
+      for (int mt = mt0; mt < mt1; ++mt) {
+        for (int ks = 0; ks < g.KS; ++ks, ++ls) {
+          const int s = ls % kBmmStages;
+          const uint32_t ph = (ls / kBmmStages) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1, abort)) break;
+          mbar_arrive_expect_tx(&full[s], kSlabBytes);
+          tma_load_3d(xsm + s * kSlabBytes, &xmap, ks * 64, mt * 128, b, &full[s]);
+        }
+        if (abort) break;
       }
-      if (abort) break;
     }
-  } else if (warp == 1 && lane == 0) {
-    // ---- MMA issuer
-    uint32_t ls = 0;
-    const uint32_t idesc = idesc_bf16(128, BN);
-    const uint32_t wbase = smem_u32(wsm);
-    for (int mt = mt0, i = 0; mt < mt1 && !abort; ++mt, ++i) {
-      const int buf = i & 1;
-      const uint32_t use = i >> 1;
-      if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort)) break;
-      tc_fence_after();
-      const uint32_t acc = tmem + buf * BN;
-      for (int ks = 0; ks < g.KS; ++ks, ++ls) {
-        const int s = ls % kBmmStages;
-        const uint32_t ph = (ls / kBmmStages) & 1;
-        if (!mbar_wait(&full[s], ph, abort)) break;
+    __syncwarp();   // whole warp reaches the final barrier converged
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer
+      uint32_t ls = 0;
+      const uint32_t idesc = idesc_bf16(128, BN);
+      const uint32_t wbase = smem_u32(wsm);
+      for (int mt = mt0, i = 0; mt < mt1 && !abort; ++mt, ++i) {
+        const int buf = i & 1;
+        const uint32_t use = i >> 1;
+        if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort)) break;
         tc_fence_after();
-        const uint32_t xs = smem_u32(xsm + s * kSlabBytes);
-        const uint32_t wsl = wbase + static_cast<uint32_t>(ks) * BN * 128;
+        const uint32_t acc = tmem + buf * BN;
+        for (int ks = 0; ks < g.KS; ++ks, ++ls) {
+          const int s = ls % kBmmStages;
+          const uint32_t ph = (ls / kBmmStages) & 1;
+          if (!mbar_wait(&full[s], ph, abort)) break;
+          tc_fence_after();
+          const uint32_t xs = smem_u32(xsm + s * kSlabBytes);
+          const uint32_t wsl = wbase + static_cast<uint32_t>(ks) * BN * 128;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          mma_bf16(acc, sdesc_sw128(xs + 32 * j), sdesc_sw128(wsl + 32 * j), idesc, (ks | j) != 0);
-        mma_commit(&empty[s]);
+          for (int j = 0; j < 4; ++j)
+            mma_bf16(acc, sdesc_sw128(xs + 32 * j), sdesc_sw128(wsl + 32 * j), idesc, (ks | j) != 0);
+          mma_commit(&empty[s]);
+        }
+        mma_commit(&acc_full[buf]);
       }
-      mma_commit(&acc_full[buf]);
     }
-  } else if (warp >= 2) {
+    __syncwarp();
+  } else {
     // ---- epilogue
     const int q = warp & 3;
     for (int mt = mt0, i = 0; mt < mt1; ++mt, ++i) {

@@ -97,68 +97,74 @@ __global__ void __launch_bounds__(192, 1) gemm_prefill_kernel(const GemmArgs g) 
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0 && lane == 0) {
-    // ---- producer: bulk copies of one k-tile per stage.  The weight tiles
-    // of the first stages are requested before waiting on the kernel that
-    // produces the activations (programmatic dependent launch).
-    const int nsub = min(2, g.w_tiles - nt * 2);   // weight row tiles that exist
-    const uint32_t bytes = kPfA + kPfSA + nsub * (kTileBytes + 1024);
-    auto load_w = [&](int kt, uint8_t* st, uint64_t* bar) {
-      for (int q = 0; q < nsub; ++q) {
-        const int rt = nt * 2 + q;
-        bulk_g2s(st + kPfA + q * kTileBytes, g.w_codes + (static_cast<size_t>(rt * KT + kt) << 14), kTileBytes, bar);
-        bulk_g2s(st + kPfA + kPfB + kPfSA + q * 1024, g.w_scales + (static_cast<size_t>(rt * 2 * KT + 2 * kt) << 9),
-                 1024, bar);
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- producer: bulk copies of one k-tile per stage.  The weight tiles
+      // of the first stages are requested before waiting on the kernel that
+      // produces the activations (programmatic dependent launch).
+      const int nsub = min(2, g.w_tiles - nt * 2);   // weight row tiles that exist
+      const uint32_t bytes = kPfA + kPfSA + nsub * (kTileBytes + 1024);
+      auto load_w = [&](int kt, uint8_t* st, uint64_t* bar) {
+        for (int q = 0; q < nsub; ++q) {
+          const int rt = nt * 2 + q;
+          bulk_g2s(st + kPfA + q * kTileBytes, g.w_codes + (static_cast<size_t>(rt * KT + kt) << 14), kTileBytes, bar);
+          bulk_g2s(st + kPfA + kPfB + kPfSA + q * 1024, g.w_scales + (static_cast<size_t>(rt * 2 * KT + 2 * kt) << 9),
+                   1024, bar);
+        }
+      };
+      auto load_a = [&](int kt, uint8_t* st, uint64_t* bar) {
+        bulk_g2s(st, g.a_codes + (static_cast<size_t>(mt * KT + kt) << 14), kTileBytes, bar);
+        bulk_g2s(st + kPfA + kPfB, g.a_scales + (static_cast<size_t>(mt * 2 * KT + 2 * kt) << 9), 1024, bar);
+      };
+      const int npre = min(kPfStages, KT);
+      for (int kt = 0; kt < npre; ++kt) {
+        mbar_arrive_expect_tx(&full[kt], bytes);
+        load_w(kt, smem + kt * kPfStageBytes, &full[kt]);
       }
-    };
-    auto load_a = [&](int kt, uint8_t* st, uint64_t* bar) {
-      bulk_g2s(st, g.a_codes + (static_cast<size_t>(mt * KT + kt) << 14), kTileBytes, bar);
-      bulk_g2s(st + kPfA + kPfB, g.a_scales + (static_cast<size_t>(mt * 2 * KT + 2 * kt) << 9), 1024, bar);
-    };
-    const int npre = min(kPfStages, KT);
-    for (int kt = 0; kt < npre; ++kt) {
-      mbar_arrive_expect_tx(&full[kt], bytes);
-      load_w(kt, smem + kt * kPfStageBytes, &full[kt]);
-    }
-    griddep_wait();
-    for (int kt = 0; kt < npre; ++kt) load_a(kt, smem + kt * kPfStageBytes, &full[kt]);
-    for (int kt = npre; kt < KT; ++kt) {
-      const int s = kt % kPfStages;
-      const uint32_t ph = (kt / kPfStages) & 1;
-      if (!mbar_wait(&empty[s], ph ^ 1, abort)) break;
-      uint8_t* st = smem + s * kPfStageBytes;
-      mbar_arrive_expect_tx(&full[s], bytes);
-      load_w(kt, st, &full[s]);
-      load_a(kt, st, &full[s]);
-    }
-  } else if (warp == 1 && lane == 0) {
-    // ---- MMA issuer
-    const uint32_t acc = tmem;
-    const uint32_t sfa = tmem + 256;       // 2 atoms x 4 columns
-    const uint32_t sfb = tmem + 264;       // 2 atoms x (2 row groups x 4 columns)
-    for (int kt = 0; kt < KT; ++kt) {
-      const int s = kt % kPfStages;
-      const uint32_t ph = (kt / kPfStages) & 1;
-      if (!mbar_wait(&full[s], ph, abort)) break;
-      tc_fence_after();
-      const uint32_t base = smem_u32(smem + s * kPfStageBytes);
-      const uint32_t a_s = base, b_s = base + kPfA, sa_s = base + kPfA + kPfB, sb_s = sa_s + kPfSA;
-      tmem_cp_scales(sfa + 0, sdesc_scales(sa_s));
-      tmem_cp_scales(sfa + 4, sdesc_scales(sa_s + 512));
-#pragma unroll
-      for (int a = 0; a < 2; ++a)
-#pragma unroll
-        for (int q = 0; q < 2; ++q) tmem_cp_scales(sfb + a * 8 + q * 4, sdesc_scales(sb_s + q * 1024 + a * 512));
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t id = idesc_mxf4(128, kPfBN, (j & 1) * 2, (j & 1) * 2);
-        mma_mxf4(acc, sdesc_sw128(a_s + 32 * j), sdesc_sw128(b_s + 32 * j), id, sfa + 4 * (j >> 1),
-                 sfb + 8 * (j >> 1), (kt | j) != 0);
+      griddep_wait();
+      for (int kt = 0; kt < npre; ++kt) load_a(kt, smem + kt * kPfStageBytes, &full[kt]);
+      for (int kt = npre; kt < KT; ++kt) {
+        const int s = kt % kPfStages;
+        const uint32_t ph = (kt / kPfStages) & 1;
+        if (!mbar_wait(&empty[s], ph ^ 1, abort)) break;
+        uint8_t* st = smem + s * kPfStageBytes;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        load_w(kt, st, &full[s]);
+        load_a(kt, st, &full[s]);
       }
-      mma_commit(&empty[s]);
     }
-    mma_commit(done);
-  } else if (warp >= 2) {
+    __syncwarp();   // whole warp reaches the final barrier converged
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer
+      const uint32_t acc = tmem;
+      const uint32_t sfa = tmem + 256;       // 2 atoms x 4 columns
+      const uint32_t sfb = tmem + 264;       // 2 atoms x (2 row groups x 4 columns)
+      for (int kt = 0; kt < KT; ++kt) {
+        const int s = kt % kPfStages;
+        const uint32_t ph = (kt / kPfStages) & 1;
+        if (!mbar_wait(&full[s], ph, abort)) break;
+        tc_fence_after();
+        const uint32_t base = smem_u32(smem + s * kPfStageBytes);
+        const uint32_t a_s = base, b_s = base + kPfA, sa_s = base + kPfA + kPfB, sb_s = sa_s + kPfSA;
+        tmem_cp_scales(sfa + 0, sdesc_scales(sa_s));
+        tmem_cp_scales(sfa + 4, sdesc_scales(sa_s + 512));
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int q = 0; q < 2; ++q) tmem_cp_scales(sfb + a * 8 + q * 4, sdesc_scales(sb_s + q * 1024 + a * 512));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t id = idesc_mxf4(128, kPfBN, (j & 1) * 2, (j & 1) * 2);
+          mma_mxf4(acc, sdesc_sw128(a_s + 32 * j), sdesc_sw128(b_s + 32 * j), id, sfa + 4 * (j >> 1),
+                   sfb + 8 * (j >> 1), (kt | j) != 0);
+        }
+        mma_commit(&empty[s]);
+      }
+      mma_commit(done);
+    }
+    __syncwarp();
+  } else {
     // ---- epilogue: TMEM -> registers -> + bias -> bf16 -> global
     griddep_wait();
     const bool ok = mbar_wait(done, 0, abort);
@@ -278,76 +284,82 @@ __global__ void __launch_bounds__(192, 1) gemm_decode_kernel(const GemmArgs g) {
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0 && lane == 0) {
-    // ---- producer.  Weight tiles of the first stages are requested before
-    // waiting on the activation-producing kernel (programmatic dependent launch).
-    const uint32_t bytes = C::kStageBytes;
-    auto load_w = [&](int64_t it, uint8_t* st, uint64_t* bar) {
-      const int t = static_cast<int>(it / KT);
-      const int kt = static_cast<int>(it - static_cast<int64_t>(t) * KT);
-      bulk_g2s(st, g.w_codes + (static_cast<size_t>(t * KT + kt) << 14), kTileBytes, bar);
-      bulk_g2s(st + C::kW, g.w_scales + (static_cast<size_t>(t * 2 * KT + 2 * kt) << 9), 1024, bar);
-    };
-    auto load_a = [&](int64_t it, uint8_t* st, uint64_t* bar) {
-      const int kt = static_cast<int>(it % KT);
-      bulk_g2s(st + C::kW + C::kSW, g.a_codes + (static_cast<size_t>(kt) << 14), C::kA, bar);
-      bulk_g2s(st + C::kW + C::kSW + C::kA, g.a_scales + (static_cast<size_t>(2 * kt) << 9), 1024, bar);
-    };
-    const int npre = static_cast<int>((it1 - it0) < C::kStages ? (it1 - it0) : C::kStages);
-    for (int i = 0; i < npre; ++i) {
-      mbar_arrive_expect_tx(&full[i], bytes);
-      load_w(it0 + i, smem + i * C::kStageBytes, &full[i]);
-    }
-    griddep_wait();
-    for (int i = 0; i < npre; ++i) load_a(it0 + i, smem + i * C::kStageBytes, &full[i]);
-    uint32_t ls = npre;
-    for (int64_t it = it0 + npre; it < it1; ++it, ++ls) {
-      const int s = ls % C::kStages;
-      const uint32_t ph = (ls / C::kStages) & 1;
-      if (!mbar_wait(&empty[s], ph ^ 1, abort)) break;
-      uint8_t* st = smem + s * C::kStageBytes;
-      mbar_arrive_expect_tx(&full[s], bytes);
-      load_w(it, st, &full[s]);
-      load_a(it, st, &full[s]);
-    }
-  } else if (warp == 1 && lane == 0) {
-    // ---- MMA issuer: one accumulator per tile segment, double-buffered
-    const uint32_t sfa = tmem + C::kAccCols;
-    const uint32_t sfb = tmem + C::kAccCols + 8;
-    uint32_t ls = 0;
-    int seg = 0;
-    for (int64_t it = it0; it < it1 && !abort; ++seg) {
-      const int t = static_cast<int>(it / KT);
-      const int ka = static_cast<int>(it - static_cast<int64_t>(t) * KT);
-      const int kb = static_cast<int>(seg_end(KT, ka, it1 - it));
-      const int buf = seg & 1;
-      const uint32_t use = seg >> 1;
-      if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort)) break;
-      tc_fence_after();
-      const uint32_t acc = tmem + buf * BN;
-      for (int kt = ka; kt < kb; ++kt, ++ls) {
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- producer.  Weight tiles of the first stages are requested before
+      // waiting on the activation-producing kernel (programmatic dependent launch).
+      const uint32_t bytes = C::kStageBytes;
+      auto load_w = [&](int64_t it, uint8_t* st, uint64_t* bar) {
+        const int t = static_cast<int>(it / KT);
+        const int kt = static_cast<int>(it - static_cast<int64_t>(t) * KT);
+        bulk_g2s(st, g.w_codes + (static_cast<size_t>(t * KT + kt) << 14), kTileBytes, bar);
+        bulk_g2s(st + C::kW, g.w_scales + (static_cast<size_t>(t * 2 * KT + 2 * kt) << 9), 1024, bar);
+      };
+      auto load_a = [&](int64_t it, uint8_t* st, uint64_t* bar) {
+        const int kt = static_cast<int>(it % KT);
+        bulk_g2s(st + C::kW + C::kSW, g.a_codes + (static_cast<size_t>(kt) << 14), C::kA, bar);
+        bulk_g2s(st + C::kW + C::kSW + C::kA, g.a_scales + (static_cast<size_t>(2 * kt) << 9), 1024, bar);
+      };
+      const int npre = static_cast<int>((it1 - it0) < C::kStages ? (it1 - it0) : C::kStages);
+      for (int i = 0; i < npre; ++i) {
+        mbar_arrive_expect_tx(&full[i], bytes);
+        load_w(it0 + i, smem + i * C::kStageBytes, &full[i]);
+      }
+      griddep_wait();
+      for (int i = 0; i < npre; ++i) load_a(it0 + i, smem + i * C::kStageBytes, &full[i]);
+      uint32_t ls = npre;
+      for (int64_t it = it0 + npre; it < it1; ++it, ++ls) {
         const int s = ls % C::kStages;
         const uint32_t ph = (ls / C::kStages) & 1;
-        if (!mbar_wait(&full[s], ph, abort)) break;
-        tc_fence_after();
-        const uint32_t base = smem_u32(smem + s * C::kStageBytes);
-        const uint32_t w_s = base, sw_s = base + C::kW, a_s = sw_s + C::kSW, sa_s = a_s + C::kA;
-        tmem_cp_scales(sfa + 0, sdesc_scales(sw_s));
-        tmem_cp_scales(sfa + 4, sdesc_scales(sw_s + 512));
-        tmem_cp_scales(sfb + 0, sdesc_scales(sa_s));
-        tmem_cp_scales(sfb + 4, sdesc_scales(sa_s + 512));
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t id = idesc_mxf4(128, BN, (j & 1) * 2, (j & 1) * 2);
-          mma_mxf4(acc, sdesc_sw128(w_s + 32 * j), sdesc_sw128(a_s + 32 * j), id, sfa + 4 * (j >> 1),
-                   sfb + 4 * (j >> 1), (kt != ka || j != 0) ? 1u : 0u);
-        }
-        mma_commit(&empty[s]);
+        if (!mbar_wait(&empty[s], ph ^ 1, abort)) break;
+        uint8_t* st = smem + s * C::kStageBytes;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        load_w(it, st, &full[s]);
+        load_a(it, st, &full[s]);
       }
-      mma_commit(&acc_full[buf]);
-      it += kb - ka;
     }
-  } else if (warp >= 2) {
+    __syncwarp();   // whole warp reaches the final barrier converged
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA issuer: one accumulator per tile segment, double-buffered
+      const uint32_t sfa = tmem + C::kAccCols;
+      const uint32_t sfb = tmem + C::kAccCols + 8;
+      uint32_t ls = 0;
+      int seg = 0;
+      for (int64_t it = it0; it < it1 && !abort; ++seg) {
+        const int t = static_cast<int>(it / KT);
+        const int ka = static_cast<int>(it - static_cast<int64_t>(t) * KT);
+        const int kb = static_cast<int>(seg_end(KT, ka, it1 - it));
+        const int buf = seg & 1;
+        const uint32_t use = seg >> 1;
+        if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort)) break;
+        tc_fence_after();
+        const uint32_t acc = tmem + buf * BN;
+        for (int kt = ka; kt < kb; ++kt, ++ls) {
+          const int s = ls % C::kStages;
+          const uint32_t ph = (ls / C::kStages) & 1;
+          if (!mbar_wait(&full[s], ph, abort)) break;
+          tc_fence_after();
+          const uint32_t base = smem_u32(smem + s * C::kStageBytes);
+          const uint32_t w_s = base, sw_s = base + C::kW, a_s = sw_s + C::kSW, sa_s = a_s + C::kA;
+          tmem_cp_scales(sfa + 0, sdesc_scales(sw_s));
+          tmem_cp_scales(sfa + 4, sdesc_scales(sw_s + 512));
+          tmem_cp_scales(sfb + 0, sdesc_scales(sa_s));
+          tmem_cp_scales(sfb + 4, sdesc_scales(sa_s + 512));
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t id = idesc_mxf4(128, BN, (j & 1) * 2, (j & 1) * 2);
+            mma_mxf4(acc, sdesc_sw128(w_s + 32 * j), sdesc_sw128(a_s + 32 * j), id, sfa + 4 * (j >> 1),
+                     sfb + 4 * (j >> 1), (kt != ka || j != 0) ? 1u : 0u);
+          }
+          mma_commit(&empty[s]);
+        }
+        mma_commit(&acc_full[buf]);
+        it += kb - ka;
+      }
+    }
+    __syncwarp();
+  } else {
     // ---- epilogue (128 threads): lane = weight row n, columns = activation rows m
     griddep_wait();
     const int q = warp & 3;
