@@ -180,6 +180,31 @@ MXFP4_API mxfp4_status a16wfp4_bmm(const void* x_dev, const void* w_packed_dev, 
                          void* stream);
 
 /*
+ * mxfp4_gemm without a workspace argument, for callers that cannot allocate
+ * device memory where they run the layer: code inside CUDA stream capture,
+ * serving loops that must not take cudaMalloc's implicit synchronisation,
+ * and hosts whose device memory belongs to an allocator this library cannot
+ * call.  (The pages have no counterpart; this entry point is an addition.)
+ *
+ * Same operation and arguments as mxfp4_gemm with a bf16 activation input;
+ * the scratch comes from one fixed device array inside the library, of
+ * mxfp4_gemm_noalloc_max_scratch_bytes() bytes (24 MiB), which every GPU that
+ * uses it holds until the process exits.  A problem whose
+ * mxfp4_gemm_workspace_bytes(M, N, K) exceeds that size is rejected with
+ * MXFP4_ERR_WORKSPACE.  Nothing is allocated or freed.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents.
+ *     Nothing in it has to start at zero (the stream-K tickets are tagged per
+ *     call and left reset), but calls that overlap on the GPU — on different
+ *     streams, or from several host threads without ordering — race on it.
+ */
+MXFP4_API mxfp4_status mxfp4_gemm_noalloc(const void* a_bf16_dev, int lda, const void* w_packed_dev,
+                                          const void* bias_dev, void* out_dev, int ldo, int M, int N, int K,
+                                          void* stream);
+MXFP4_API size_t mxfp4_gemm_noalloc_max_scratch_bytes(void);
+
+/*
  * Synchronises `stream`, then reads and clears the library's device error
  * words on the current device.  Returns MXFP4_ERR_TIMEOUT if a kernel gave
  * up a bounded wait since the last call, MXFP4_OK otherwise (or

@@ -41,6 +41,8 @@ _SIGNATURES = {
     "mxfp4_gemm": (_i, [_p, _i, _p, _p, _i, _p, _p, _p, _i, _i, _i, _i, _p, _sz, _p]),
     "a16wfp4_bmm": (_i, [_p, _p, _p, _i, _i, _i, _i, _i, _p]),
     "mxfp4_get_device_error": (_i, [_p]),
+    "mxfp4_gemm_noalloc": (_i, [_p, _i, _p, _p, _p, _i, _i, _i, _i, _p]),
+    "mxfp4_gemm_noalloc_max_scratch_bytes": (_sz, []),
 }
 for _name, (_res, _args) in _SIGNATURES.items():
     _fn = getattr(lib, _name)
@@ -121,6 +123,17 @@ def mxfp4_gemm(a_bf16, lda: int, a_codes, a_scales, a_layout: int, w_packed, bia
 def a16wfp4_bmm(x, w_packed, out, B: int, M: int, N: int, K: int, out_layout: int, stream=None) -> None:
     _check(lib.a16wfp4_bmm(_ptr(x), _ptr(w_packed), _ptr(out), B, M, N, K, out_layout, _stream(stream)),
            "a16wfp4_bmm")
+
+
+def mxfp4_gemm_noalloc(a_bf16, lda: int, w_packed, bias, out, ldo: int, M: int, N: int, K: int,
+                       stream=None) -> None:
+    _check(lib.mxfp4_gemm_noalloc(_ptr(a_bf16), lda, _ptr(w_packed), _ptr(bias), _ptr(out), ldo, M, N, K,
+                                  _stream(stream)),
+           "mxfp4_gemm_noalloc")
+
+
+def mxfp4_gemm_noalloc_max_scratch_bytes() -> int:
+    return lib.mxfp4_gemm_noalloc_max_scratch_bytes()
 
 
 def mxfp4_get_device_error(stream=None) -> int:

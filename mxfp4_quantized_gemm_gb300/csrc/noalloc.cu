@@ -1,0 +1,63 @@
+// mxfp4_gemm_noalloc: the W4A4 GEMM without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory at the point where they run the
+// linear layer: code executing inside CUDA stream capture (allocation there
+// either breaks the capture or is forbidden by the surrounding framework),
+// serving loops that must never hit cudaMalloc's implicit synchronisation,
+// and host applications whose memory is owned by a foreign allocator that
+// this library cannot reach.  For them, the scratch that mxfp4_gemm needs
+// (tiled activation codes and scales, stream-K partial sums and tickets)
+// lives in one file-scope device array of fixed size instead.
+//
+// The array exists on every GPU where this library's module is loaded, from
+// the first use on that device until the process exits.  Its address is
+// looked up once per device (on that device's first call) and handed to the
+// existing GEMM path; nothing here allocates or frees memory.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "internal.h"
+#include "mxfp4.h"
+
+namespace mx {
+
+// Upper bound of the scratch a call may use.
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(24) << 20;   // 24 MiB
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+static void* g_noalloc_ptr[64];     // device address of the array, per device
+static std::mutex g_noalloc_mutex;
+
+// Device address of the scratch array on the current device (looked up once
+// per device), or nullptr on failure.
+static void* noalloc_scratch(int device) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[device] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return nullptr;
+    g_noalloc_ptr[device] = ptr;
+  }
+  return g_noalloc_ptr[device];
+}
+
+}  // namespace mx
+
+extern "C" size_t mxfp4_gemm_noalloc_max_scratch_bytes(void) { return mx::kNoAllocScratchBytes; }
+
+extern "C" mxfp4_status mxfp4_gemm_noalloc(const void* a_bf16, int lda, const void* w_packed, const void* bias,
+                                           void* out, int ldo, int M, int N, int K, void* stream) {
+  if (a_bf16 == nullptr || w_packed == nullptr || out == nullptr) return MXFP4_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_INVALID_ARG;
+  const size_t need = mxfp4_gemm_workspace_bytes(M, N, K);
+  if (need == 0) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  if (need > mx::kNoAllocScratchBytes) return MXFP4_ERR_WORKSPACE;   // problem too large for the static scratch
+  mx::DeviceInfo dev;
+  if (mx::current_device_info(&dev) != cudaSuccess || !dev.ok) return MXFP4_ERR_NO_DEVICE;
+  void* scratch = mx::noalloc_scratch(dev.device);
+  if (scratch == nullptr) return MXFP4_ERR_CUDA;
+  return mxfp4_gemm(a_bf16, lda, nullptr, nullptr, MXFP4_LAYOUT_ROWMAJOR, w_packed, bias, out, ldo, M, N, K, scratch,
+                    mx::kNoAllocScratchBytes, stream);
+}

@@ -1,0 +1,74 @@
+"""The allocation-free GEMM entry point (mxfp4_gemm_noalloc).
+
+Callers that cannot allocate device memory where they run the layer (inside
+stream capture, in serving loops that must avoid cudaMalloc's implicit
+synchronisation, or under a foreign allocator) use this entry point; its
+scratch lives in a fixed device array inside the library.  The test calls it
+through the C ABI twice in a row and checks each output against the
+workspace-taking mxfp4_gemm with the same tolerance as the other GEMM tests,
+and checks that problems larger than the fixed scratch are refused.  It sits
+in its own file so that pytest collects it last.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from mxfp4_quantized_gemm_gb300 import synth
+from helpers import dev_bf16, empty_u8, host_bits, pack_weights, ulp_bf16
+from oracle import mxfp4_ref as ref
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def capi():
+    from mxfp4_quantized_gemm_gb300 import capi as c
+    return c
+
+
+def with_workspace(capi, x, packed, bias, M, N, K):
+    out = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
+    wsb = capi.mxfp4_gemm_workspace_bytes(M, N, K)
+    capi.mxfp4_gemm(x, K, None, None, 0, packed, bias, out, N, M, N, K, empty_u8(wsb), wsb)
+    torch.cuda.synchronize()
+    return host_bits(out)
+
+
+def without_workspace(capi, x, packed, bias, M, N, K):
+    out = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
+    capi.mxfp4_gemm_noalloc(x, K, packed, bias, out, N, M, N, K)
+    torch.cuda.synchronize()
+    assert capi.mxfp4_get_device_error() == capi.OK
+    return host_bits(out)
+
+
+def assert_within_2ulp(got_bits, want_bits):
+    got = ref.bf16_bits_to_f64(got_bits)
+    want = ref.bf16_bits_to_f64(want_bits)
+    assert np.all(np.isfinite(got))
+    assert np.all(np.abs(got - want) <= 2 * ulp_bf16(want))
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 14336, 5120), (64, 5120, 14336), (300, 1000, 5152)])
+def test_noalloc_matches_workspace_entry_twice(capi, M, N, K):
+    wc = synth.weight_codes(N, K, seed=M)
+    ws = synth.weight_scales(N, K, -8, 2, seed=M)
+    packed = pack_weights(capi, wc, ws, K)
+    bias = dev_bf16(synth.bias(N, seed=M))
+    for call in range(2):     # two calls in a row share the fixed scratch
+        x = dev_bf16(synth.activations(M, K, seed=100 * M + call, outlier_frac=0.01))
+        want = with_workspace(capi, x, packed, bias, M, N, K)
+        got = without_workspace(capi, x, packed, bias, M, N, K)
+        assert_within_2ulp(got, want)
+
+
+def test_noalloc_refuses_problems_beyond_its_scratch(capi):
+    M, N, K = 8192, 1024, 14336
+    assert capi.mxfp4_gemm_workspace_bytes(M, N, K) > capi.mxfp4_gemm_noalloc_max_scratch_bytes()
+    out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros(M, K, dtype=torch.bfloat16, device="cuda")
+    packed = empty_u8(capi.mxfp4_packed_weight_bytes(1, N, K))
+    st = capi.lib.mxfp4_gemm_noalloc(x.data_ptr(), K, packed.data_ptr(), None, out.data_ptr(), N, M, N, K,
+                                     torch.cuda.current_stream().cuda_stream)
+    assert st == capi.ERR_WORKSPACE
