@@ -188,7 +188,7 @@ MXFP4_API mxfp4_status a16wfp4_bmm(const void* x_dev, const void* w_packed_dev, 
  *
  * Same operation and arguments as mxfp4_gemm with a bf16 activation input;
  * the scratch comes from one fixed device array inside the library, of
- * mxfp4_gemm_noalloc_max_scratch_bytes() bytes (24 MiB), which every GPU that
+ * mxfp4_gemm_noalloc_max_scratch_bytes() bytes (48 MiB), which every GPU that
  * uses it holds until the process exits.  A problem whose
  * mxfp4_gemm_workspace_bytes(M, N, K) exceeds that size is rejected with
  * MXFP4_ERR_WORKSPACE.  Nothing is allocated or freed.

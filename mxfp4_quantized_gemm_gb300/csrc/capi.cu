@@ -50,13 +50,21 @@ static mxfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MXFP4_O
 struct GemmWorkspace {
   size_t codes_off, scales_off, streamk_off, total;
 };
-static GemmWorkspace gemm_workspace_layout(int M, int N, int K) {
+static GemmWorkspace gemm_workspace_layout(int M, int N, int K, int grid) {
   GemmWorkspace w{};
   w.codes_off = 0;
   w.scales_off = round_up(static_cast<size_t>(tiled_code_bytes(M, K)), 1024);
   w.streamk_off = w.scales_off + round_up(static_cast<size_t>(tiled_scale_bytes(M, K)), 1024);
-  w.total = w.streamk_off + round_up(gemm_streamk_workspace_bytes(M, N, K), 1024);
+  w.total = w.streamk_off + round_up(gemm_streamk_workspace_bytes(M, N, K, grid), 1024);
   return w;
+}
+
+// Stream-K grid of the current device (the largest grid if none is usable).
+static int current_gemm_grid() {
+  DeviceInfo dev;
+  if (current_device_info(&dev) == cudaSuccess && dev.ok) return gemm_grid(dev);
+  cudaGetLastError();   // clear the error of a failed device query
+  return kMaxStreamKCtas;
 }
 
 }  // namespace mx
@@ -125,13 +133,13 @@ mxfp4_status mxfp4_quant_act(const void* x, int M, int K, int ldx, uint8_t* code
   DeviceInfo dev;
   mxfp4_status st = device_ready(&dev);
   if (st != MXFP4_OK) return st;
-  return from_cuda(launch_quant(x, M, K, ldx, codes, scales, layout == MXFP4_LAYOUT_TILED, dev,
+  return from_cuda(launch_quant(x, M, K, ldx, codes, scales, layout == MXFP4_LAYOUT_TILED, 0, dev,
                                 static_cast<cudaStream_t>(stream)));
 }
 
 size_t mxfp4_gemm_workspace_bytes(int M, int N, int K) {
   if (M <= 0 || N <= 0 || K <= 0 || (K & 1)) return 0;
-  return gemm_workspace_layout(M, N, K).total;
+  return gemm_workspace_layout(M, N, K, current_gemm_grid()).total;
 }
 
 mxfp4_status mxfp4_gemm(const void* a_bf16, int lda, const uint8_t* a_codes, const uint8_t* a_scales,
@@ -150,13 +158,22 @@ mxfp4_status mxfp4_gemm(const void* a_bf16, int lda, const uint8_t* a_codes, con
   if (from_bf16 && (reinterpret_cast<uintptr_t>(a_bf16) & 1)) return MXFP4_ERR_MISALIGNED;
   if (!from_bf16 && a_layout == MXFP4_LAYOUT_TILED && (!aligned16(a_codes) || !aligned16(a_scales)))
     return MXFP4_ERR_MISALIGNED;
-  const GemmWorkspace wl = gemm_workspace_layout(M, N, K);
-  if (workspace == nullptr || workspace_bytes < wl.total) return MXFP4_ERR_WORKSPACE;
+  if (workspace == nullptr) return MXFP4_ERR_WORKSPACE;
   if (!aligned16(workspace)) return MXFP4_ERR_MISALIGNED;
+  // without a usable device, check against the largest grid's requirement
+  if (workspace_bytes < gemm_workspace_layout(M, N, K, kMaxStreamKCtas).total) {
+    DeviceInfo probe;
+    if (current_device_info(&probe) != cudaSuccess || !probe.ok) {
+      cudaGetLastError();
+      return MXFP4_ERR_WORKSPACE;
+    }
+  }
 
   DeviceInfo dev;
   mxfp4_status st = device_ready(&dev);
   if (st != MXFP4_OK) return st;
+  const GemmWorkspace wl = gemm_workspace_layout(M, N, K, gemm_grid(dev));
+  if (workspace_bytes < wl.total) return MXFP4_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
 
@@ -164,7 +181,9 @@ mxfp4_status mxfp4_gemm(const void* a_bf16, int lda, const uint8_t* a_codes, con
   if (from_bf16) {
     p.a_codes = ws + wl.codes_off;
     p.a_scales = ws + wl.scales_off;
-    cudaError_t e = launch_quant(a_bf16, M, K, lda, ws + wl.codes_off, ws + wl.scales_off, true, dev, s);
+    // for small M the GEMM reads only the first gemm_rows_a(M) activation rows
+    const int rows = M <= kDecodeMaxM ? gemm_rows_a(M) : 0;
+    cudaError_t e = launch_quant(a_bf16, M, K, lda, ws + wl.codes_off, ws + wl.scales_off, true, rows, dev, s);
     if (e != cudaSuccess) return MXFP4_ERR_CUDA;
   } else if (a_layout == MXFP4_LAYOUT_ROWMAJOR) {
     // the pages' pre-quantized (x_fp4, x_scales) input: re-lay out, pad scales with 0x7F

@@ -4,24 +4,31 @@
 //
 // the gemm_a4w4 + bias step of sglang PR #39598 (blog analysis, section 2,
 // apply_weights).  Both operands arrive in the TILED layout, so every stage
-// is a handful of contiguous 1-D bulk copies (16 KiB code tiles already in
-// the 128-byte-swizzled K-major image, 512-byte scale atoms already in the
-// tcgen05.cp source layout).  One thread issues
-// tcgen05.mma.kind::mxf4.block_scale (K = 64 per instruction, two UE8M0
-// scales per row per instruction) into a TMEM fp32 accumulator; four warps
-// drain TMEM with tcgen05.ld and run the bias + bf16 epilogue.
+// is a few contiguous 1-D bulk copies: 16 KiB code tiles already in the
+// 128-byte-swizzled K-major image, 512-byte scale atoms already in the
+// tcgen05.cp source layout.
 //
-// Two kernels share that machinery:
-//  * prefill (M > 64): one CTA per 128 x 256 output tile, full K;
-//  * decode (M <= 64): swap-AB -- the weight rows are the MMA's M = 128
-//    operand and the few activation rows its N (16/32/64) -- with a balanced
-//    stream-K split of the (weight tile, k-tile) iteration space over one CTA
-//    per SM, so every SM streams the same number of weight bytes; partial
-//    tiles are summed by the last CTA to finish them (atomic ticket, fixed
-//    summation order, no waiting).
+// One persistent kernel serves every M.  An output tile is 128 activation
+// rows (the MMA's M) by 256 weight rows (its N).  A
+// tcgen05.mma.kind::mxf4.block_scale instruction costs about the same for any
+// N, so the 256-row weight side moves the most weight bytes per tensor-pipe
+// cycle.  That serves both the weight-streaming decode shapes (M <= 64: only
+// 16/32/64 activation rows are loaded) and the compute-bound prefill shapes.
+// The (tile, 256-wide k-step) iteration space is split evenly over one CTA
+// per SM (stream-K), so every SM streams the same number of weight bytes.  A
+// tile split between CTAs is finished by the last CTA to finish its part,
+// which sums the fp32 partials in CTA order (deterministic, no spin-waits).
+//
+// Roles (320 threads): warp 0 streams stages with bulk copies; warp 1 issues
+// tcgen05.cp (scales -> TMEM) and the MMAs into one 128 x 256 fp32 TMEM
+// accumulator; warps 2..9 drain it (each 32 rows x 128 columns) with
+// tcgen05.ld, release it at once, then add the bias and store bf16 (or
+// publish the partial).  The kernel is launched as a programmatic dependent:
+// it sets up and requests its first weight stages while the activation
+// quantizer before it finishes, and lets the next kernel launch early.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
-#include <atomic>
+
 #include <cstdint>
 
 #include "internal.h"
@@ -31,6 +38,11 @@ namespace mx {
 
 static __device__ uint32_t g_gemm_error;
 
+constexpr int kTileN = 256;          // weight rows per output tile (the MMA's N)
+constexpr int kThreads = 320;        // producer warp, MMA warp, 8 epilogue warps
+constexpr int kEpiThreads = 256;
+constexpr int kMaxSmem = 232448;     // 227 KiB of dynamic shared memory per CTA
+
 struct GemmArgs {
   const uint8_t* a_codes;
   const uint8_t* a_scales;
@@ -39,229 +51,119 @@ struct GemmArgs {
   const __nv_bfloat16* bias;
   __nv_bfloat16* out;
   int ldo, M, N, KT;
-  int w_tiles;          // Np / 128
-  // stream-K (decode)
-  float* partials;
-  unsigned long long* tickets;   // per weight tile: (call tag << 16) | arrivals
-  unsigned long long tag;        // 48-bit tag of this call
+  int w_tiles;                     // Np / 128: 128-row tiles of the packed weights
+  int n_tiles;                     // ceil(N / 256)
+  int total;                       // output tiles x KT
   int grid;
-  int64_t total_iters;
+  int rows_a;                      // activation rows per tile that are loaded (16/32/64/128)
+  float* partials;                 // 2 slots per CTA, rows_a x 256 floats each
+};
+
+template <int kRowsA>
+struct Cfg {
+  static constexpr int kW = 2 * kTileBytes;       // 256 weight rows of codes
+  // Only the first kRowsA activation rows are loaded and reserved per stage.
+  // The M = 128 MMA reads 16 KiB from the activation offset; for kRowsA <
+  // 128 the rows past kRowsA come from whatever follows (the next stage, or a
+  // tail pad after the last one, so every read stays inside the allocation)
+  // and feed only accumulator rows that are never read.
+  static constexpr int kALoad = kRowsA * 128;
+  static constexpr int kA = kALoad;
+  static constexpr int kTailPad = kTileBytes - kALoad;
+  static constexpr int kSA = 1024;                // 2 activation scale atoms
+  static constexpr int kSW = 2048;                // 2 x 2 weight scale atoms
+  static constexpr int kStageBytes = kW + kA + kSA + kSW;
+  static constexpr int kStagesFit = (kMaxSmem - 1024 - 512 - kTailPad) / kStageBytes;
+  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+  static constexpr int kRing = kStages * kStageBytes + kTailPad;
+  static constexpr int kSmem = kRing + 1024 + 512;
+  static constexpr uint32_t kTmemCols = 512;      // accumulator 256 + scales 24
+  static constexpr uint32_t kSfa = 256, kSfb = 264;
 };
 
 __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
 }
-
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
 
-// ===================================================================== prefill
-constexpr int kPfBN = 256;
-constexpr int kPfStages = 4;
-constexpr int kPfA = kTileBytes;                     // 128 rows of A codes
-constexpr int kPfB = kPfBN * 128;                    // 256 rows of W codes
-constexpr int kPfSA = 1024;                          // 2 scale atoms of A
-constexpr int kPfSB = (kPfBN / 128) * 1024;          // 2 x 2 scale atoms of W
-constexpr int kPfStageBytes = kPfA + kPfB + kPfSA + kPfSB;
-constexpr int kPfSmem = kPfStages * kPfStageBytes + 1024 /*align*/ + 256 /*barriers*/;
-constexpr uint32_t kPfTmemCols = 512;                // 256 accumulator + 24 scale columns
-
-__global__ void __launch_bounds__(192, 1) gemm_prefill_kernel(const GemmArgs g) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align_1024(smem_raw);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kPfStages * kPfStageBytes);
-  uint64_t* empty = full + kPfStages;
-  uint64_t* done = empty + kPfStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nt = blockIdx.x, mt = blockIdx.y;
-  const int KT = g.KT;
-  bool abort = false;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kPfStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    mbar_init(done, 1);
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, kPfTmemCols);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---- producer: bulk copies of one k-tile per stage.  The weight tiles
-      // of the first stages are requested before waiting on the kernel that
-      // produces the activations (programmatic dependent launch).
-      const int nsub = min(2, g.w_tiles - nt * 2);   // weight row tiles that exist
-      const uint32_t bytes = kPfA + kPfSA + nsub * (kTileBytes + 1024);
-      auto load_w = [&](int kt, uint8_t* st, uint64_t* bar) {
-        for (int q = 0; q < nsub; ++q) {
-          const int rt = nt * 2 + q;
-          bulk_g2s(st + kPfA + q * kTileBytes, g.w_codes + (static_cast<size_t>(rt * KT + kt) << 14), kTileBytes, bar);
-          bulk_g2s(st + kPfA + kPfB + kPfSA + q * 1024, g.w_scales + (static_cast<size_t>(rt * 2 * KT + 2 * kt) << 9),
-                   1024, bar);
-        }
-      };
-      auto load_a = [&](int kt, uint8_t* st, uint64_t* bar) {
-        bulk_g2s(st, g.a_codes + (static_cast<size_t>(mt * KT + kt) << 14), kTileBytes, bar);
-        bulk_g2s(st + kPfA + kPfB, g.a_scales + (static_cast<size_t>(mt * 2 * KT + 2 * kt) << 9), 1024, bar);
-      };
-      const int npre = min(kPfStages, KT);
-      for (int kt = 0; kt < npre; ++kt) {
-        mbar_arrive_expect_tx(&full[kt], bytes);
-        load_w(kt, smem + kt * kPfStageBytes, &full[kt]);
-      }
-      griddep_wait();
-      for (int kt = 0; kt < npre; ++kt) load_a(kt, smem + kt * kPfStageBytes, &full[kt]);
-      for (int kt = npre; kt < KT; ++kt) {
-        const int s = kt % kPfStages;
-        const uint32_t ph = (kt / kPfStages) & 1;
-        if (!mbar_wait(&empty[s], ph ^ 1, abort)) break;
-        uint8_t* st = smem + s * kPfStageBytes;
-        mbar_arrive_expect_tx(&full[s], bytes);
-        load_w(kt, st, &full[s]);
-        load_a(kt, st, &full[s]);
-      }
-    }
-    __syncwarp();   // whole warp reaches the final barrier converged
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ---- MMA issuer
-      const uint32_t acc = tmem;
-      const uint32_t sfa = tmem + 256;       // 2 atoms x 4 columns
-      const uint32_t sfb = tmem + 264;       // 2 atoms x (2 row groups x 4 columns)
-      for (int kt = 0; kt < KT; ++kt) {
-        const int s = kt % kPfStages;
-        const uint32_t ph = (kt / kPfStages) & 1;
-        if (!mbar_wait(&full[s], ph, abort)) break;
-        tc_fence_after();
-        const uint32_t base = smem_u32(smem + s * kPfStageBytes);
-        const uint32_t a_s = base, b_s = base + kPfA, sa_s = base + kPfA + kPfB, sb_s = sa_s + kPfSA;
-        tmem_cp_scales(sfa + 0, sdesc_scales(sa_s));
-        tmem_cp_scales(sfa + 4, sdesc_scales(sa_s + 512));
-#pragma unroll
-        for (int a = 0; a < 2; ++a)
-#pragma unroll
-          for (int q = 0; q < 2; ++q) tmem_cp_scales(sfb + a * 8 + q * 4, sdesc_scales(sb_s + q * 1024 + a * 512));
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t id = idesc_mxf4(128, kPfBN, (j & 1) * 2, (j & 1) * 2);
-          mma_mxf4(acc, sdesc_sw128(a_s + 32 * j), sdesc_sw128(b_s + 32 * j), id, sfa + 4 * (j >> 1),
-                   sfb + 8 * (j >> 1), (kt | j) != 0);
-        }
-        mma_commit(&empty[s]);
-      }
-      mma_commit(done);
-    }
-    __syncwarp();
-  } else {
-    // ---- epilogue: TMEM -> registers -> + bias -> bf16 -> global
-    griddep_wait();
-    const bool ok = mbar_wait(done, 0, abort);
-    tc_fence_after();
-    const int q = warp & 3;                 // TMEM lane quarter this warp may access
-    const int row = mt * 128 + q * 32 + lane;
-    if (ok) {
-#pragma unroll 1
-      for (int c0 = 0; c0 < kPfBN; c0 += 16) {
-        uint32_t r[16];
-        tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + c0, r);
-        tmem_wait_ld();
-        const int n0 = nt * kPfBN + c0;
-        if (row < g.M && n0 < g.N) {
-          float v[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            v[i] = __uint_as_float(r[i]);
-            if (g.bias != nullptr && n0 + i < g.N)
-              v[i] += bf16_bits_to_float(__ldg(reinterpret_cast<const uint16_t*>(g.bias) + n0 + i));
-          }
-          __nv_bfloat16* dst = g.out + static_cast<size_t>(row) * g.ldo + n0;
-          if (n0 + 16 <= g.N && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-            uint4 w0, w1;
-            w0.x = pack_bf16x2(v[0], v[1]);   w0.y = pack_bf16x2(v[2], v[3]);
-            w0.z = pack_bf16x2(v[4], v[5]);   w0.w = pack_bf16x2(v[6], v[7]);
-            w1.x = pack_bf16x2(v[8], v[9]);   w1.y = pack_bf16x2(v[10], v[11]);
-            w1.z = pack_bf16x2(v[12], v[13]); w1.w = pack_bf16x2(v[14], v[15]);
-            reinterpret_cast<uint4*>(dst)[0] = w0;
-            reinterpret_cast<uint4*>(dst)[1] = w1;
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (n0 + i < g.N) dst[i] = __float2bfloat16_rn(v[i]);
-          }
-        }
-      }
-    }
-    tc_fence_before();
-  }
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, kPfTmemCols);
-  }
-  if (abort) atomicOr(&g_gemm_error, kErrTimeout);
+// Balanced stream-K split: CTA c owns iterations [sk_begin(c), sk_begin(c+1)).
+__device__ __forceinline__ int sk_begin(int c, int total, int grid) {
+  return static_cast<int>((static_cast<long long>(c) * total) / grid);
 }
-
-// ===================================================================== decode
-template <int BN>
-struct DecodeCfg {
-  static constexpr int kW = kTileBytes;          // 128 weight rows
-  static constexpr int kSW = 1024;               // 2 weight scale atoms
-  static constexpr int kA = BN * 128;            // BN activation rows
-  static constexpr int kSA = 1024;               // 2 activation scale atoms
-  static constexpr int kStageBytes = kW + kSW + kA + kSA;
-  static constexpr int kStages = (200 * 1024) / kStageBytes > 10 ? 10 : (200 * 1024) / kStageBytes;
-  static constexpr int kSmem = kStages * kStageBytes + 1024 + 512;
-  static constexpr uint32_t kAccCols = 2 * BN;   // double-buffered accumulator
-  static constexpr uint32_t kTmemCols = (kAccCols + 16 <= 64) ? 64 : (kAccCols + 16 <= 128) ? 128 : 256;
-};
-
-__device__ __forceinline__ int64_t sk_begin(int c, int64_t total, int grid) {
-  return (static_cast<int64_t>(c) * total) / grid;
-}
-// CTA whose balanced range [sk_begin(c), sk_begin(c+1)) holds iteration `it`.
-__device__ __forceinline__ int sk_owner(int64_t it, int64_t total, int grid) {
-  int c = static_cast<int>((it * grid) / total);
+// CTA whose range holds iteration `it`.
+__device__ __forceinline__ int sk_owner(int it, int total, int grid) {
+  int c = static_cast<int>((static_cast<long long>(it) * grid) / total);
   while (c + 1 < grid && sk_begin(c + 1, total, grid) <= it) ++c;
   while (c > 0 && sk_begin(c, total, grid) > it) --c;
   return c;
 }
 
-// End (exclusive k-tile) of the segment that starts at k-tile ka of a tile
-// when `left` iterations of the CTA's range remain.
-__device__ __forceinline__ int64_t seg_end(int KT, int ka, int64_t left) {
-  const int64_t e = ka + left;
-  return e < KT ? e : KT;
+// 32 consecutive outputs of row m starting at column n: + bias, bf16, store.
+__device__ __forceinline__ void store_chunk(const GemmArgs& g, int m, int n, const float (&v)[32]) {
+  __nv_bfloat16* dst = g.out + static_cast<size_t>(m) * g.ldo + n;
+  const uint16_t* bias = reinterpret_cast<const uint16_t*>(g.bias);
+  if (n + 32 <= g.N && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+#pragma unroll
+    for (int c = 0; c < 32; c += 8) {
+      float b[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) b[i] = bias != nullptr ? bf16_bits_to_float(__ldg(bias + n + c + i)) : 0.f;
+      uint4 w;
+      w.x = pack_bf16x2(v[c] + b[0], v[c + 1] + b[1]);
+      w.y = pack_bf16x2(v[c + 2] + b[2], v[c + 3] + b[3]);
+      w.z = pack_bf16x2(v[c + 4] + b[4], v[c + 5] + b[5]);
+      w.w = pack_bf16x2(v[c + 6] + b[6], v[c + 7] + b[7]);
+      *reinterpret_cast<uint4*>(dst + c) = w;
+    }
+  } else {
+    for (int c = 0; c < 32; ++c)
+      if (n + c < g.N)
+        dst[c] = __float2bfloat16_rn(v[c] + (bias != nullptr ? bf16_bits_to_float(__ldg(bias + n + c)) : 0.f));
+  }
 }
 
-template <int BN>
-__global__ void __launch_bounds__(192, 1) gemm_decode_kernel(const GemmArgs g) {
-  using C = DecodeCfg<BN>;
+// 4 consecutive outputs of row m starting at column n: + bias, bf16, store.
+__device__ __forceinline__ void store_quad(const GemmArgs& g, int m, int n, float4 v) {
+  if (n >= g.N) return;
+  __nv_bfloat16* dst = g.out + static_cast<size_t>(m) * g.ldo + n;
+  const uint16_t* bias = reinterpret_cast<const uint16_t*>(g.bias);
+  float x[4] = {v.x, v.y, v.z, v.w};
+  if (bias != nullptr) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (n + i < g.N) x[i] += bf16_bits_to_float(__ldg(bias + n + i));
+  }
+  if (n + 4 <= g.N && (reinterpret_cast<uintptr_t>(dst) & 7) == 0) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (n + i < g.N) dst[i] = __float2bfloat16_rn(x[i]);
+  }
+}
+
+// At most 96 registers per thread (the bound asks for two CTAs' worth; the
+// shared-memory ring still allows one CTA per SM): the quantizer and fix-up
+// blocks of neighbouring calls then fit on the SM beside it, so the next
+// call's GEMM can take the SM and prefetch weights while they run.
+template <int kRowsA>
+__global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const GemmArgs g) {
+  using C = Cfg<kRowsA>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kRing);
   uint64_t* empty = full + C::kStages;
   uint64_t* acc_full = empty + C::kStages;
-  uint64_t* acc_empty = acc_full + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 2);
-  volatile uint32_t* last_flag = tmem_slot + 1;
+  uint64_t* acc_empty = acc_full + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KT = g.KT;
   const int cta = blockIdx.x;
-  const int64_t it0 = sk_begin(cta, g.total_iters, g.grid);
-  const int64_t it1 = sk_begin(cta + 1, g.total_iters, g.grid);
+  const int it0 = sk_begin(cta, g.total, g.grid);
+  const int it1 = sk_begin(cta + 1, g.total, g.grid);
   bool abort = false;
 
   if (threadIdx.x == 0) {
@@ -269,10 +171,8 @@ __global__ void __launch_bounds__(192, 1) gemm_decode_kernel(const GemmArgs g) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&acc_full[b], 1);
-      mbar_init(&acc_empty[b], 128);
-    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, kEpiThreads);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -283,174 +183,155 @@ __global__ void __launch_bounds__(192, 1) gemm_decode_kernel(const GemmArgs g) {
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The next kernel in the stream waits for this one to complete before it
+  // touches memory (griddepcontrol.wait), so it may be launched right away;
+  // its CTAs take SMs as this kernel's CTAs leave.
+  if (threadIdx.x == 0) griddep_launch_dependents();
 
   if (warp == 0) {
-    if (lane == 0) {
-      // ---- producer.  Weight tiles of the first stages are requested before
-      // waiting on the activation-producing kernel (programmatic dependent launch).
-      const uint32_t bytes = C::kStageBytes;
-      auto load_w = [&](int64_t it, uint8_t* st, uint64_t* bar) {
-        const int t = static_cast<int>(it / KT);
-        const int kt = static_cast<int>(it - static_cast<int64_t>(t) * KT);
-        bulk_g2s(st, g.w_codes + (static_cast<size_t>(t * KT + kt) << 14), kTileBytes, bar);
-        bulk_g2s(st + C::kW, g.w_scales + (static_cast<size_t>(t * 2 * KT + 2 * kt) << 9), 1024, bar);
-      };
-      auto load_a = [&](int64_t it, uint8_t* st, uint64_t* bar) {
-        const int kt = static_cast<int>(it % KT);
-        bulk_g2s(st + C::kW + C::kSW, g.a_codes + (static_cast<size_t>(kt) << 14), C::kA, bar);
-        bulk_g2s(st + C::kW + C::kSW + C::kA, g.a_scales + (static_cast<size_t>(2 * kt) << 9), 1024, bar);
-      };
-      const int npre = static_cast<int>((it1 - it0) < C::kStages ? (it1 - it0) : C::kStages);
-      for (int i = 0; i < npre; ++i) {
-        mbar_arrive_expect_tx(&full[i], bytes);
-        load_w(it0 + i, smem + i * C::kStageBytes, &full[i]);
+    // ---- producer.  A stage is one 256-wide k-step of one output tile.
+    auto w_load = [&](int it, uint8_t* st, uint64_t* bar) {
+      const int t = it / KT, kt = it - t * KT;
+      const int nt = t % g.n_tiles;
+      for (int q = 0; q < 2; ++q) {
+        const int rt = 2 * nt + q;
+        if (rt < g.w_tiles) {
+          bulk_g2s(st + q * kTileBytes, g.w_codes + (static_cast<size_t>(rt * KT + kt) << 14), kTileBytes, bar);
+          bulk_g2s(st + C::kW + C::kA + C::kSA + q * 1024, g.w_scales + (static_cast<size_t>(rt * KT + kt) << 10),
+                   1024, bar);
+        }
       }
+    };
+    auto a_load = [&](int it, uint8_t* st, uint64_t* bar) {
+      const int t = it / KT, kt = it - t * KT;
+      const int mt = t / g.n_tiles;
+      bulk_g2s(st + C::kW, g.a_codes + (static_cast<size_t>(mt * KT + kt) << 14), C::kALoad, bar);
+      bulk_g2s(st + C::kW + C::kA, g.a_scales + (static_cast<size_t>(mt * KT + kt) << 10), 1024, bar);
+    };
+    auto stage_bytes = [&](int it) -> uint32_t {
+      const int nt = (it / KT) % g.n_tiles;
+      const int nsub = (2 * nt + 1 < g.w_tiles) ? 2 : 1;
+      return static_cast<uint32_t>(C::kALoad + C::kSA + nsub * (kTileBytes + 1024));
+    };
+    const int n_iter = it1 - it0;
+    const int npre = n_iter < C::kStages ? n_iter : C::kStages;
+    // Lane i issues prologue stage i (one copy instruction per lane rather
+    // than a serial chain).  Weights are requested before waiting on the
+    // activation-producing kernel: the kernel this one follows never writes
+    // them (the weight repack ends with an ordinary launch).
+    if (lane < npre) {
+      uint8_t* st = smem + lane * C::kStageBytes;
+      mbar_arrive_expect_tx(&full[lane], stage_bytes(it0 + lane));
+      w_load(it0 + lane, st, &full[lane]);
       griddep_wait();
-      for (int i = 0; i < npre; ++i) load_a(it0 + i, smem + i * C::kStageBytes, &full[i]);
-      uint32_t ls = npre;
-      for (int64_t it = it0 + npre; it < it1; ++it, ++ls) {
-        const int s = ls % C::kStages;
-        const uint32_t ph = (ls / C::kStages) & 1;
+      a_load(it0 + lane, st, &full[lane]);
+    }
+    __syncwarp();
+    if (lane == 0) {
+      for (int i = npre; i < n_iter; ++i) {
+        const int s = i % C::kStages;
+        const uint32_t ph = (i / C::kStages) & 1;
         if (!mbar_wait(&empty[s], ph ^ 1, abort)) break;
         uint8_t* st = smem + s * C::kStageBytes;
-        mbar_arrive_expect_tx(&full[s], bytes);
-        load_w(it, st, &full[s]);
-        load_a(it, st, &full[s]);
+        mbar_arrive_expect_tx(&full[s], stage_bytes(it0 + i));
+        w_load(it0 + i, st, &full[s]);
+        a_load(it0 + i, st, &full[s]);
       }
     }
     __syncwarp();   // whole warp reaches the final barrier converged
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---- MMA issuer: one accumulator per tile segment, double-buffered
-      const uint32_t sfa = tmem + C::kAccCols;
-      const uint32_t sfb = tmem + C::kAccCols + 8;
-      uint32_t ls = 0;
-      int seg = 0;
-      for (int64_t it = it0; it < it1 && !abort; ++seg) {
-        const int t = static_cast<int>(it / KT);
-        const int ka = static_cast<int>(it - static_cast<int64_t>(t) * KT);
-        const int kb = static_cast<int>(seg_end(KT, ka, it1 - it));
-        const int buf = seg & 1;
-        const uint32_t use = seg >> 1;
-        if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort)) break;
+      // ---- MMA issuer: one accumulator, one segment (part of a tile) at a time
+      const uint32_t sfa = tmem + C::kSfa, sfb = tmem + C::kSfb;
+      int i = 0, seg = 0, kt = it0 % KT;
+      for (int it = it0; it < it1 && !abort; ++seg) {
+        const int len = (KT - kt) < (it1 - it) ? (KT - kt) : (it1 - it);
+        if (!mbar_wait(acc_empty, (seg & 1) ^ 1, abort)) break;
         tc_fence_after();
-        const uint32_t acc = tmem + buf * BN;
-        for (int kt = ka; kt < kb; ++kt, ++ls) {
-          const int s = ls % C::kStages;
-          const uint32_t ph = (ls / C::kStages) & 1;
+        for (int j = 0; j < len; ++j, ++i) {
+          const int s = i % C::kStages;
+          const uint32_t ph = (i / C::kStages) & 1;
           if (!mbar_wait(&full[s], ph, abort)) break;
           tc_fence_after();
           const uint32_t base = smem_u32(smem + s * C::kStageBytes);
-          const uint32_t w_s = base, sw_s = base + C::kW, a_s = sw_s + C::kSW, sa_s = a_s + C::kA;
-          tmem_cp_scales(sfa + 0, sdesc_scales(sw_s));
-          tmem_cp_scales(sfa + 4, sdesc_scales(sw_s + 512));
-          tmem_cp_scales(sfb + 0, sdesc_scales(sa_s));
-          tmem_cp_scales(sfb + 4, sdesc_scales(sa_s + 512));
+          const uint32_t w_s = base, a_s = base + C::kW, sa_s = a_s + C::kA, sw_s = sa_s + C::kSA;
+          tmem_cp_scales(sfa + 0, sdesc_scales(sa_s));
+          tmem_cp_scales(sfa + 4, sdesc_scales(sa_s + 512));
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t id = idesc_mxf4(128, BN, (j & 1) * 2, (j & 1) * 2);
-            mma_mxf4(acc, sdesc_sw128(w_s + 32 * j), sdesc_sw128(a_s + 32 * j), id, sfa + 4 * (j >> 1),
-                     sfb + 4 * (j >> 1), (kt != ka || j != 0) ? 1u : 0u);
+          for (int a = 0; a < 2; ++a)
+#pragma unroll
+            for (int q = 0; q < 2; ++q) tmem_cp_scales(sfb + a * 8 + q * 4, sdesc_scales(sw_s + q * 1024 + a * 512));
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t id = idesc_mxf4(128, kTileN, (q & 1) * 2, (q & 1) * 2);
+            mma_mxf4(tmem, sdesc_sw128(a_s + 32 * q), sdesc_sw128(w_s + 32 * q), id, sfa + 4 * (q >> 1),
+                     sfb + 8 * (q >> 1), (j != 0 || q != 0) ? 1u : 0u);
           }
           mma_commit(&empty[s]);
         }
-        mma_commit(&acc_full[buf]);
-        it += kb - ka;
+        mma_commit(acc_full);
+        it += len;
+        kt = 0;
       }
     }
     __syncwarp();
   } else {
-    // ---- epilogue (128 threads): lane = weight row n, columns = activation rows m
+    // ---- epilogue: warp w drains accumulator rows 32*(w%4).., columns 128*h..
     griddep_wait();
     const int q = warp & 3;
-    const int rl = q * 32 + lane;            // row inside the 128-row weight tile
-    int seg = 0;
-    for (int64_t it = it0; it < it1; ++seg) {
-      const int t = static_cast<int>(it / KT);
-      const int ka = static_cast<int>(it - static_cast<int64_t>(t) * KT);
-      const int kb = static_cast<int>(seg_end(KT, ka, it1 - it));
-      const int buf = seg & 1;
-      const uint32_t use = seg >> 1;
-      const bool ok = mbar_wait(&acc_full[buf], use & 1, abort);
+    const int h = (warp - 2) >> 2;
+    const int rl = q * 32 + lane;                 // accumulator row = activation row in the tile
+    const bool warp_live = q * 32 < kRowsA;       // quarters beyond kRowsA rows hold nothing
+    int seg = 0, kt = it0 % KT;
+    for (int it = it0; it < it1; ++seg) {
+      const int len = (KT - kt) < (it1 - it) ? (KT - kt) : (it1 - it);
+      const int t = it / KT;
+      const int mt = t / g.n_tiles, nt = t - mt * g.n_tiles;
+      const bool ok = mbar_wait(acc_full, seg & 1, abort);
       tc_fence_after();
-      float v[BN];
-      if (ok) {
+      const int m = mt * 128 + rl;
+      const int n0 = nt * kTileN + h * 128;
+      const bool live = warp_live && rl < kRowsA && m < g.M;
+      const bool whole = kt == 0 && len == KT;
+      const int slot = 2 * cta + (it == it0 ? 0 : 1);
+      // Two passes of 64 columns; the accumulator is released right after the
+      // second pass is loaded.  A whole tile is stored; a part of a tile is
+      // published as fp32 for the fix-up kernel that follows.
 #pragma unroll
-        for (int c0 = 0; c0 < BN; c0 += 16) {
-          uint32_t r[16];
-          tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + c0, r);
+      for (int pass = 0; pass < 2; ++pass) {
+        float v[64];
+        if (warp_live) {
+          uint32_t r[64];
+#pragma unroll
+          for (int c0 = 0; c0 < 64; c0 += 16)
+            tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128 + pass * 64 + c0,
+                      *reinterpret_cast<uint32_t(*)[16]>(&r[c0]));
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) v[c0 + i] = __uint_as_float(r[i]);
+          for (int c = 0; c < 64; ++c) v[c] = ok ? __uint_as_float(r[c]) : 0.f;
         }
-      } else {
+        if (pass == 1) {
+          tc_fence_before();
+          mbar_arrive(acc_empty);                 // accumulator free for the next segment
+        }
+        if (!live) continue;
+        if (whole) {
 #pragma unroll
-        for (int i = 0; i < BN; ++i) v[i] = 0.f;
+          for (int c0 = 0; c0 < 64; c0 += 32) {
+            float chunk[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) chunk[c] = v[c0 + c];
+            store_chunk(g, m, n0 + pass * 64 + c0, chunk);
+          }
+        } else {
+          float4* P = reinterpret_cast<float4*>(g.partials + (static_cast<size_t>(slot) * kRowsA + rl) * kTileN +
+                                                h * 128 + pass * 64);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) __stcg(P + c, make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));
+        }
       }
-      tc_fence_before();
-      mbar_arrive(&acc_empty[buf]);
-
-      const int n = t * 128 + rl;
-      const float b = (g.bias != nullptr && n < g.N)
-                          ? bf16_bits_to_float(__ldg(reinterpret_cast<const uint16_t*>(g.bias) + n))
-                          : 0.f;
-      const bool whole = (ka == 0 && kb == KT);
-      if (whole) {
-        if (n < g.N) {
-#pragma unroll
-          for (int m = 0; m < BN; ++m)
-            if (m < g.M) g.out[static_cast<size_t>(m) * g.ldo + n] = __float2bfloat16_rn(v[m] + b);
-        }
-      } else {
-        // partial tile: publish the fp32 partial, last finisher sums in order
-        const int slot = 2 * cta + (it == it0 ? 0 : 1);
-        float* P = g.partials + static_cast<size_t>(slot) * (BN * 128);
-#pragma unroll
-        for (int m = 0; m < BN; ++m) __stcg(P + m * 128 + rl, v[m]);
-        __threadfence();
-        named_barrier(1, 128);
-        const int64_t tb = static_cast<int64_t>(t) * KT;
-        const int c_lo = sk_owner(tb, g.total_iters, g.grid);
-        const int c_hi = sk_owner(tb + KT - 1, g.total_iters, g.grid);
-        if (threadIdx.x == 64) {
-          // Arrival count of this call on tile t.  A word whose tag is not this
-          // call's counts as zero, so the workspace needs no initialisation.
-          unsigned long long* tk = &g.tickets[t];
-          unsigned long long cur = atomicAdd(tk, 0ull);
-          unsigned long long before;
-          while (true) {
-            before = ((cur >> 16) == g.tag) ? (cur & 0xFFFFull) : 0ull;
-            const unsigned long long want = (g.tag << 16) | (before + 1);
-            const unsigned long long seen = atomicCAS(tk, cur, want);
-            if (seen == cur) break;
-            cur = seen;
-          }
-          *last_flag = (before == static_cast<unsigned long long>(c_hi - c_lo)) ? 1u : 0u;
-        }
-        named_barrier(1, 128);
-        if (*last_flag) {
-          __threadfence();
-          float sum[BN];
-#pragma unroll
-          for (int m = 0; m < BN; ++m) sum[m] = 0.f;
-          for (int cc = c_lo; cc <= c_hi; ++cc) {
-            const int64_t b0 = sk_begin(cc, g.total_iters, g.grid);
-            const int sl = 2 * cc + ((b0 / KT) == t ? 0 : 1);
-            const float* Q = g.partials + static_cast<size_t>(sl) * (BN * 128);
-#pragma unroll
-            for (int m = 0; m < BN; ++m)
-              if (m < g.M) sum[m] += __ldcg(Q + m * 128 + rl);
-          }
-          if (n < g.N) {
-#pragma unroll
-            for (int m = 0; m < BN; ++m)
-              if (m < g.M) g.out[static_cast<size_t>(m) * g.ldo + n] = __float2bfloat16_rn(sum[m] + b);
-          }
-          if (threadIdx.x == 64) atomicExch(&g.tickets[t], 0ull);   // leave the ticket clean
-        }
-        named_barrier(1, 128);
-      }
-      it += kb - ka;
+      it += len;
+      kt = 0;
     }
   }
   __syncthreads();
@@ -459,6 +340,66 @@ __global__ void __launch_bounds__(192, 1) gemm_decode_kernel(const GemmArgs g) {
     tmem_dealloc(tmem, C::kTmemCols);
   }
   if (abort) atomicOr(&g_gemm_error, kErrTimeout);
+}
+
+// ===================================================================== fix-up
+// Tiles split between CTAs, summed after the GEMM.  Block (x, y) takes
+// split tile x, float4 groups [512 y, 512 y + 512) of it (group gi = row
+// gi / 64, columns 4 * (gi % 64)..); each group adds the contributors' fp32
+// parts in CTA order (deterministic), then the bias, and is stored as bf16.
+// Loads of 4 contributors x 2 groups per thread are in flight together.
+constexpr int kMaxSplitTiles = kMaxStreamKCtas;
+constexpr int kFixupGroups = 512;
+struct FixupArgs {
+  GemmArgs g;
+  int tiles[kMaxSplitTiles];
+};
+
+// At most 64 registers per thread, so a waiting fix-up block fits on an SM
+// next to a resident GEMM CTA (of the next call).
+__global__ void __launch_bounds__(256, 4) gemm_fixup_kernel(const __grid_constant__ FixupArgs f) {
+  griddep_launch_dependents();
+  griddep_wait();                                   // the GEMM's parts are complete and visible
+  const GemmArgs& g = f.g;
+  const int KT = g.KT;
+  const int t = f.tiles[blockIdx.x];
+  const int mt = t / g.n_tiles, nt = t - mt * g.n_tiles;
+  const int c_lo = sk_owner(t * KT, g.total, g.grid);
+  const int c_hi = sk_owner(t * KT + KT - 1, g.total, g.grid);
+  const int rows = (g.M - mt * 128) < g.rows_a ? (g.M - mt * 128) : g.rows_a;
+  const int groups = rows * (kTileN / 4);
+  const int g0 = blockIdx.y * kFixupGroups + threadIdx.x;   // this thread: groups g0 and g0 + 256
+  if (g0 >= groups) return;
+  float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+  for (int cg = c_lo; cg <= c_hi; cg += 4) {
+    float4 p[4][2];
+#pragma unroll
+    for (int jc = 0; jc < 4; ++jc) {
+      const int cc = cg + jc;
+      if (cc > c_hi) continue;
+      const int sl = 2 * cc + (sk_begin(cc, g.total, g.grid) / KT == t ? 0 : 1);
+      const float4* Q = reinterpret_cast<const float4*>(g.partials + static_cast<size_t>(sl) * g.rows_a * kTileN);
+#pragma unroll
+      for (int j = 0; j < 2; ++j)
+        if (g0 + 256 * j < groups) p[jc][j] = __ldcg(Q + g0 + 256 * j);
+    }
+#pragma unroll
+    for (int jc = 0; jc < 4; ++jc) {
+      if (cg + jc > c_hi) continue;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        acc[j].x += p[jc][j].x;
+        acc[j].y += p[jc][j].y;
+        acc[j].z += p[jc][j].z;
+        acc[j].w += p[jc][j].w;
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int gi = g0 + 256 * j;
+    if (gi < groups) store_quad(g, mt * 128 + gi / (kTileN / 4), nt * kTileN + 4 * (gi % (kTileN / 4)), acc[j]);
+  }
 }
 
 // ===================================================================== host
@@ -475,22 +416,18 @@ static cudaError_t ensure_smem(Kern k, int smem, int dev, int which) {
   return cudaSuccess;
 }
 
-size_t gemm_streamk_workspace_bytes(int M, int N, int K) {
-  (void)M;
+size_t gemm_streamk_workspace_bytes(int M, int N, int K, int grid) {
+  (void)N;
   (void)K;
-  const size_t partials = static_cast<size_t>(2) * kMaxStreamKCtas * kDecodeMaxM * 128 * sizeof(float);
-  const size_t tickets = static_cast<size_t>(ceil_div(N, 128)) * sizeof(unsigned long long);
-  return partials + ((tickets + 255) & ~static_cast<size_t>(255));
+  return static_cast<size_t>(2) * grid * gemm_rows_a(M) * kTileN * sizeof(float);
 }
 
-// Launch with programmatic stream serialization: the kernel may start while
-// the previous kernel in the stream (the activation quantizer) is finishing;
-// it waits on it with griddepcontrol.wait before reading activations.
-template <typename Kern>
-static cudaError_t launch_pdl(Kern k, dim3 grid, int smem, cudaStream_t s, const GemmArgs& a) {
+// Launch as a programmatic dependent of the previous kernel in the stream.
+template <typename Kern, typename Args>
+static cudaError_t launch_pdl(Kern k, int grid, int threads, int smem, cudaStream_t s, const Args& a) {
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(192, 1, 1);
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -501,24 +438,15 @@ static cudaError_t launch_pdl(Kern k, dim3 grid, int smem, cudaStream_t s, const
   return cudaLaunchKernelEx(&cfg, k, a);
 }
 
-template <int BN>
-static cudaError_t launch_decode(GemmArgs& a, const DeviceInfo& dev, cudaStream_t s, int which) {
-  using C = DecodeCfg<BN>;
-  cudaError_t e = ensure_smem(gemm_decode_kernel<BN>, C::kSmem, dev.device, which);
+template <int kRowsA>
+static cudaError_t launch_rows(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t s, int which) {
+  using C = Cfg<kRowsA>;
+  cudaError_t e = ensure_smem(gemm_kernel<kRowsA>, C::kSmem, dev.device, which);
   if (e != cudaSuccess) return e;
-  return launch_pdl(gemm_decode_kernel<BN>, dim3(a.grid), C::kSmem, s, a);
+  return launch_pdl(gemm_kernel<kRowsA>, a.grid, kThreads, C::kSmem, s, a);
 }
 
-// 48-bit tag distinguishing this call's stream-K tickets from stale words.
-static unsigned long long next_call_tag() {
-  static std::atomic<unsigned long long> seq{0};
-  unsigned long long x = seq.fetch_add(1, std::memory_order_relaxed) + 0x632BE59BD9B4E019ull;
-  x ^= x >> 31;
-  x *= 0x9E3779B97F4A7C15ull;
-  x ^= x >> 29;
-  x &= 0xFFFFFFFFFFFFull;
-  return x == 0 ? 1 : x;
-}
+int gemm_grid(const DeviceInfo& dev) { return dev.sm_count < kMaxStreamKCtas ? dev.sm_count : kMaxStreamKCtas; }
 
 cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_t s) {
   GemmArgs a{};
@@ -535,24 +463,45 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
   a.N = p.N;
   a.KT = static_cast<int>(Kp / kKTile);
   a.w_tiles = static_cast<int>(Np / 128);
-
-  if (p.M <= kDecodeMaxM) {
-    a.total_iters = static_cast<int64_t>(a.w_tiles) * a.KT;
-    int grid = dev.sm_count < kMaxStreamKCtas ? dev.sm_count : kMaxStreamKCtas;
-    if (grid > a.total_iters) grid = static_cast<int>(a.total_iters);
-    a.grid = grid;
-    a.partials = static_cast<float*>(p.workspace);
-    const size_t partial_bytes = static_cast<size_t>(2) * kMaxStreamKCtas * kDecodeMaxM * 128 * sizeof(float);
-    a.tickets = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(p.workspace) + partial_bytes);
-    a.tag = next_call_tag();
-    if (p.M <= 16) return launch_decode<16>(a, dev, s, 1);
-    if (p.M <= 32) return launch_decode<32>(a, dev, s, 2);
-    return launch_decode<64>(a, dev, s, 3);
+  a.n_tiles = static_cast<int>(ceil_div(p.N, kTileN));
+  const int64_t tiles = ceil_div(p.M, 128) * static_cast<int64_t>(a.n_tiles);
+  a.total = static_cast<int>(tiles * a.KT);
+  int grid = gemm_grid(dev);
+  if (grid > a.total) grid = a.total;
+  a.grid = grid;
+  a.rows_a = gemm_rows_a(p.M);
+  a.partials = static_cast<float*>(p.workspace);
+  cudaError_t e;
+  switch (a.rows_a) {
+    case 16: e = launch_rows<16>(a, dev, s, 0); break;
+    case 32: e = launch_rows<32>(a, dev, s, 1); break;
+    case 64: e = launch_rows<64>(a, dev, s, 2); break;
+    default: e = launch_rows<128>(a, dev, s, 3); break;
   }
-  cudaError_t e = ensure_smem(gemm_prefill_kernel, kPfSmem, dev.device, 0);
   if (e != cudaSuccess) return e;
-  dim3 grid(static_cast<unsigned>(ceil_div(p.N, kPfBN)), static_cast<unsigned>(ceil_div(p.M, 128)));
-  return launch_pdl(gemm_prefill_kernel, grid, kPfSmem, s, a);
+  // Tiles that a CTA boundary cuts are summed by the fix-up kernel.
+  FixupArgs f;
+  f.g = a;
+  int n_split = 0, prev = -1;
+  for (int c = 1; c < grid; ++c) {
+    const int b = static_cast<int>((static_cast<long long>(c) * a.total) / grid);
+    if (b % a.KT == 0) continue;
+    const int t = b / a.KT;
+    if (t != prev) f.tiles[n_split++] = t;
+    prev = t;
+  }
+  if (n_split == 0) return cudaSuccess;
+  const int chunks = static_cast<int>(ceil_div(static_cast<int64_t>(a.rows_a) * (kTileN / 4), kFixupGroups));
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(n_split), static_cast<unsigned>(chunks), 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_fixup_kernel, f);
 }
 
 uint32_t gemm_read_clear_error() {

@@ -26,6 +26,9 @@ constexpr uint32_t kErrTimeout = 1u;
 constexpr int kMaxStreamKCtas = 256;
 // Largest activation row count served by the swap-AB decode kernel.
 constexpr int kDecodeMaxM = 64;
+// Activation rows of a 128-row tile the GEMM loads: 16, 32 or 64 when
+// M <= kDecodeMaxM (only those rows of the tiled activations are read), else 128.
+inline int gemm_rows_a(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128)); }
 
 struct DeviceInfo {
   int device;
@@ -36,8 +39,9 @@ struct DeviceInfo {
 cudaError_t current_device_info(DeviceInfo* out);
 
 // quant.cu
+// tiled_rows: rows of the tiled output to write (0 = all Rp rows).
 cudaError_t launch_quant(const void* x, int M, int K, int ldx, uint8_t* codes, uint8_t* scales, bool tiled,
-                         const DeviceInfo& dev, cudaStream_t s);
+                         int tiled_rows, const DeviceInfo& dev, cudaStream_t s);
 cudaError_t launch_pack(const uint8_t* codes, const uint8_t* scales, int batch, int R, int K, uint8_t* packed,
                         const DeviceInfo& dev, cudaStream_t s);
 uint32_t quant_read_clear_error();
@@ -53,7 +57,10 @@ struct GemmProblem {
   void* workspace;          // stream-K partials + tickets
   size_t workspace_bytes;
 };
-size_t gemm_streamk_workspace_bytes(int M, int N, int K);
+// Stream-K CTAs of the GEMM on this device, and the partial-sum + ticket
+// workspace it needs for that grid.
+int gemm_grid(const DeviceInfo& dev);
+size_t gemm_streamk_workspace_bytes(int M, int N, int K, int grid);
 cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_t s);
 uint32_t gemm_read_clear_error();
 

@@ -24,7 +24,7 @@
 namespace mx {
 
 // Upper bound of the scratch a call may use.
-constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(24) << 20;   // 24 MiB
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(48) << 20;   // 48 MiB
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 

@@ -30,8 +30,10 @@ __device__ __forceinline__ uint32_t e2m1_magnitude(float a) {
 
 // One warp per unit of (row, 256 consecutive elements): lane l holds
 // elements 8l..8l+7, four lanes form one 32-element block.
+// At most 64 registers per thread, so a quantizer block fits on an SM next
+// to a resident GEMM CTA.
 template <bool kTiled>
-__global__ void __launch_bounds__(256) quant_kernel(const uint16_t* __restrict__ x, int M, int K, int ldx,
+__global__ void __launch_bounds__(256, 4) quant_kernel(const uint16_t* __restrict__ x, int M, int K, int ldx,
                                                     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                                                     int rows, int KT, bool vec_ok) {
   const int lane = threadIdx.x & 31;
@@ -39,56 +41,72 @@ __global__ void __launch_bounds__(256) quant_kernel(const uint16_t* __restrict__
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int64_t units = static_cast<int64_t>(rows) * KT;
   const int nb = (K + 31) >> 5;   // scale blocks per row
-  // let a GEMM launched behind this kernel set up and prefetch weights now
+  // Launched as a programmatic dependent: let the GEMM behind this kernel
+  // start its set-up and weight prefetch now, but touch memory only after the
+  // kernel before this one (which may produce x or still read the outputs'
+  // buffers) has completed.
   griddep_launch_dependents();
+  griddep_wait();
 
-  for (int64_t u = warp; u < units; u += nwarps) {
-    const int r = static_cast<int>(u / KT);
-    const int kt = static_cast<int>(u - static_cast<int64_t>(r) * KT);
-    const int e0 = kt * 256 + lane * 8;
-
-    uint16_t v[8];
-    if (r < M && vec_ok && e0 + 8 <= K) {
-      const uint4 q = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(r) * ldx + e0));
-      v[0] = q.x & 0xFFFF; v[1] = q.x >> 16; v[2] = q.y & 0xFFFF; v[3] = q.y >> 16;
-      v[4] = q.z & 0xFFFF; v[5] = q.z >> 16; v[6] = q.w & 0xFFFF; v[7] = q.w >> 16;
-    } else {
+  // Four units per warp per pass: their loads are all in flight together.
+  for (int64_t u0 = warp; u0 < units; u0 += 4 * nwarps) {
+    uint16_t v[4][8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        v[i] = (r < M && e0 + i < K) ? x[static_cast<size_t>(r) * ldx + e0 + i] : static_cast<uint16_t>(0);
+    for (int j = 0; j < 4; ++j) {
+      const int64_t u = u0 + j * nwarps;
+      const int r = static_cast<int>(u / KT);
+      const int kt = static_cast<int>(u - static_cast<int64_t>(r) * KT);
+      const int e0 = kt * 256 + lane * 8;
+      if (u < units && r < M && vec_ok && e0 + 8 <= K) {
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(r) * ldx + e0));
+        v[j][0] = q.x & 0xFFFF; v[j][1] = q.x >> 16; v[j][2] = q.y & 0xFFFF; v[j][3] = q.y >> 16;
+        v[j][4] = q.z & 0xFFFF; v[j][5] = q.z >> 16; v[j][6] = q.w & 0xFFFF; v[j][7] = q.w >> 16;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          v[j][i] = (u < units && r < M && e0 + i < K) ? x[static_cast<size_t>(r) * ldx + e0 + i]
+                                                       : static_cast<uint16_t>(0);
+      }
     }
-
-    // Block amax on the magnitude bits (bf16 magnitudes order like integers;
-    // Inf and NaN sort above every finite value).
-    uint32_t am = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) am = max(am, static_cast<uint32_t>(v[i] & 0x7FFF));
-    am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
-    am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
+    for (int j = 0; j < 4; ++j) {
+      const int64_t u = u0 + j * nwarps;
+      if (u >= units) break;     // warp-uniform
+      const int r = static_cast<int>(u / KT);
+      const int kt = static_cast<int>(u - static_cast<int64_t>(r) * KT);
+      const int e0 = kt * 256 + lane * 8;
 
-    const uint32_t ef = am >> 7;                 // biased exponent field of amax
-    const bool nonfinite = ef == 0xFF;
-    // floor(log2 amax) - 2 as an E8M0 byte, clamped at 0 (zero / subnormal amax)
-    const uint32_t sbyte = nonfinite ? 0xFFu : (ef > 2 ? ef - 2 : 0u);
-    const float inv = __uint_as_float((254u - (nonfinite ? 0u : sbyte)) << 23);   // 2^(127 - sbyte)
-
-    uint32_t packed = 0;
+      // Block amax on the magnitude bits (bf16 magnitudes order like
+      // integers; Inf and NaN sort above every finite value).
+      uint32_t am = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float a = __uint_as_float(static_cast<uint32_t>(v[i] & 0x7FFF) << 16) * inv;
-      uint32_t c = e2m1_magnitude(a) | ((v[i] >> 12) & 8u);
-      if (nonfinite) c = 0;
-      packed |= c << (4 * i);
-    }
+      for (int i = 0; i < 8; ++i) am = max(am, static_cast<uint32_t>(v[j][i] & 0x7FFF));
+      am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
+      am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
 
-    const int blk = kt * 8 + (lane >> 2);
-    const bool blk_real = r < M && blk < nb;
-    const int j0 = kt * 128 + lane * 4;   // first code byte of this lane in the row
-    if (kTiled) {
-      *reinterpret_cast<uint32_t*>(codes + tiled_code_offset(r, j0, KT)) = packed;
-      if ((lane & 3) == 0) scales[tiled_scale_offset(r, blk, KT)] = blk_real ? static_cast<uint8_t>(sbyte) : 0x7F;
-    } else {
-      if (r < M) {
+      const uint32_t ef = am >> 7;               // biased exponent field of amax
+      const bool nonfinite = ef == 0xFF;
+      // floor(log2 amax) - 2 as an E8M0 byte, clamped at 0 (zero / subnormal amax)
+      const uint32_t sbyte = nonfinite ? 0xFFu : (ef > 2 ? ef - 2 : 0u);
+      const float inv = __uint_as_float((254u - (nonfinite ? 0u : sbyte)) << 23);   // 2^(127 - sbyte)
+
+      uint32_t packed = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float a = __uint_as_float(static_cast<uint32_t>(v[j][i] & 0x7FFF) << 16) * inv;
+        uint32_t c = e2m1_magnitude(a) | ((v[j][i] >> 12) & 8u);
+        if (nonfinite) c = 0;
+        packed |= c << (4 * i);
+      }
+
+      const int blk = kt * 8 + (lane >> 2);
+      const bool blk_real = r < M && blk < nb;
+      const int j0 = kt * 128 + lane * 4;   // first code byte of this lane in the row
+      if (kTiled) {
+        *reinterpret_cast<uint32_t*>(codes + tiled_code_offset(r, j0, KT)) = packed;
+        if ((lane & 3) == 0)
+          scales[tiled_scale_offset(r, blk, KT)] = blk_real ? static_cast<uint8_t>(sbyte) : 0x7F;
+      } else if (r < M) {
         const int row_bytes = K >> 1;
         uint8_t* dst = codes + static_cast<size_t>(r) * row_bytes + j0;
         if (e0 + 8 <= K && (reinterpret_cast<uintptr_t>(dst) & 3) == 0) {
@@ -170,23 +188,50 @@ static int grid_for(int64_t work_items, int per_block, const DeviceInfo& dev) {
   return static_cast<int>(blocks);
 }
 
-cudaError_t launch_quant(const void* x, int M, int K, int ldx, uint8_t* codes, uint8_t* scales, bool tiled,
-                         const DeviceInfo& dev, cudaStream_t s) {
-  const bool vec_ok = (reinterpret_cast<uintptr_t>(x) & 15) == 0 && (ldx % 8) == 0;
-  if (tiled) {
-    const int rows = static_cast<int>(padded_rows(M));
-    const int KT = static_cast<int>(padded_k(K) / kKTile);
-    const int grid = grid_for(static_cast<int64_t>(rows) * KT, 8, dev);
-    quant_kernel<true><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x), M, K, ldx, codes, scales, rows, KT,
-                                            vec_ok);
-  } else {
-    const int KT = static_cast<int>(ceil_div(K, kKTile));
-    const int grid = grid_for(static_cast<int64_t>(M) * KT, 8, dev);
-    quant_kernel<false><<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(x), M, K, ldx, codes, scales, M, KT,
-                                             vec_ok);
-  }
-  return cudaGetLastError();
+template <typename Kern, typename... Args>
+static cudaError_t launch_dependent(Kern k, int grid, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, args...);
 }
+
+// Decode-sized inputs (a few rows): at most one 256-thread CTA per SM, which
+// fits next to a resident GEMM CTA, so the whole grid starts (and triggers
+// its dependent GEMM) at once.  Larger inputs: up to eight CTAs per SM.
+static int quant_grid(int64_t units, int M, const DeviceInfo& dev) {
+  int64_t blocks = (units + 7) / 8;
+  const int64_t cap = static_cast<int64_t>(dev.sm_count) * (M <= kDecodeMaxM ? 1 : 8);
+  if (blocks > cap) blocks = cap;
+  return static_cast<int>(blocks < 1 ? 1 : blocks);
+}
+
+cudaError_t launch_quant(const void* x, int M, int K, int ldx, uint8_t* codes, uint8_t* scales, bool tiled,
+                         int tiled_rows, const DeviceInfo& dev, cudaStream_t s) {
+  const bool vec_ok = (reinterpret_cast<uintptr_t>(x) & 15) == 0 && (ldx % 8) == 0;
+  const uint16_t* xs = static_cast<const uint16_t*>(x);
+  if (tiled) {
+    const int rows = tiled_rows > 0 ? tiled_rows : static_cast<int>(padded_rows(M));
+    const int KT = static_cast<int>(padded_k(K) / kKTile);
+    const int grid = quant_grid(static_cast<int64_t>(rows) * KT, M, dev);
+    return launch_dependent(quant_kernel<true>, grid, s, xs, M, K, ldx, codes, scales, rows, KT, vec_ok);
+  }
+  const int KT = static_cast<int>(ceil_div(K, kKTile));
+  const int grid = quant_grid(static_cast<int64_t>(M) * KT, M, dev);
+  return launch_dependent(quant_kernel<false>, grid, s, xs, M, K, ldx, codes, scales, M, KT, vec_ok);
+}
+
+// Empty kernel launched (normally) after the repack: a programmatic
+// dependent launched behind it, such as the GEMM, may prefetch weights before
+// its dependency wait, and this guarantees the repack has fully completed.
+__global__ void ordering_kernel() {}
 
 cudaError_t launch_pack(const uint8_t* codes, const uint8_t* scales, int batch, int R, int K, uint8_t* packed,
                         const DeviceInfo& dev, cudaStream_t s) {
@@ -200,6 +245,9 @@ cudaError_t launch_pack(const uint8_t* codes, const uint8_t* scales, int batch, 
   if (e != cudaSuccess) return e;
   pack_scales_kernel<<<grid_for(sb * batch, 256, dev), 256, 0, s>>>(scales, batch, R, K, packed, per_batch,
                                                                     static_cast<size_t>(cb), KT, sb);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ordering_kernel<<<1, 32, 0, s>>>();
   return cudaGetLastError();
 }
 
