@@ -12,21 +12,11 @@
 #include "internal.h"
 #include "layout.cuh"
 #include "ptx.cuh"
+#include "quant_math.cuh"
 
 namespace mx {
 
 static __device__ uint32_t g_quant_error;
-
-// E2M1 magnitude index of a non-negative float by round-to-nearest-even on
-// the grid {0, .5, 1, 1.5, 2, 3, 4, 6}, saturating at 6.  Each comparison is
-// one midpoint of the grid; a value exactly on a midpoint goes to the
-// neighbour with the even code (the comparison is strict towards the odd
-// code: 0.25 -> 0, 0.75 -> 2, 1.25 -> 2, 1.75 -> 4, 2.5 -> 4, 3.5 -> 6, 5 -> 6).
-__device__ __forceinline__ uint32_t e2m1_magnitude(float a) {
-  return static_cast<uint32_t>(a > 0.25f) + static_cast<uint32_t>(a >= 0.75f) +
-         static_cast<uint32_t>(a > 1.25f) + static_cast<uint32_t>(a >= 1.75f) +
-         static_cast<uint32_t>(a > 2.5f) + static_cast<uint32_t>(a >= 3.5f) + static_cast<uint32_t>(a > 5.0f);
-}
 
 // One warp per unit of (row, 256 consecutive elements): lane l holds
 // elements 8l..8l+7, four lanes form one 32-element block.
@@ -56,17 +46,7 @@ __global__ void __launch_bounds__(256, 4) quant_kernel(const uint16_t* __restric
       const int64_t u = u0 + j * nwarps;
       const int r = static_cast<int>(u / KT);
       const int kt = static_cast<int>(u - static_cast<int64_t>(r) * KT);
-      const int e0 = kt * 256 + lane * 8;
-      if (u < units && r < M && vec_ok && e0 + 8 <= K) {
-        const uint4 q = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(r) * ldx + e0));
-        v[j][0] = q.x & 0xFFFF; v[j][1] = q.x >> 16; v[j][2] = q.y & 0xFFFF; v[j][3] = q.y >> 16;
-        v[j][4] = q.z & 0xFFFF; v[j][5] = q.z >> 16; v[j][6] = q.w & 0xFFFF; v[j][7] = q.w >> 16;
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          v[j][i] = (u < units && r < M && e0 + i < K) ? x[static_cast<size_t>(r) * ldx + e0 + i]
-                                                       : static_cast<uint16_t>(0);
-      }
+      load8_bf16(x, u < units ? r : M, M, K, ldx, kt * 256 + lane * 8, vec_ok, v[j]);
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -75,29 +55,8 @@ __global__ void __launch_bounds__(256, 4) quant_kernel(const uint16_t* __restric
       const int r = static_cast<int>(u / KT);
       const int kt = static_cast<int>(u - static_cast<int64_t>(r) * KT);
       const int e0 = kt * 256 + lane * 8;
-
-      // Block amax on the magnitude bits (bf16 magnitudes order like
-      // integers; Inf and NaN sort above every finite value).
-      uint32_t am = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) am = max(am, static_cast<uint32_t>(v[j][i] & 0x7FFF));
-      am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
-      am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
-
-      const uint32_t ef = am >> 7;               // biased exponent field of amax
-      const bool nonfinite = ef == 0xFF;
-      // floor(log2 amax) - 2 as an E8M0 byte, clamped at 0 (zero / subnormal amax)
-      const uint32_t sbyte = nonfinite ? 0xFFu : (ef > 2 ? ef - 2 : 0u);
-      const float inv = __uint_as_float((254u - (nonfinite ? 0u : sbyte)) << 23);   // 2^(127 - sbyte)
-
-      uint32_t packed = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float a = __uint_as_float(static_cast<uint32_t>(v[j][i] & 0x7FFF) << 16) * inv;
-        uint32_t c = e2m1_magnitude(a) | ((v[j][i] >> 12) & 8u);
-        if (nonfinite) c = 0;
-        packed |= c << (4 * i);
-      }
+      uint32_t sbyte;
+      const uint32_t packed = quantize8(v[j], sbyte);
 
       const int blk = kt * 8 + (lane >> 2);
       const bool blk_real = r < M && blk < nb;
