@@ -60,10 +60,15 @@ def gemm_kernel_bytes(M, N, K):
 
 
 def launches_per_call(M, N, K):
-    """Kernels one mxfp4_gemm call launches: quantizer, GEMM, and the fix-up when a CTA boundary cuts a tile."""
+    """Kernels one mxfp4_gemm call with a bf16 input launches.  M <= 64: one
+    (quantizer, GEMM and split-tile sums in one kernel; for K > 98304 the
+    quantizer runs first).  Larger M: quantizer, GEMM, and the fix-up when a
+    CTA boundary cuts a tile."""
     import torch
-    grid = min(torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count, 256)
     kt = ceil_div(K, 256)
+    if M <= 64:
+        return 1 if kt <= 384 else 2
+    grid = min(torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count, 256)
     total = ceil_div(M, 128) * ceil_div(N, 256) * kt
     grid = min(grid, total)
     split = any(((c * total) // grid) % kt for c in range(1, grid))
@@ -81,7 +86,7 @@ def load_peaks():
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("gemm.cu", "ptx.cuh", "internal.h"):
+    for f in ("decode.cu", "gemm_common.cuh", "quant_math.cuh", "ptx.cuh", "internal.h"):
         h.update(open(os.path.join(ROOT, "mxfp4_quantized_gemm_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -232,7 +237,7 @@ def run_ours(args, world, rank, local):
             "x_host": synth.bf16_tensor(x_bits).pin_memory(),
             "out": torch.empty(M, N, dtype=torch.bfloat16, device=dev),
             "out_host": torch.empty(M, N, dtype=torch.bfloat16).pin_memory(),
-            "ws": torch.empty(ws_bytes, dtype=torch.uint8, device=dev),
+            "ws": torch.zeros(ws_bytes, dtype=torch.uint8, device=dev),
             "ws_bytes": ws_bytes,
         })
     del packed_master
@@ -259,8 +264,7 @@ def run_ours(args, world, rank, local):
     assert capi.mxfp4_get_device_error(sptr) == capi.OK
 
     # graph of G steps; the last one carries timing events at case boundaries
-    # (events between the quantizer and the GEMM would cut their programmatic
-    # dependent launch, so each case is timed as the quant -> GEMM pair)
+    # (each case is one decode kernel launch)
     K_steps, W_steps = args.steps, args.warmup
     G = max(g for g in range(1, min(K_steps, 50) + 1) if K_steps % g == 0)
     ev = [[make_event(torch, True), make_event(torch, True)] for _ in state]
@@ -354,15 +358,16 @@ def run_ours(args, world, rank, local):
             "cases_per_step": len(state),
             "l2": "inputs larger than L2: each case reads its own packed-weight copy (15 buffers, "
                   f"{sum(c['packed'].numel() for c in state) / 1e9:.2f} GB per step)",
-            "timing": f"CUDA graph of {G} steps replayed {replays}x; each case is one mxfp4_gemm call (quantizer, "
-                      "GEMM and split-tile fix-up kernels chained by programmatic dependent launch); external events "
-                      "at the case boundaries of each replay's last step",
+            "timing": f"CUDA graph of {G} steps replayed {replays}x; each case is one mxfp4_gemm call = one "
+                      "decode_kernel launch (activation quantization, GEMM and split-tile sums inside; consecutive "
+                      "calls overlap by programmatic dependent launch); external events at the case boundaries of "
+                      "each replay's last step",
             "parallelism": f"replicas x{world}",
         },
         "roofline": {
             "bound": "hbm",
-            "kernel": "decode dense linear per mxfp4_gemm call: quant_kernel -> gemm_kernel -> gemm_fixup_kernel "
-                      "(PDL-chained; the GEMM holds the largest share of the launch-list time)",
+            "kernel": "decode_kernel (one launch per mxfp4_gemm call: activation quantization, GEMM, split-tile "
+                      "sums, bias, bf16 store)",
             "bytes_per_launch": "N*K/2 + N*K/32 (packed W) + 2*M*K (bf16 A) + 2*M*N (bf16 out)",
             "achieved": round(achieved, 1),
             "peak": hbm_peak,
@@ -398,7 +403,7 @@ def run_prefill(args, torch, np, capi, synth, dev, stream, bf16_peak, peak_src):
             x = synth.bf16_tensor(synth.activations(M, K, seed=M, tensor_id=1)).to(dev)
             out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
             wsb = capi.mxfp4_gemm_workspace_bytes(M, N, K)
-            work = torch.empty(wsb, dtype=torch.uint8, device=dev)
+            work = torch.zeros(wsb, dtype=torch.uint8, device=dev)
 
             def call():
                 capi.mxfp4_gemm(x, K, None, None, 0, packed, bias, out, N, M, N, K, work, wsb, sptr)
@@ -550,7 +555,7 @@ def run_single(args):
     x = synth.bf16_tensor(synth.activations(M, K, seed=1, outlier_frac=0.01)).cuda()
     out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
     wsb = capi.mxfp4_gemm_workspace_bytes(M, N, K)
-    work = torch.empty(wsb, dtype=torch.uint8, device="cuda")
+    work = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
     for i in range(args.calls):
         capi.mxfp4_gemm(x, K, None, None, 0, pks[i % len(pks)], None, out, N, M, N, K, work, wsb)
     torch.cuda.synchronize()

@@ -134,6 +134,15 @@ MXFP4_API mxfp4_status mxfp4_quant_act(const void* x_dev, int M, int K, int ldx,
 MXFP4_API size_t mxfp4_gemm_workspace_bytes(int M, int N, int K);
 
 /*
+ * Prepares a GEMM workspace for its first use: zeroes its control words
+ * (the first 16 KiB), stream-ordered on `stream`.  Needed once per
+ * workspace, before its first mxfp4_gemm call, unless the memory was
+ * allocated zeroed; never needed again while it is used only by mxfp4_gemm.
+ * Errors: INVALID_ARG, WORKSPACE (fewer than 16 KiB), MISALIGNED, CUDA.
+ */
+MXFP4_API mxfp4_status mxfp4_gemm_workspace_init(void* workspace_dev, size_t workspace_bytes, void* stream);
+
+/*
  * W4A4 MXFP4 GEMM with fused bias — the pages' gemm_a4w4 followed by
  * `y + bias` (PR #39598 blog analysis, section 2, apply_weights):
  *   out[m][n] = bf16_RNE( sum_k deq(A)[m][k] * deq(W)[n][k] + bias[n] )
@@ -150,9 +159,19 @@ MXFP4_API size_t mxfp4_gemm_workspace_bytes(int M, int N, int K);
  *   bias_dev       bf16 [N] or NULL
  *   out_dev        bf16 [M][ldo], ldo >= N
  *   workspace_dev  >= mxfp4_gemm_workspace_bytes(M, N, K) bytes of device
- *                  scratch owned by the caller; contents need not be
- *                  initialised and are clobbered.
+ *                  scratch owned by the caller.  Its first 16 KiB hold
+ *                  control words (flags between the kernel's thread blocks
+ *                  and an epoch counter) that must be zero before the
+ *                  workspace's first use (mxfp4_gemm_workspace_init, or
+ *                  zeroed memory) and that the caller must not write
+ *                  afterwards; the rest is clobbered by every call.  One
+ *                  workspace may serve calls of any shape.
  * Calls sharing one workspace must be ordered on the GPU.
+ * For M <= 64 the whole call is one kernel launch (the bf16 input is
+ * quantized inside the GEMM kernel when K <= 98304) whose thread blocks,
+ * at most one per SM, must all be resident together; if work on other
+ * streams keeps SMs occupied for about a second, the call gives up and
+ * mxfp4_get_device_error reports MXFP4_ERR_TIMEOUT.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, WORKSPACE, CUDA.
  */
 MXFP4_API mxfp4_status mxfp4_gemm(const void* a_bf16_dev, int lda,
@@ -195,9 +214,9 @@ MXFP4_API mxfp4_status a16wfp4_bmm(const void* x_dev, const void* w_packed_dev, 
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress); make that first call before any stream capture.
  *   - All calls share the one array and it keeps the last call's contents.
- *     Nothing in it has to start at zero (the stream-K tickets are tagged per
- *     call and left reset), but calls that overlap on the GPU — on different
- *     streams, or from several host threads without ordering — race on it.
+ *     It starts zeroed (its control words need that), and calls that
+ *     overlap on the GPU — on different streams, or from several host
+ *     threads without ordering — race on it.
  */
 MXFP4_API mxfp4_status mxfp4_gemm_noalloc(const void* a_bf16_dev, int lda, const void* w_packed_dev,
                                           const void* bias_dev, void* out_dev, int ldo, int M, int N, int K,

@@ -1,4 +1,5 @@
-// W4A4 MXFP4 GEMM on the sm_103a block-scaled tensor cores.
+// W4A4 MXFP4 GEMM on the sm_103a block-scaled tensor cores, for M > 64
+// (the decode shapes, M <= 64, run in decode.cu).
 //
 //   out[m][n] = bf16_RNE( sum_k deq(A)[m][k] * deq(W)[n][k] + bias[n] )
 //
@@ -8,22 +9,19 @@
 // 128-byte-swizzled K-major image, 512-byte scale atoms already in the
 // tcgen05.cp source layout.
 //
-// One persistent kernel serves every M.  An output tile is 128 activation
-// rows (the MMA's M) by 256 weight rows (its N).  A
-// tcgen05.mma.kind::mxf4.block_scale instruction costs about the same for any
-// N, so the 256-row weight side moves the most weight bytes per tensor-pipe
-// cycle.  That serves both the weight-streaming decode shapes (M <= 64: only
-// 16/32/64 activation rows are loaded) and the compute-bound prefill shapes.
-// The (tile, 256-wide k-step) iteration space is split evenly over one CTA
-// per SM (stream-K), so every SM streams the same number of weight bytes.  A
-// tile split between CTAs is finished by the last CTA to finish its part,
-// which sums the fp32 partials in CTA order (deterministic, no spin-waits).
+// An output tile is 128 activation rows (the MMA's M) by 256 weight rows
+// (its N): a tcgen05.mma.kind::mxf4.block_scale instruction costs about the
+// same for any N, so the 256-row weight side does the most work per issued
+// instruction.  The (tile, 256-wide k-step) iteration space is split evenly
+// over one CTA per SM (stream-K).  Tiles cut by a CTA boundary are published
+// as fp32 parts and summed, in CTA order (deterministic), by a fix-up kernel
+// launched behind the GEMM.
 //
 // Roles (320 threads): warp 0 streams stages with bulk copies; warp 1 issues
 // tcgen05.cp (scales -> TMEM) and the MMAs into one 128 x 256 fp32 TMEM
 // accumulator; warps 2..9 drain it (each 32 rows x 128 columns) with
 // tcgen05.ld, release it at once, then add the bias and store bf16 (or
-// publish the partial).  The kernel is launched as a programmatic dependent:
+// publish the part).  The kernel is launched as a programmatic dependent:
 // it sets up and requests its first weight stages while the activation
 // quantizer before it finishes, and lets the next kernel launch early.
 #include <cuda_bf16.h>
@@ -31,6 +29,7 @@
 
 #include <cstdint>
 
+#include "gemm_common.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -38,116 +37,24 @@ namespace mx {
 
 static __device__ uint32_t g_gemm_error;
 
-constexpr int kTileN = 256;          // weight rows per output tile (the MMA's N)
-constexpr int kThreads = 320;        // producer warp, MMA warp, 8 epilogue warps
-constexpr int kEpiThreads = 256;
-constexpr int kMaxSmem = 232448;     // 227 KiB of dynamic shared memory per CTA
-
 struct GemmArgs {
   const uint8_t* a_codes;
   const uint8_t* a_scales;
   const uint8_t* w_codes;
   const uint8_t* w_scales;
-  const __nv_bfloat16* bias;
-  __nv_bfloat16* out;
-  int ldo, M, N, KT;
+  OutView o;
+  int M, KT;
   int w_tiles;                     // Np / 128: 128-row tiles of the packed weights
   int n_tiles;                     // ceil(N / 256)
   int total;                       // output tiles x KT
   int grid;
-  int rows_a;                      // activation rows per tile that are loaded (16/32/64/128)
+  int rows_a;                      // activation rows per tile that are loaded (128)
   float* partials;                 // 2 slots per CTA, rows_a x 256 floats each
 };
 
-template <int kRowsA>
-struct Cfg {
-  static constexpr int kW = 2 * kTileBytes;       // 256 weight rows of codes
-  // Only the first kRowsA activation rows are loaded and reserved per stage.
-  // The M = 128 MMA reads 16 KiB from the activation offset; for kRowsA <
-  // 128 the rows past kRowsA come from whatever follows (the next stage, or a
-  // tail pad after the last one, so every read stays inside the allocation)
-  // and feed only accumulator rows that are never read.
-  static constexpr int kALoad = kRowsA * 128;
-  static constexpr int kA = kALoad;
-  static constexpr int kTailPad = kTileBytes - kALoad;
-  static constexpr int kSA = 1024;                // 2 activation scale atoms
-  static constexpr int kSW = 2048;                // 2 x 2 weight scale atoms
-  static constexpr int kStageBytes = kW + kA + kSA + kSW;
-  static constexpr int kStagesFit = (kMaxSmem - 1024 - 512 - kTailPad) / kStageBytes;
-  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
-  static constexpr int kRing = kStages * kStageBytes + kTailPad;
-  static constexpr int kSmem = kRing + 1024 + 512;
-  static constexpr uint32_t kTmemCols = 512;      // accumulator 256 + scales 24
-  static constexpr uint32_t kSfa = 256, kSfb = 264;
-};
-
-__device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
-}
-__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
-  return __uint_as_float(static_cast<uint32_t>(b) << 16);
-}
-
-// Balanced stream-K split: CTA c owns iterations [sk_begin(c), sk_begin(c+1)).
-__device__ __forceinline__ int sk_begin(int c, int total, int grid) {
-  return static_cast<int>((static_cast<long long>(c) * total) / grid);
-}
-// CTA whose range holds iteration `it`.
-__device__ __forceinline__ int sk_owner(int it, int total, int grid) {
-  int c = static_cast<int>((static_cast<long long>(it) * grid) / total);
-  while (c + 1 < grid && sk_begin(c + 1, total, grid) <= it) ++c;
-  while (c > 0 && sk_begin(c, total, grid) > it) --c;
-  return c;
-}
-
-// 32 consecutive outputs of row m starting at column n: + bias, bf16, store.
-__device__ __forceinline__ void store_chunk(const GemmArgs& g, int m, int n, const float (&v)[32]) {
-  __nv_bfloat16* dst = g.out + static_cast<size_t>(m) * g.ldo + n;
-  const uint16_t* bias = reinterpret_cast<const uint16_t*>(g.bias);
-  if (n + 32 <= g.N && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-#pragma unroll
-    for (int c = 0; c < 32; c += 8) {
-      float b[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) b[i] = bias != nullptr ? bf16_bits_to_float(__ldg(bias + n + c + i)) : 0.f;
-      uint4 w;
-      w.x = pack_bf16x2(v[c] + b[0], v[c + 1] + b[1]);
-      w.y = pack_bf16x2(v[c + 2] + b[2], v[c + 3] + b[3]);
-      w.z = pack_bf16x2(v[c + 4] + b[4], v[c + 5] + b[5]);
-      w.w = pack_bf16x2(v[c + 6] + b[6], v[c + 7] + b[7]);
-      *reinterpret_cast<uint4*>(dst + c) = w;
-    }
-  } else {
-    for (int c = 0; c < 32; ++c)
-      if (n + c < g.N)
-        dst[c] = __float2bfloat16_rn(v[c] + (bias != nullptr ? bf16_bits_to_float(__ldg(bias + n + c)) : 0.f));
-  }
-}
-
-// 4 consecutive outputs of row m starting at column n: + bias, bf16, store.
-__device__ __forceinline__ void store_quad(const GemmArgs& g, int m, int n, float4 v) {
-  if (n >= g.N) return;
-  __nv_bfloat16* dst = g.out + static_cast<size_t>(m) * g.ldo + n;
-  const uint16_t* bias = reinterpret_cast<const uint16_t*>(g.bias);
-  float x[4] = {v.x, v.y, v.z, v.w};
-  if (bias != nullptr) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      if (n + i < g.N) x[i] += bf16_bits_to_float(__ldg(bias + n + i));
-  }
-  if (n + 4 <= g.N && (reinterpret_cast<uintptr_t>(dst) & 7) == 0) {
-    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
-  } else {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      if (n + i < g.N) dst[i] = __float2bfloat16_rn(x[i]);
-  }
-}
-
 // At most 96 registers per thread (the bound asks for two CTAs' worth; the
-// shared-memory ring still allows one CTA per SM): the quantizer and fix-up
-// blocks of neighbouring calls then fit on the SM beside it, so the next
-// call's GEMM can take the SM and prefetch weights while they run.
+// shared-memory ring still allows one CTA per SM): the fix-up blocks of the
+// previous call then fit on the SM beside it.
 template <int kRowsA>
 __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const GemmArgs g) {
   using C = Cfg<kRowsA>;
@@ -242,7 +149,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const GemmArgs g) {
   } else if (warp == 1) {
     if (lane == 0) {
       // ---- MMA issuer: one accumulator, one segment (part of a tile) at a time
-      const uint32_t sfa = tmem + C::kSfa, sfb = tmem + C::kSfb;
       int i = 0, seg = 0, kt = it0 % KT;
       for (int it = it0; it < it1 && !abort; ++seg) {
         const int len = (KT - kt) < (it1 - it) ? (KT - kt) : (it1 - it);
@@ -253,20 +159,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const GemmArgs g) {
           const uint32_t ph = (i / C::kStages) & 1;
           if (!mbar_wait(&full[s], ph, abort)) break;
           tc_fence_after();
-          const uint32_t base = smem_u32(smem + s * C::kStageBytes);
-          const uint32_t w_s = base, a_s = base + C::kW, sa_s = a_s + C::kA, sw_s = sa_s + C::kSA;
-          tmem_cp_scales(sfa + 0, sdesc_scales(sa_s));
-          tmem_cp_scales(sfa + 4, sdesc_scales(sa_s + 512));
-#pragma unroll
-          for (int a = 0; a < 2; ++a)
-#pragma unroll
-            for (int q = 0; q < 2; ++q) tmem_cp_scales(sfb + a * 8 + q * 4, sdesc_scales(sw_s + q * 1024 + a * 512));
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t id = idesc_mxf4(128, kTileN, (q & 1) * 2, (q & 1) * 2);
-            mma_mxf4(tmem, sdesc_sw128(a_s + 32 * q), sdesc_sw128(w_s + 32 * q), id, sfa + 4 * (q >> 1),
-                     sfb + 8 * (q >> 1), (j != 0 || q != 0) ? 1u : 0u);
-          }
+          issue_stage_mma<kRowsA>(tmem, smem_u32(smem + s * C::kStageBytes), j != 0 ? 1u : 0u);
           mma_commit(&empty[s]);
         }
         mma_commit(acc_full);
@@ -321,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const GemmArgs g) {
             float chunk[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) chunk[c] = v[c0 + c];
-            store_chunk(g, m, n0 + pass * 64 + c0, chunk);
+            store_chunk(g.o, m, n0 + pass * 64 + c0, chunk);
           }
         } else {
           float4* P = reinterpret_cast<float4*>(g.partials + (static_cast<size_t>(slot) * kRowsA + rl) * kTileN +
@@ -398,23 +291,13 @@ __global__ void __launch_bounds__(256, 4) gemm_fixup_kernel(const __grid_constan
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     const int gi = g0 + 256 * j;
-    if (gi < groups) store_quad(g, mt * 128 + gi / (kTileN / 4), nt * kTileN + 4 * (gi % (kTileN / 4)), acc[j]);
+    if (gi < groups) store_quad(g.o, mt * 128 + gi / (kTileN / 4), nt * kTileN + 4 * (gi % (kTileN / 4)), acc[j]);
   }
 }
 
 // ===================================================================== host
-static bool g_attr_set[64][4];
+static bool g_attr_set[64];
 
-template <typename Kern>
-static cudaError_t ensure_smem(Kern k, int smem, int dev, int which) {
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!g_attr_set[dev][which]) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    g_attr_set[dev][which] = true;
-  }
-  return cudaSuccess;
-}
 
 size_t gemm_streamk_workspace_bytes(int M, int N, int K, int grid) {
   (void)N;
@@ -422,29 +305,6 @@ size_t gemm_streamk_workspace_bytes(int M, int N, int K, int grid) {
   return static_cast<size_t>(2) * grid * gemm_rows_a(M) * kTileN * sizeof(float);
 }
 
-// Launch as a programmatic dependent of the previous kernel in the stream.
-template <typename Kern, typename Args>
-static cudaError_t launch_pdl(Kern k, int grid, int threads, int smem, cudaStream_t s, const Args& a) {
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
-  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, a);
-}
-
-template <int kRowsA>
-static cudaError_t launch_rows(const GemmArgs& a, const DeviceInfo& dev, cudaStream_t s, int which) {
-  using C = Cfg<kRowsA>;
-  cudaError_t e = ensure_smem(gemm_kernel<kRowsA>, C::kSmem, dev.device, which);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(gemm_kernel<kRowsA>, a.grid, kThreads, C::kSmem, s, a);
-}
 
 int gemm_grid(const DeviceInfo& dev) { return dev.sm_count < kMaxStreamKCtas ? dev.sm_count : kMaxStreamKCtas; }
 
@@ -456,11 +316,11 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
   a.a_scales = p.a_scales;
   a.w_codes = p.w_packed;
   a.w_scales = p.w_packed + Np * Kp / 2;
-  a.bias = static_cast<const __nv_bfloat16*>(p.bias);
-  a.out = static_cast<__nv_bfloat16*>(p.out);
-  a.ldo = p.ldo;
+  a.o.bias = static_cast<const __nv_bfloat16*>(p.bias);
+  a.o.out = static_cast<__nv_bfloat16*>(p.out);
+  a.o.ldo = p.ldo;
+  a.o.N = p.N;
   a.M = p.M;
-  a.N = p.N;
   a.KT = static_cast<int>(Kp / kKTile);
   a.w_tiles = static_cast<int>(Np / 128);
   a.n_tiles = static_cast<int>(ceil_div(p.N, kTileN));
@@ -471,13 +331,15 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
   a.grid = grid;
   a.rows_a = gemm_rows_a(p.M);
   a.partials = static_cast<float*>(p.workspace);
-  cudaError_t e;
-  switch (a.rows_a) {
-    case 16: e = launch_rows<16>(a, dev, s, 0); break;
-    case 32: e = launch_rows<32>(a, dev, s, 1); break;
-    case 64: e = launch_rows<64>(a, dev, s, 2); break;
-    default: e = launch_rows<128>(a, dev, s, 3); break;
+  if (a.rows_a != 128) return cudaErrorInvalidValue;   // M <= 64 runs in decode.cu
+  using C = Cfg<128>;
+  if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+  if (!g_attr_set[dev.device]) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    g_attr_set[dev.device] = true;
   }
+  cudaError_t e = launch_pdl(gemm_kernel<128>, a.grid, kThreads, C::kSmem, s, a);
   if (e != cudaSuccess) return e;
   // Tiles that a CTA boundary cuts are summed by the fix-up kernel.
   FixupArgs f;

@@ -1,0 +1,155 @@
+// Pieces shared by the two W4A4 GEMM kernels (gemm.cu: M > 64, decode.cu:
+// M <= 64): the shared-memory stage geometry, the stream-K split of the
+// (output tile, k-step) iteration space, and the bias + bf16 output stores.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mx {
+
+constexpr int kTileN = 256;          // weight rows per output tile (the MMA's N)
+constexpr int kThreads = 320;        // producer warp, MMA warp, 8 epilogue warps
+constexpr int kEpiThreads = 256;
+constexpr int kMaxSmem = 232448;     // 227 KiB of dynamic shared memory per CTA
+
+// One pipeline stage = one 256-wide k-step of one output tile: 256 weight
+// rows of codes (two 16 KiB tiles), kRowsA activation rows of codes, two
+// activation scale atoms and 2 x 2 weight scale atoms.
+template <int kRowsA>
+struct Cfg {
+  static constexpr int kW = 2 * kTileBytes;       // 256 weight rows of codes
+  // Only the first kRowsA activation rows are loaded and reserved per stage.
+  // The M = 128 MMA reads 16 KiB from the activation offset; for kRowsA <
+  // 128 the rows past kRowsA come from whatever follows (the next stage, or a
+  // tail pad after the last one, so every read stays inside the allocation)
+  // and feed only accumulator rows that are never read.
+  static constexpr int kALoad = kRowsA * 128;
+  static constexpr int kA = kALoad;
+  static constexpr int kTailPad = kTileBytes - kALoad;
+  static constexpr int kSA = 1024;                // 2 activation scale atoms
+  static constexpr int kSW = 2048;                // 2 x 2 weight scale atoms
+  static constexpr int kStageBytes = kW + kA + kSA + kSW;
+  static constexpr int kStagesFit = (kMaxSmem - 1024 - 512 - kTailPad) / kStageBytes;
+  static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
+  static constexpr int kRing = kStages * kStageBytes + kTailPad;
+  static constexpr int kSmem = kRing + 1024 + 512;
+  static constexpr uint32_t kTmemCols = 512;      // accumulator 256 + scales 24
+  static constexpr uint32_t kSfa = 256, kSfb = 264;
+};
+
+__device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
+}
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+// Balanced stream-K split: CTA c owns iterations [sk_begin(c), sk_begin(c+1)).
+__device__ __forceinline__ int sk_begin(int c, int total, int grid) {
+  return static_cast<int>((static_cast<long long>(c) * total) / grid);
+}
+// CTA whose range holds iteration `it`.
+__device__ __forceinline__ int sk_owner(int it, int total, int grid) {
+  int c = static_cast<int>((static_cast<long long>(it) * grid) / total);
+  while (c + 1 < grid && sk_begin(c + 1, total, grid) <= it) ++c;
+  while (c > 0 && sk_begin(c, total, grid) > it) --c;
+  return c;
+}
+
+// Where the bf16 results go.
+struct OutView {
+  __nv_bfloat16* out;
+  const __nv_bfloat16* bias;   // [N] or null
+  int ldo, N;
+};
+
+// 32 consecutive outputs of row m starting at column n: + bias, bf16, store.
+__device__ __forceinline__ void store_chunk(const OutView& o, int m, int n, const float (&v)[32]) {
+  __nv_bfloat16* dst = o.out + static_cast<size_t>(m) * o.ldo + n;
+  const uint16_t* bias = reinterpret_cast<const uint16_t*>(o.bias);
+  if (n + 32 <= o.N && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+#pragma unroll
+    for (int c = 0; c < 32; c += 8) {
+      float b[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) b[i] = bias != nullptr ? bf16_bits_to_float(__ldg(bias + n + c + i)) : 0.f;
+      uint4 w;
+      w.x = pack_bf16x2(v[c] + b[0], v[c + 1] + b[1]);
+      w.y = pack_bf16x2(v[c + 2] + b[2], v[c + 3] + b[3]);
+      w.z = pack_bf16x2(v[c + 4] + b[4], v[c + 5] + b[5]);
+      w.w = pack_bf16x2(v[c + 6] + b[6], v[c + 7] + b[7]);
+      *reinterpret_cast<uint4*>(dst + c) = w;
+    }
+  } else {
+    for (int c = 0; c < 32; ++c)
+      if (n + c < o.N)
+        dst[c] = __float2bfloat16_rn(v[c] + (bias != nullptr ? bf16_bits_to_float(__ldg(bias + n + c)) : 0.f));
+  }
+}
+
+// 4 consecutive outputs of row m starting at column n: + bias, bf16, store.
+__device__ __forceinline__ void store_quad(const OutView& o, int m, int n, float4 v) {
+  if (n >= o.N) return;
+  __nv_bfloat16* dst = o.out + static_cast<size_t>(m) * o.ldo + n;
+  const uint16_t* bias = reinterpret_cast<const uint16_t*>(o.bias);
+  float x[4] = {v.x, v.y, v.z, v.w};
+  if (bias != nullptr) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (n + i < o.N) x[i] += bf16_bits_to_float(__ldg(bias + n + i));
+  }
+  if (n + 4 <= o.N && (reinterpret_cast<uintptr_t>(dst) & 7) == 0) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (n + i < o.N) dst[i] = __float2bfloat16_rn(x[i]);
+  }
+}
+
+// Issues the tcgen05.cp scale copies and the four K = 64 block-scaled MMAs
+// of one stage: accumulator [128 act rows x 256 weight rows] at `tmem`,
+// activation scales at TMEM column sfa (2 atoms), weight scales at sfb
+// (2 atoms x 2 row halves).  `accumulate` = 0 starts a new tile.
+template <int kRowsA>
+__device__ __forceinline__ void issue_stage_mma(uint32_t tmem, uint32_t stage_base, uint32_t accumulate) {
+  using C = Cfg<kRowsA>;
+  const uint32_t sfa = tmem + C::kSfa, sfb = tmem + C::kSfb;
+  const uint32_t w_s = stage_base, a_s = stage_base + C::kW, sa_s = a_s + C::kA, sw_s = sa_s + C::kSA;
+  tmem_cp_scales(sfa + 0, sdesc_scales(sa_s));
+  tmem_cp_scales(sfa + 4, sdesc_scales(sa_s + 512));
+#pragma unroll
+  for (int a = 0; a < 2; ++a)
+#pragma unroll
+    for (int q = 0; q < 2; ++q) tmem_cp_scales(sfb + a * 8 + q * 4, sdesc_scales(sw_s + q * 1024 + a * 512));
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t id = idesc_mxf4(128, kTileN, (q & 1) * 2, (q & 1) * 2);
+    mma_mxf4(tmem, sdesc_sw128(a_s + 32 * q), sdesc_sw128(w_s + 32 * q), id, sfa + 4 * (q >> 1), sfb + 8 * (q >> 1),
+             (accumulate != 0 || q != 0) ? 1u : 0u);
+  }
+}
+
+// Launch as a programmatic dependent of the previous kernel in the stream.
+template <typename Kern, typename Args>
+static cudaError_t launch_pdl(Kern k, int grid, int threads, int smem, cudaStream_t s, const Args& a) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, a);
+}
+
+}  // namespace mx

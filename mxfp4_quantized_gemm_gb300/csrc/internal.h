@@ -24,8 +24,22 @@ constexpr uint32_t kErrTimeout = 1u;
 
 // Largest stream-K grid the decode GEMM uses; sizes its partial-sum slots.
 constexpr int kMaxStreamKCtas = 256;
-// Largest activation row count served by the swap-AB decode kernel.
+// Largest activation row count served by the one-launch decode kernel.
 constexpr int kDecodeMaxM = 64;
+
+// Control words at the start of every GEMM workspace (must be zero before
+// the workspace's first use): word 0 epoch, word 1 CTAs done, words
+// kCtrlPartFlags.. one flag per stream-K partial slot (2 per CTA), words
+// kCtrlUnitFlags.. one flag per (activation k-step, 8-row unit).
+constexpr size_t kDecodeCtrlBytes = 16384;
+constexpr int kCtrlEpoch = 0;
+constexpr int kCtrlDone = 1;
+constexpr int kCtrlPartFlags = 256;
+constexpr int kCtrlUnitFlags = 1024;
+// Largest K / 256 for which the decode kernel quantizes the activations
+// itself (8 unit flags per k-step fit the control region).
+constexpr int kMaxFusedKT = static_cast<int>((kDecodeCtrlBytes / 4 - kCtrlUnitFlags) / 8);
+static_assert(kCtrlPartFlags + 2 * kMaxStreamKCtas <= kCtrlUnitFlags, "part flags overlap unit flags");
 // Activation rows of a 128-row tile the GEMM loads: 16, 32 or 64 when
 // M <= kDecodeMaxM (only those rows of the tiled activations are read), else 128.
 inline int gemm_rows_a(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128)); }
@@ -54,7 +68,7 @@ struct GemmProblem {
   const void* bias;         // bf16 [N] or null
   void* out;                // bf16 [M][ldo]
   int ldo, M, N, K;
-  void* workspace;          // stream-K partials + tickets
+  void* workspace;          // stream-K partial sums
   size_t workspace_bytes;
 };
 // Stream-K CTAs of the GEMM on this device, and the partial-sum + ticket
@@ -63,6 +77,22 @@ int gemm_grid(const DeviceInfo& dev);
 size_t gemm_streamk_workspace_bytes(int M, int N, int K, int grid);
 cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_t s);
 uint32_t gemm_read_clear_error();
+
+// decode.cu: M <= kDecodeMaxM in one launch.
+struct DecodeProblem {
+  const void* x;            // bf16 activations [M][ldx]; null when a_codes/a_scales hold them already
+  int ldx;
+  const uint8_t* a_codes;   // TILED activation codes (written by the kernel when x != null)
+  const uint8_t* a_scales;  // TILED activation scales
+  const uint8_t* w_packed;
+  const void* bias;
+  void* out;
+  int ldo, M, N, K;
+  uint32_t* ctrl;           // kDecodeCtrlBytes of control words
+  float* partials;          // gemm_streamk_workspace_bytes(M, N, K, grid)
+};
+cudaError_t launch_decode(const DecodeProblem& p, const DeviceInfo& dev, cudaStream_t s);
+uint32_t decode_read_clear_error();
 
 // bmm.cu
 cudaError_t launch_bmm(const void* x, const uint8_t* w_packed, void* out, int B, int M, int N, int K,

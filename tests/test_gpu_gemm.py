@@ -13,7 +13,8 @@ import torch
 
 from oracle import mxfp4_ref as ref
 from mxfp4_quantized_gemm_gb300 import synth
-from helpers import (check_close, dev_bf16, dev_u8, empty_u8, host_bits, oracle_gemm_rows, pack_weights,
+from helpers import (check_close, dev_bf16, dev_u8, empty_u8, gemm_workspace, host_bits, oracle_gemm_rows,
+                     pack_weights,
                      sample_rows, tiled_from_oracle)
 
 pytestmark = pytest.mark.gpu
@@ -39,7 +40,7 @@ def run_gemm(capi, x_bits, packed, bias_bits, M, N, K, ldo=None, mode="bf16", pr
     ldo = ldo or N
     out = torch.zeros(M, ldo, dtype=torch.bfloat16, device="cuda")
     ws_bytes = capi.mxfp4_gemm_workspace_bytes(M, N, K)
-    ws = empty_u8(ws_bytes)
+    ws = gemm_workspace(capi, ws_bytes)
     bias = dev_bf16(bias_bits) if bias_bits is not None else None
     if mode == "bf16":
         capi.mxfp4_gemm(dev_bf16(x_bits), K, None, None, 0, packed, bias, out, ldo, M, N, K, ws, ws_bytes)
@@ -175,3 +176,58 @@ def test_tiny_shape_sweep(capi):
         except AssertionError as e:
             bad.append(str(e)[:200])
     assert not bad, f"{len(bad)} of {len(TINY)} shapes failed: {bad[:4]}"
+
+
+@pytest.mark.parametrize("M,N,K", [(64, 256, 32768), (5, 300, 65536), (2, 256, 98560)])
+def test_tiles_shared_by_many_ctas(capi, M, N, K):
+    """One or two output tiles over a long K: every tile's k-steps are split
+    over dozens of CTAs (more than a warp's worth of parts to wait for and
+    sum); K = 98560 also passes the longest K whose activations the decode
+    kernel quantizes itself, so the quantizer kernel runs first."""
+    full_check(capi, M, N, K, seed=21, with_bias=True)
+
+
+def test_one_workspace_for_every_shape_and_graph_replays(capi):
+    """Calls of different shapes and input forms share one workspace (its
+    control words carry over from call to call), eagerly and replayed from a
+    CUDA graph, and give the bits of the same calls on fresh workspaces."""
+    shapes = [(1, 14336, 5120), (64, 5120, 14336), (200, 1024, 5120), (16, 1000, 5152), (33, 128, 256),
+              (2, 256, 98560)]
+    probs, want = [], []
+    for i, (M, N, K) in enumerate(shapes):
+        x, wc, ws, b = make_problem(M, N, K, seed=40 + i, with_bias=(i % 2 == 1))
+        packed = pack_weights(capi, wc, ws, K)
+        probs.append((M, N, K, dev_bf16(x), packed, dev_bf16(b) if b is not None else None))
+        want.append(run_gemm(capi, x, packed, b, M, N, K))
+    wsb = max(capi.mxfp4_gemm_workspace_bytes(M, N, K) for M, N, K in shapes)
+    work = gemm_workspace(capi, wsb)
+    outs = [torch.empty(M, N, dtype=torch.bfloat16, device="cuda") for M, N, K, *_ in probs]
+
+    def calls(stream=None):
+        for (M, N, K, x, packed, bias), out in zip(probs, outs):
+            capi.mxfp4_gemm(x, K, None, None, 0, packed, bias, out, N, M, N, K, work, wsb, stream)
+
+    for _ in range(3):
+        for o in outs:
+            o.fill_(float("nan"))
+        calls()
+        torch.cuda.synchronize()
+        assert capi.mxfp4_get_device_error() == capi.OK
+        for o, w in zip(outs, want):
+            assert np.array_equal(host_bits(o), w)
+
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        calls(s.cuda_stream)          # warm-up on the capture stream
+        s.synchronize()
+        with torch.cuda.graph(graph, stream=s):
+            calls(s.cuda_stream)
+    for _ in range(5):
+        for o in outs:
+            o.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert capi.mxfp4_get_device_error() == capi.OK
+        for o, w in zip(outs, want):
+            assert np.array_equal(host_bits(o), w)

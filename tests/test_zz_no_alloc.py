@@ -15,7 +15,7 @@ import pytest
 import torch
 
 from mxfp4_quantized_gemm_gb300 import synth
-from helpers import dev_bf16, empty_u8, host_bits, pack_weights, ulp_bf16
+from helpers import dev_bf16, empty_u8, gemm_workspace, host_bits, pack_weights, ulp_bf16
 from oracle import mxfp4_ref as ref
 
 pytestmark = pytest.mark.gpu
@@ -30,7 +30,7 @@ def capi():
 def with_workspace(capi, x, packed, bias, M, N, K):
     out = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
     wsb = capi.mxfp4_gemm_workspace_bytes(M, N, K)
-    capi.mxfp4_gemm(x, K, None, None, 0, packed, bias, out, N, M, N, K, empty_u8(wsb), wsb)
+    capi.mxfp4_gemm(x, K, None, None, 0, packed, bias, out, N, M, N, K, gemm_workspace(capi, wsb), wsb)
     torch.cuda.synchronize()
     return host_bits(out)
 
