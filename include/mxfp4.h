@@ -167,8 +167,8 @@ MXFP4_API mxfp4_status mxfp4_gemm_workspace_init(void* workspace_dev, size_t wor
  *                  afterwards; the rest is clobbered by every call.  One
  *                  workspace may serve calls of any shape.
  * Calls sharing one workspace must be ordered on the GPU.
- * For M <= 64 the whole call is one kernel launch (the bf16 input is
- * quantized inside the GEMM kernel when K <= 98304) whose thread blocks,
+ * For M <= 64 the whole call is one kernel launch (a bf16 input is
+ * quantized inside the GEMM kernel) whose thread blocks,
  * at most one per SM, must all be resident together; if work on other
  * streams keeps SMs occupied for about a second, the call gives up and
  * mxfp4_get_device_error reports MXFP4_ERR_TIMEOUT.

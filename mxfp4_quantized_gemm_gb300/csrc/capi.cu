@@ -192,15 +192,8 @@ mxfp4_status mxfp4_gemm(const void* a_bf16, int lda, const uint8_t* a_codes, con
     d.a_codes = ws + wl.codes_off;
     d.a_scales = ws + wl.scales_off;
     if (from_bf16) {
-      if (padded_k(K) / kKTile <= kMaxFusedKT) {
-        d.x = a_bf16;   // quantized inside the GEMM kernel
-        d.ldx = lda;
-      } else {
-        // too many k-steps for the control region's unit flags: quantize first
-        cudaError_t e = launch_quant(a_bf16, M, K, lda, ws + wl.codes_off, ws + wl.scales_off, true, gemm_rows_a(M),
-                                     dev, s);
-        if (e != cudaSuccess) return MXFP4_ERR_CUDA;
-      }
+      d.x = a_bf16;   // quantized inside the GEMM kernel
+      d.ldx = lda;
     } else if (a_layout == MXFP4_LAYOUT_ROWMAJOR) {
       // the pages' pre-quantized (x_fp4, x_scales) input: re-lay out, pad scales with 0x7F
       cudaError_t e = launch_pack(a_codes, a_scales, 1, M, K, ws + wl.codes_off, dev, s);

@@ -10,26 +10,32 @@
 //
 // At M <= 64 the weights are almost all of the bytes (N*K/2 codes against
 // 2*M*K activation bytes), and a call lasts only a few microseconds, so the
-// kernel is organised to have every SM's copy engine pulling weights from
-// the moment it is scheduled until it exits:
-//  * stream-K as in the large-M GEMM: output tiles of 128 activation rows
-//    (of which only the first 16/32/64 are loaded) by 256 weight rows, the
-//    (tile, 256-wide k-step) iterations split evenly over one CTA per SM;
-//  * the activation quantization runs inside the kernel: the epilogue warps
-//    of CTA c quantize units (k-step, 8 rows) c, c + grid, ... straight into
-//    the TILED workspace image and publish a flag per unit; the producer warp
-//    requests its first weight stages before anything else and waits for the
-//    flags of the k-steps it needs only before their activation copies;
+// kernel is organised around one dependent chain per call (activations ready
+// -> MMAs -> split-tile sums -> outputs) with as much of the weight stream as
+// possible taken off it:
+//  * output tiles of 128 activation rows (of which only the first 16/32/64
+//    are loaded) by 256 weight rows; with fewer tiles than SMs every tile is
+//    split into the same number of k-ranges, one CTA each (an even stream-K
+//    split of the (tile, 256-wide k-step) iterations whose parts line up with
+//    tile boundaries), which leaves the remaining SMs free for the next
+//    launch to start on;
+//  * the kernel is a programmatic dependent launch and lets its own
+//    dependent launch at once, so a CTA requests its first weight stages as
+//    soon as it has an SM, usually while the previous call is still running
+//    (the packed weights are never written by the kernel this one follows);
+//  * the activations are quantized inside the kernel, by one of two schemes
+//    (DecodeMode): every CTA quantizes a share of the activation units and
+//    publishes a flag per unit, or each CTA quantizes its own k-steps;
 //  * tiles cut by CTA boundaries are summed inside the kernel: every part is
 //    published as fp32 with a flag, then each contributing CTA sums a 1/n
 //    share of the tile's outputs over all parts in CTA order (deterministic:
 //    the same order for every call) and stores them with the bias.
 //
-// The flags live in the first kDecodeCtrlBytes of the workspace together
-// with an epoch word: a call publishes value epoch+1 and waits for exactly
-// that value, and the last CTA to finish advances the epoch, so stale flags
-// of earlier calls are never mistaken for this call's.  The region must be
-// zero before the workspace's first use.
+// The part flags live in the first kDecodeCtrlBytes of the workspace with an
+// epoch word: a call publishes value epoch+1 and waits for exactly that
+// value, and the last CTA to finish advances the epoch, so stale flags of
+// earlier calls are never mistaken for this call's.  The region must be zero
+// before the workspace's first use.
 //
 // Every CTA must be resident at the same time (a CTA waits for flags that
 // other CTAs set).  The grid is at most one CTA per SM and a CTA's shared
@@ -52,10 +58,11 @@ namespace mx {
 static __device__ uint32_t g_decode_error;
 
 struct DecodeArgs {
-  const uint16_t* x;       // bf16 activations [M][ldx], or null when a_codes/a_scales already hold them quantized
+  const uint16_t* x;       // bf16 activations [M][ldx] (modes kQuantGlobal, kQuantLocal)
   int ldx;
   int vec_ok;              // x and ldx allow 16-byte row loads
-  uint8_t* a_codes;        // TILED activation codes (written by this kernel when x != null)
+  int mode;                // kPrequantized, kQuantGlobal or kQuantLocal
+  uint8_t* a_codes;        // TILED activation codes (read; written first in mode kQuantGlobal)
   uint8_t* a_scales;       // TILED activation scales
   const uint8_t* w_codes;
   const uint8_t* w_scales;
@@ -66,8 +73,19 @@ struct DecodeArgs {
   int total;               // n_tiles x KT iterations
   int grid;
   float* partials;         // 2 slots per CTA, kRowsA x 256 floats each
-  uint32_t* ctrl;          // epoch, done counter, part flags, unit flags
+  uint32_t* ctrl;          // epoch, done counter, part flags
 };
+
+// Where the activation codes of a stage come from.
+//  kPrequantized: the caller's TILED codes/scales, copied in by the producer.
+//  kQuantGlobal:  every CTA first quantizes a share of the (k-step, 8-row)
+//                 units into the TILED workspace image and publishes a flag
+//                 per unit; producers wait for the flags of their k-steps and
+//                 copy the codes in.  x is read once in all.
+//  kQuantLocal:   each CTA quantizes the k-steps of its own range straight
+//                 into its stages (warps 2, 3, 6, 7); no flags, but each CTA
+//                 reads x for its k-steps (M x 512 bytes per stage).
+enum DecodeMode : int { kPrequantized = 0, kQuantGlobal = 1, kQuantLocal = 2 };
 
 // Partial-sum slot of CTA c's part of tile t: slot 0 when t is where c's
 // range begins, slot 1 when t is where it ends.
@@ -75,10 +93,32 @@ __device__ __forceinline__ int part_slot(int c, int t, int KT, int total, int gr
   return 2 * c + (sk_begin(c, total, grid) / KT == t ? 0 : 1);
 }
 
+constexpr int kQuantThreads = 128;     // warps 2, 3, 6, 7
+constexpr int kDrainThreads = 128;     // warps 4, 5, 8, 9: accumulator rows 0..63
+// Named barriers (0 is __syncthreads).
+constexpr uint32_t kBarQuant = 1, kBarDrain = 2, kBarAll = 3;
+
+// Loads this lane's 8 bf16 values of row r, elements [e0, e0 + 8), as a
+// uint4 (zeros past K or for r >= M).
+__device__ __forceinline__ uint4 load8_packed(const uint16_t* __restrict__ x, int r, int M, int K, int ldx, int e0,
+                                              bool vec_ok) {
+  if (r >= M) return make_uint4(0, 0, 0, 0);
+  const uint16_t* src = x + static_cast<size_t>(r) * ldx + e0;
+  if (vec_ok && e0 + 8 <= K) return __ldg(reinterpret_cast<const uint4*>(src));
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t lo = e0 + 2 * i < K ? src[2 * i] : 0u;
+    const uint32_t hi = e0 + 2 * i + 1 < K ? src[2 * i + 1] : 0u;
+    w[i] = lo | (hi << 16);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 template <int kRowsA>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs g) {
   using C = Cfg<kRowsA>;
-  constexpr int kGroups = kRowsA / 8;   // 8-row quantization units per k-step
+  constexpr int kRowsPerWarp = kRowsA / 4;   // rows a quantizing warp covers per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kRing);
@@ -92,18 +132,28 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   const int cta = blockIdx.x;
   const int it0 = sk_begin(cta, g.total, g.grid);
   const int it1 = sk_begin(cta + 1, g.total, g.grid);
+  const int n_iter = it1 - it0;
+  const bool local = g.mode == kQuantLocal;   // activations written into the stages here
   uint32_t* part_flag = g.ctrl + kCtrlPartFlags;
   uint32_t* unit_flag = g.ctrl + kCtrlUnitFlags;
+  constexpr int kGroups = kRowsA / 8;         // 8-row quantization units per k-step (kQuantGlobal)
   bool abort = false;
   uint32_t epoch = 0;
 
+  // Tiles of this range shared with other CTAs: the first segment when the
+  // range starts inside a tile or ends before that tile's end, the last one
+  // when the range ends inside a later tile (CTA-uniform).
+  const int t_first = it0 / KT, t_last = (it1 - 1) / KT;
+  const int split_first = (it0 % KT != 0 || it1 < (t_first + 1) * KT) ? t_first : -1;
+  const int split_last = (t_last != t_first && it1 % KT != 0) ? t_last : -1;
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], local ? 2 : 1);    // copied bytes (+ activations written by the quantizing warps)
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, kEpiThreads);
+    mbar_init(acc_empty, kDrainThreads);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -121,17 +171,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 
   if (warp == 0) {
     // ---- producer.  A stage is one 256-wide k-step of one output tile.
+    // Weights are read once: evict-first keeps L2 for the activations and
+    // the partial sums.
+    const uint64_t evict_first = policy_evict_first();
     auto w_load = [&](int it, uint8_t* st, uint64_t* bar) {
       const int t = it / KT, kt = it - t * KT;
       for (int q = 0; q < 2; ++q) {
         const int rt = 2 * t + q;
         if (rt < g.w_tiles) {
-          bulk_g2s(st + q * kTileBytes, g.w_codes + (static_cast<size_t>(rt * KT + kt) << 14), kTileBytes, bar);
-          bulk_g2s(st + C::kW + C::kA + C::kSA + q * 1024, g.w_scales + (static_cast<size_t>(rt * KT + kt) << 10),
-                   1024, bar);
+          bulk_g2s_hint(st + q * kTileBytes, g.w_codes + (static_cast<size_t>(rt * KT + kt) << 14), kTileBytes, bar,
+                        evict_first);
+          bulk_g2s_hint(st + C::kW + C::kA + C::kSA + q * 1024,
+                        g.w_scales + (static_cast<size_t>(rt * KT + kt) << 10), 1024, bar, evict_first);
         }
       }
     };
+    // Pre-quantized activations (TILED, rows 0..kRowsA-1 of row tile 0).
     auto a_load = [&](int it, uint8_t* st, uint64_t* bar) {
       const int kt = it % KT;
       bulk_g2s(st + C::kW, g.a_codes + (static_cast<size_t>(kt) << 14), C::kALoad, bar);
@@ -140,9 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     auto stage_bytes = [&](int it) -> uint32_t {
       const int t = it / KT;
       const int nsub = (2 * t + 1 < g.w_tiles) ? 2 : 1;
-      return static_cast<uint32_t>(C::kALoad + C::kSA + nsub * (kTileBytes + 1024));
+      return static_cast<uint32_t>((local ? 0 : C::kALoad + C::kSA) + nsub * (kTileBytes + 1024));
     };
-    const int n_iter = it1 - it0;
     const int npre = n_iter < C::kStages ? n_iter : C::kStages;
     // Lane i requests the weights of prologue stage i at once: the packed
     // weights are never written by the kernel this one follows (the repack
@@ -153,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     }
     griddep_wait();
     epoch = ld_acquire_gpu(g.ctrl + kCtrlEpoch);
-    if (g.x != nullptr) {
+    if (g.mode == kQuantGlobal) {
       // Wait until every activation k-step this CTA reads is quantized: the
       // lanes share the (k-step, 8-row unit) flags of the range.
       const int nkt = n_iter < KT ? n_iter : KT;
@@ -166,8 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       __syncwarp();                  // every lane is ordered after every lane's acquire
       fence_proxy_async_global();    // ... and so are its bulk copies below
     }
-    abort = __any_sync(0xFFFFFFFFu, abort);
-    if (lane < npre) a_load(it0 + lane, smem + lane * C::kStageBytes, &full[lane]);
+    if (!local && lane < npre) a_load(it0 + lane, smem + lane * C::kStageBytes, &full[lane]);
     __syncwarp();
     if (lane == 0) {
       for (int i = npre; i < n_iter; ++i) {
@@ -177,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         uint8_t* st = smem + s * C::kStageBytes;
         mbar_arrive_expect_tx(&full[s], stage_bytes(it0 + i));
         w_load(it0 + i, st, &full[s]);
-        a_load(it0 + i, st, &full[s]);
+        if (!local) a_load(it0 + i, st, &full[s]);
       }
     }
     __syncwarp();   // whole warp reaches the final barrier converged
@@ -204,32 +257,47 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     }
     __syncwarp();
   } else {
-    griddep_wait();
-    epoch = ld_acquire_gpu(g.ctrl + kCtrlEpoch);
-    const int et = threadIdx.x - 64;   // 0..255 within the epilogue warps
-
-    // ---- quantize this CTA's activation units: unit u = rg * KT + kt is
-    // rows 8 rg .. 8 rg + 7, k-step kt; warp 2 + w takes row 8 rg + w, lane l
-    // elements 8 l .. 8 l + 7 of the k-step.  Up to four units per pass have
-    // their loads in flight together.
-    if (g.x != nullptr) {
+    // ---- warps 2..9
+    const int et = threadIdx.x - 64;   // 0..255
+    if (g.mode == kQuantGlobal && g.vec_ok != 0 && lane == 0) {
+      // L2 prefetch of the rows of this CTA's first units (a prefetch returns
+      // no data, so it may run before the dependency wait).
+      const int units = KT * kGroups;
+      for (int u = cta; u < units && u < cta + 4 * g.grid; u += g.grid) {
+        const int kt = u % KT, r = (u / KT) * 8 + (warp - 2);
+        const int n = g.K - kt * 256 < 256 ? g.K - kt * 256 : 256;
+        const uint32_t bytes = static_cast<uint32_t>(2 * n) & ~15u;
+        if (r < g.M && bytes != 0) bulk_prefetch_l2(g.x + static_cast<size_t>(r) * g.ldx + kt * 256, bytes);
+      }
+    }
+    if (g.mode == kQuantGlobal) {
+      griddep_wait();
+      epoch = ld_acquire_gpu(g.ctrl + kCtrlEpoch);
+      // Quantize this CTA's units into the TILED workspace image: unit
+      // u = rg * KT + kt is rows 8 rg .. 8 rg + 7 of k-step kt; warp 2 + w
+      // takes row 8 rg + w, lane l elements 8 l .. 8 l + 7.  Up to four units
+      // per pass have their loads in flight together.
       const int units = KT * kGroups;
       const int nb = (g.K + 31) >> 5;
       for (int u0 = cta; u0 < units; u0 += 4 * g.grid) {
-        uint16_t v[4][8];
+        uint4 v4[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int u = u0 + j * g.grid;
           const int kt = u % KT, r = (u / KT) * 8 + (warp - 2);
-          load8_bf16(g.x, u < units ? r : g.M, g.M, g.K, g.ldx, kt * 256 + lane * 8, g.vec_ok != 0, v[j]);
+          v4[j] = load8_packed(g.x, u < units ? r : g.M, g.M, g.K, g.ldx, kt * 256 + lane * 8, g.vec_ok != 0);
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int u = u0 + j * g.grid;
           if (u >= units) break;   // warp-uniform
           const int kt = u % KT, r = (u / KT) * 8 + (warp - 2);
+          const uint16_t v[8] = {static_cast<uint16_t>(v4[j].x & 0xFFFF), static_cast<uint16_t>(v4[j].x >> 16),
+                                 static_cast<uint16_t>(v4[j].y & 0xFFFF), static_cast<uint16_t>(v4[j].y >> 16),
+                                 static_cast<uint16_t>(v4[j].z & 0xFFFF), static_cast<uint16_t>(v4[j].z >> 16),
+                                 static_cast<uint16_t>(v4[j].w & 0xFFFF), static_cast<uint16_t>(v4[j].w >> 16)};
           uint32_t sbyte;
-          const uint32_t packed = quantize8(v[j], sbyte);
+          const uint32_t packed = quantize8(v, sbyte);
           const int blk = kt * 8 + (lane >> 2);
           *reinterpret_cast<uint32_t*>(g.a_codes + tiled_code_offset(r, kt * 128 + lane * 4, KT)) = packed;
           if ((lane & 3) == 0)
@@ -237,9 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         }
         // The units are read by other CTAs' bulk copies (async proxy).
         fence_proxy_async_global();
-        named_barrier(1, kEpiThreads);
+        named_barrier(kBarAll, kEpiThreads);
         if (et == 0) {
-          __threadfence();
           for (int j = 0; j < 4; ++j) {
             const int u = u0 + j * g.grid;
             if (u < units) st_release_gpu(unit_flag + (u % KT) * 8 + u / KT, epoch + 1);
@@ -247,15 +314,100 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         }
       }
     }
-
-    // ---- epilogue: warp w drains accumulator rows 32*(w%4).., columns 128*h..
+  if ((warp & 3) >= 2) {
+    // ---- warps 2, 3, 6, 7 (kQuantLocal): quantize each stage's activations
+    // (k-step kt, rows 0..kRowsA-1) straight into its shared-memory image.
+    // Warp qw takes rows qw, qw + 4, ...; lane l elements 8 l .. 8 l + 7,
+    // four lanes per 32-element block.  The loads of the next kDepth - 1
+    // chunks are in flight while a chunk is converted.
+    const int qw = (warp & 1) + 2 * ((warp - 2) >> 2);
+    const bool vec_ok = g.vec_ok != 0;
+    const int nb = (g.K + 31) >> 5;
+    if (local && lane == 0) {
+      // L2 prefetch of this CTA's first activation rows (a prefetch returns
+      // no data, so it may run before the dependency wait).
+      for (int i = 0; i < n_iter && i < 4; ++i) {
+        const int kt = (it0 + i) % KT;
+        const int n = g.K - kt * 256 < 256 ? g.K - kt * 256 : 256;
+        const uint32_t bytes = static_cast<uint32_t>(2 * n) & ~15u;
+        for (int j = 0; j < kRowsPerWarp; ++j) {
+          const int r = qw + 4 * j;
+          if (vec_ok && r < g.M && bytes != 0)
+            bulk_prefetch_l2(g.x + static_cast<size_t>(r) * g.ldx + kt * 256, bytes);
+        }
+      }
+    }
+    griddep_wait();
+    if (local) {
+      // Rows are handled in chunks of up to 8 per warp; kDepth chunks are in
+      // registers (16 x 16-byte loads per thread at most).
+      constexpr int kChunkRows = kRowsPerWarp < 8 ? kRowsPerWarp : 8;
+      constexpr int kChunks = kRowsPerWarp / kChunkRows;   // per stage
+      constexpr int kDepth = 16 / kChunkRows;
+      const int n_chunks = n_iter * kChunks;
+      auto load_chunk = [&](int c, uint4 (&buf)[kChunkRows]) {
+        const int i = c / kChunks, part = c - i * kChunks;
+        const int e0 = ((it0 + i) % KT) * 256 + lane * 8;
+#pragma unroll
+        for (int j = 0; j < kChunkRows; ++j)
+          buf[j] = load8_packed(g.x, qw + 4 * (part * kChunkRows + j), g.M, g.K, g.ldx, e0, vec_ok);
+      };
+      auto quant_chunk = [&](int c, const uint4 (&buf)[kChunkRows]) {
+        const int i = c / kChunks, part = c - i * kChunks;
+        const int s = i % C::kStages;
+        if (part == 0 && i >= C::kStages) mbar_wait(&empty[s], ((i / C::kStages) & 1) ^ 1, abort);
+        uint8_t* a_s = smem + s * C::kStageBytes + C::kW;
+        uint8_t* sa_s = a_s + C::kA;
+        const int blk = ((it0 + i) % KT) * 8 + (lane >> 2);
+#pragma unroll
+        for (int j = 0; j < kChunkRows; ++j) {
+          const int r = qw + 4 * (part * kChunkRows + j);
+          const uint16_t v[8] = {static_cast<uint16_t>(buf[j].x & 0xFFFF), static_cast<uint16_t>(buf[j].x >> 16),
+                                 static_cast<uint16_t>(buf[j].y & 0xFFFF), static_cast<uint16_t>(buf[j].y >> 16),
+                                 static_cast<uint16_t>(buf[j].z & 0xFFFF), static_cast<uint16_t>(buf[j].z >> 16),
+                                 static_cast<uint16_t>(buf[j].w & 0xFFFF), static_cast<uint16_t>(buf[j].w >> 16)};
+          uint32_t sbyte;
+          const uint32_t packed = quantize8(v, sbyte);
+          // row r of the 128-byte-swizzled K-major image; scale atom of
+          // blocks 0-3 / 4-7 of the k-step (row r: 16 (r % 32) + 4 (r / 32))
+          *reinterpret_cast<uint32_t*>(a_s + r * 128 + ((((lane >> 2) ^ (r & 7))) << 4) + (lane & 3) * 4) = packed;
+          if ((lane & 3) == 0)
+            sa_s[(lane >> 4) * 512 + 16 * (r & 31) + 4 * (r >> 5) + ((lane >> 2) & 3)] =
+                (r < g.M && blk < nb) ? static_cast<uint8_t>(sbyte) : 0x7F;
+        }
+        if (part == kChunks - 1) {
+          fence_proxy_async_smem();                // the MMA and tcgen05.cp read it
+          named_barrier(kBarQuant, kQuantThreads);
+          if (qw == 0 && lane == 0) mbar_arrive(&full[s]);
+        }
+      };
+      uint4 buf[kDepth][kChunkRows];
+#pragma unroll
+      for (int d = 0; d < kDepth - 1; ++d)
+        if (d < n_chunks) load_chunk(d, buf[d]);
+      for (int c0 = 0; c0 < n_chunks; c0 += kDepth) {
+#pragma unroll
+        for (int d = 0; d < kDepth; ++d) {
+          const int c = c0 + d;
+          if (c >= n_chunks) break;
+          if (c + kDepth - 1 < n_chunks) load_chunk(c + kDepth - 1, buf[(d + kDepth - 1) % kDepth]);
+          quant_chunk(c, buf[d]);
+        }
+      }
+    }
+    if (g.mode != kQuantGlobal) epoch = ld_acquire_gpu(g.ctrl + kCtrlEpoch);
+  } else {
+    // ---- warps 4, 5, 8, 9 drain the accumulator: warp w rows 32 (w % 4)..,
+    // columns 128 h.. (h = 0 for warps 4, 5; 1 for 8, 9).
+    if (g.mode != kQuantGlobal) {
+      griddep_wait();
+      epoch = ld_acquire_gpu(g.ctrl + kCtrlEpoch);
+    }
     const OutView& o = g.o;
     const int q = warp & 3;
     const int h = (warp - 2) >> 2;
     const int rl = q * 32 + lane;                 // accumulator row = activation row
-    const bool warp_live = q * 32 < kRowsA;       // quarters beyond kRowsA rows hold nothing
-    const bool live = warp_live && rl < g.M;
-    int split_first = -1, split_last = -1;        // this CTA's tiles that other CTAs share
+    const bool live = rl < g.M;
     int seg = 0, kt = it0 % KT;
     for (int it = it0; it < it1; ++seg) {
       const int len = (KT - kt) < (it1 - it) ? (KT - kt) : (it1 - it);
@@ -269,16 +421,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       // second pass is loaded.  A whole tile is stored; a part is published.
 #pragma unroll
       for (int pass = 0; pass < 2; ++pass) {
-        float v[64];
-        if (warp_live) {
-          uint32_t r[64];
+        uint32_t r[64];
 #pragma unroll
-          for (int c0 = 0; c0 < 64; c0 += 16)
-            tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128 + pass * 64 + c0,
-                      *reinterpret_cast<uint32_t(*)[16]>(&r[c0]));
-          tmem_wait_ld();
+        for (int c0 = 0; c0 < 64; c0 += 16)
+          tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128 + pass * 64 + c0,
+                    *reinterpret_cast<uint32_t(*)[16]>(&r[c0]));
+        tmem_wait_ld();
+        if (!ok) {
 #pragma unroll
-          for (int c = 0; c < 64; ++c) v[c] = ok ? __uint_as_float(r[c]) : 0.f;
+          for (int c = 0; c < 64; ++c) r[c] = 0u;
         }
         if (pass == 1) {
           tc_fence_before();
@@ -290,78 +441,85 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           for (int c0 = 0; c0 < 64; c0 += 32) {
             float chunk[32];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) chunk[c] = v[c0 + c];
+            for (int c = 0; c < 32; ++c) chunk[c] = __uint_as_float(r[c0 + c]);
             store_chunk(o, rl, n0 + pass * 64 + c0, chunk);
           }
         } else {
-          float4* P = reinterpret_cast<float4*>(g.partials + (static_cast<size_t>(slot) * kRowsA + rl) * kTileN +
-                                                h * 128 + pass * 64);
+          uint4* P = reinterpret_cast<uint4*>(g.partials + (static_cast<size_t>(slot) * kRowsA + rl) * kTileN +
+                                              h * 128 + pass * 64);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) __stcg(P + c, make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));
+          for (int c = 0; c < 16; ++c) __stcg(P + c, make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]));
         }
       }
       if (!whole) {
-        named_barrier(1, kEpiThreads);          // the whole part is written
-        if (et == 0) {
-          __threadfence();
-          st_release_gpu(part_flag + slot, epoch + 1);
-        }
-        if (it == it0) split_first = t;
-        else split_last = t;
+        named_barrier(kBarDrain, kDrainThreads);       // the whole part is written
+        if (threadIdx.x == 128) st_release_gpu(part_flag + slot, epoch + 1);
       }
       it += len;
       kt = 0;
     }
+  }
+  }
 
-    // ---- shared tiles: contributor j of n sums outputs [j/n, (j+1)/n) of
-    // the tile over every part in CTA order, adds the bias, stores bf16.
-    // Each thread keeps 2 groups (4 consecutive outputs each) x 4 parts of
-    // loads in flight.
-    for (int which = 0; which < 2; ++which) {
-      const int t = which == 0 ? split_first : split_last;
-      if (t < 0) continue;
-      const int c_lo = sk_owner(t * KT, g.total, g.grid);
-      const int c_hi = sk_owner(t * KT + KT - 1, g.total, g.grid);
-      if (warp == 2) {
-        for (int c = c_lo + lane; c <= c_hi; c += 32)
+  // ---- shared tiles (at most two), by warps 2..9.  Contributor j of n
+  // finishes outputs [j/n, (j+1)/n) of the tile: warp 2 waits for the other
+  // parts, then each thread sums 4 groups (4 consecutive outputs each) over
+  // all parts in CTA order, 4 parts' loads in flight per group, adds the bias
+  // and stores bf16.
+  if (warp >= 2 && (split_first >= 0 || split_last >= 0)) {
+    const int et = threadIdx.x - 64;   // 0..255
+    const int groups = g.M * (kTileN / 4);     // float4 groups of a tile's live rows
+    if (warp == 2) {
+#pragma unroll
+      for (int w = 0; w < 2; ++w) {
+        const int t = w == 0 ? split_first : split_last;
+        if (t < 0) continue;
+        const int lo = sk_owner(t * KT, g.total, g.grid), hi = sk_owner(t * KT + KT - 1, g.total, g.grid);
+        for (int c = lo + lane; c <= hi; c += 32)
           if (c != cta) flag_wait(part_flag + part_slot(c, t, KT, g.total, g.grid), epoch + 1, abort);
       }
-      named_barrier(1, kEpiThreads);
-      const int n_c = c_hi - c_lo + 1;
-      const int groups = g.M * (kTileN / 4);
-      const int j = cta - c_lo;
-      const int gb = static_cast<int>(static_cast<long long>(j) * groups / n_c);
-      const int ge = static_cast<int>(static_cast<long long>(j + 1) * groups / n_c);
-      for (int g0 = gb + et; g0 < ge; g0 += 2 * kEpiThreads) {
-        float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-        for (int cg = c_lo; cg <= c_hi; cg += 4) {
-          float4 p[4][2];
+    }
+    named_barrier(kBarAll, kEpiThreads);
+#pragma unroll 1
+    for (int w = 0; w < 2; ++w) {
+      const int t = w == 0 ? split_first : split_last;
+      if (t < 0) continue;
+      const int lo = sk_owner(t * KT, g.total, g.grid);
+      const int nc = sk_owner(t * KT + KT - 1, g.total, g.grid) - lo + 1;
+      const int j = cta - lo;
+      const int gb = static_cast<int>(static_cast<long long>(j) * groups / nc);
+      const int ge = static_cast<int>(static_cast<long long>(j + 1) * groups / nc);
+      for (int g0 = gb + et; g0 < ge; g0 += 4 * kEpiThreads) {
+        float4 acc[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int cg = 0; cg < nc; cg += 4) {
+          float4 p[4][4];
 #pragma unroll
           for (int jc = 0; jc < 4; ++jc) {
-            const int cc = cg + jc;
-            if (cc > c_hi) continue;
+            if (cg + jc >= nc) continue;
             const float4* Q = reinterpret_cast<const float4*>(
-                g.partials + static_cast<size_t>(part_slot(cc, t, KT, g.total, g.grid)) * kRowsA * kTileN);
+                g.partials + static_cast<size_t>(part_slot(lo + cg + jc, t, KT, g.total, g.grid)) * kRowsA * kTileN);
 #pragma unroll
-            for (int k = 0; k < 2; ++k)
-              if (g0 + kEpiThreads * k < ge) p[jc][k] = __ldcg(Q + g0 + kEpiThreads * k);
+            for (int k = 0; k < 4; ++k)
+              if (g0 + k * kEpiThreads < ge) p[k][jc] = __ldcg(Q + g0 + k * kEpiThreads);
           }
 #pragma unroll
-          for (int jc = 0; jc < 4; ++jc) {
-            if (cg + jc > c_hi) continue;
+          for (int k = 0; k < 4; ++k) {
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              acc[k].x += p[jc][k].x;
-              acc[k].y += p[jc][k].y;
-              acc[k].z += p[jc][k].z;
-              acc[k].w += p[jc][k].w;
+            for (int jc = 0; jc < 4; ++jc) {
+              if (cg + jc >= nc) continue;
+              acc[k].x += p[k][jc].x;
+              acc[k].y += p[k][jc].y;
+              acc[k].z += p[k][jc].z;
+              acc[k].w += p[k][jc].w;
             }
           }
         }
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          const int gi = g0 + kEpiThreads * k;
-          if (gi < ge) store_quad(o, gi / (kTileN / 4), t * kTileN + 4 * (gi % (kTileN / 4)), acc[k]);
+        for (int k = 0; k < 4; ++k) {
+          const int gi = g0 + k * kEpiThreads;
+          if (gi < ge) store_quad(g.o, gi / (kTileN / 4), t * kTileN + 4 * (gi % (kTileN / 4)), acc[k]);
         }
       }
     }
@@ -403,6 +561,7 @@ cudaError_t launch_decode(const DecodeProblem& p, const DeviceInfo& dev, cudaStr
   const int64_t Np = padded_rows(p.N);
   const int64_t Kp = padded_k(p.K);
   a.x = static_cast<const uint16_t*>(p.x);
+  a.mode = p.x == nullptr ? kPrequantized : ((Kp / kKTile) > kMaxUnitKT ? kQuantLocal : kQuantGlobal);
   a.ldx = p.ldx;
   a.vec_ok = p.x != nullptr && (reinterpret_cast<uintptr_t>(p.x) & 15) == 0 && (p.ldx % 8) == 0;
   a.a_codes = const_cast<uint8_t*>(p.a_codes);
@@ -419,12 +578,22 @@ cudaError_t launch_decode(const DecodeProblem& p, const DeviceInfo& dev, cudaStr
   a.w_tiles = static_cast<int>(Np / 128);
   a.n_tiles = static_cast<int>(ceil_div(p.N, kTileN));
   a.total = a.n_tiles * a.KT;
-  int grid = gemm_grid(dev);
+  // With fewer 256-row tiles than SMs, split every tile into the same number
+  // S of k-ranges (grid = tiles x S): each CTA then works on one tile, parts
+  // line up with tile boundaries (S parts per tile when S divides K/256), and
+  // the SMs left over are free for the next launch to start on.  More tiles
+  // than SMs: balanced stream-K over all SMs.
+  const int max_grid = gemm_grid(dev);
+  int grid = max_grid;
+  if (a.n_tiles < max_grid) {
+    int split = max_grid / a.n_tiles;
+    if (split > a.KT) split = a.KT;
+    grid = a.n_tiles * split;
+  }
   if (grid > a.total) grid = a.total;
   a.grid = grid;
   a.partials = p.partials;
   a.ctrl = p.ctrl;
-  if (p.x != nullptr && a.KT > kMaxFusedKT) return cudaErrorInvalidValue;
   switch (gemm_rows_a(p.M)) {
     case 16: return launch_rows<16>(a, dev, s, 0);
     case 32: return launch_rows<32>(a, dev, s, 1);

@@ -36,9 +36,8 @@ constexpr int kCtrlEpoch = 0;
 constexpr int kCtrlDone = 1;
 constexpr int kCtrlPartFlags = 256;
 constexpr int kCtrlUnitFlags = 1024;
-// Largest K / 256 for which the decode kernel quantizes the activations
-// itself (8 unit flags per k-step fit the control region).
-constexpr int kMaxFusedKT = static_cast<int>((kDecodeCtrlBytes / 4 - kCtrlUnitFlags) / 8);
+// Largest K / 256 with unit flags for every k-step (8 per k-step).
+constexpr int kMaxUnitKT = static_cast<int>((kDecodeCtrlBytes / 4 - kCtrlUnitFlags) / 8);
 static_assert(kCtrlPartFlags + 2 * kMaxStreamKCtas <= kCtrlUnitFlags, "part flags overlap unit flags");
 // Activation rows of a 128-row tile the GEMM loads: 16, 32 or 64 when
 // M <= kDecodeMaxM (only those rows of the tiled activations are read), else 128.
@@ -80,9 +79,9 @@ uint32_t gemm_read_clear_error();
 
 // decode.cu: M <= kDecodeMaxM in one launch.
 struct DecodeProblem {
-  const void* x;            // bf16 activations [M][ldx]; null when a_codes/a_scales hold them already
+  const void* x;            // bf16 activations [M][ldx] (quantized by the kernel); null when a_codes/a_scales hold them
   int ldx;
-  const uint8_t* a_codes;   // TILED activation codes (written by the kernel when x != null)
+  const uint8_t* a_codes;   // TILED activation codes (input when x == null, else scratch)
   const uint8_t* a_scales;  // TILED activation scales
   const uint8_t* w_packed;
   const void* bias;

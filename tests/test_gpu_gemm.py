@@ -178,12 +178,13 @@ def test_tiny_shape_sweep(capi):
     assert not bad, f"{len(bad)} of {len(TINY)} shapes failed: {bad[:4]}"
 
 
-@pytest.mark.parametrize("M,N,K", [(64, 256, 32768), (5, 300, 65536), (2, 256, 98560)])
+@pytest.mark.parametrize("M,N,K", [(64, 256, 32768), (5, 300, 65536), (2, 256, 98560), (33, 256, 98560)])
 def test_tiles_shared_by_many_ctas(capi, M, N, K):
     """One or two output tiles over a long K: every tile's k-steps are split
     over dozens of CTAs (more than a warp's worth of parts to wait for and
-    sum); K = 98560 also passes the longest K whose activations the decode
-    kernel quantizes itself, so the quantizer kernel runs first."""
+    sum).  K = 98560 is past the longest K with a flag per activation unit,
+    so every CTA quantizes the activations of its own k-steps, also for
+    M = 33 (64-row tiles)."""
     full_check(capi, M, N, K, seed=21, with_bias=True)
 
 
