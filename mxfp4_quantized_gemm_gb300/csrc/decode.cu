@@ -23,9 +23,10 @@
 //    dependent launch at once, so a CTA requests its first weight stages as
 //    soon as it has an SM, usually while the previous call is still running
 //    (the packed weights are never written by the kernel this one follows);
-//  * the activations are quantized inside the kernel, by one of two schemes
-//    (DecodeMode): every CTA quantizes a share of the activation units and
-//    publishes a flag per unit, or each CTA quantizes its own k-steps;
+//  * the activations are quantized inside the kernel: every CTA quantizes a
+//    share of the (k-step, 8-row) units into the TILED workspace image and
+//    publishes a flag per unit, and producers copy a k-step in once its
+//    units are flagged;
 //  * tiles cut by CTA boundaries are summed inside the kernel: every part is
 //    published as fp32 with a flag, then each contributing CTA sums a 1/n
 //    share of the tile's outputs over all parts in CTA order (deterministic:
@@ -58,10 +59,10 @@ namespace mx {
 static __device__ uint32_t g_decode_error;
 
 struct DecodeArgs {
-  const uint16_t* x;       // bf16 activations [M][ldx] (modes kQuantGlobal, kQuantLocal)
+  const uint16_t* x;       // bf16 activations [M][ldx] (mode kQuantGlobal)
   int ldx;
   int vec_ok;              // x and ldx allow 16-byte row loads
-  int mode;                // kPrequantized, kQuantGlobal or kQuantLocal
+  int mode;                // kPrequantized or kQuantGlobal
   uint8_t* a_codes;        // TILED activation codes (read; written first in mode kQuantGlobal)
   uint8_t* a_scales;       // TILED activation scales
   const uint8_t* w_codes;
@@ -75,28 +76,6 @@ struct DecodeArgs {
   float* partials;         // 2 slots per CTA, kRowsA x 256 floats each
   uint32_t* ctrl;          // epoch, done counter, part flags
 };
-
-// Where the activation codes of a stage come from.
-//  kPrequantized: the caller's TILED codes/scales, copied in by the producer.
-//  kQuantGlobal:  every CTA first quantizes a share of the (k-step, 8-row)
-//                 units into the TILED workspace image and publishes a flag
-//                 per unit; producers wait for the flags of their k-steps and
-//                 copy the codes in.  x is read once in all.
-//  kQuantLocal:   each CTA quantizes the k-steps of its own range straight
-//                 into its stages (warps 2, 3, 6, 7); no flags, but each CTA
-//                 reads x for its k-steps (M x 512 bytes per stage).
-enum DecodeMode : int { kPrequantized = 0, kQuantGlobal = 1, kQuantLocal = 2 };
-
-// Partial-sum slot of CTA c's part of tile t: slot 0 when t is where c's
-// range begins, slot 1 when t is where it ends.
-__device__ __forceinline__ int part_slot(int c, int t, int KT, int total, int grid) {
-  return 2 * c + (sk_begin(c, total, grid) / KT == t ? 0 : 1);
-}
-
-constexpr int kQuantThreads = 128;     // warps 2, 3, 6, 7
-constexpr int kDrainThreads = 128;     // warps 4, 5, 8, 9: accumulator rows 0..63
-// Named barriers (0 is __syncthreads).
-constexpr uint32_t kBarQuant = 1, kBarDrain = 2, kBarAll = 3;
 
 // Loads this lane's 8 bf16 values of row r, elements [e0, e0 + 8), as a
 // uint4 (zeros past K or for r >= M).
@@ -115,10 +94,29 @@ __device__ __forceinline__ uint4 load8_packed(const uint16_t* __restrict__ x, in
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Where the activation codes of a stage come from.
+//  kPrequantized: the caller's TILED codes/scales, copied in by the producer.
+//  kQuantGlobal:  every CTA first quantizes a share of the (k-step, 8-row)
+//                 units into the TILED workspace image and publishes a flag
+//                 per unit; producers wait for the flags of their k-steps and
+//                 copy the codes in.  x is read once in all.
+// (Quantizing inside each CTA from its own copy of x was measured slower at
+// every M: its stages complete at a fraction of the rate of copied ones.)
+enum DecodeMode : int { kPrequantized = 0, kQuantGlobal = 1 };
+
+// Partial-sum slot of CTA c's part of tile t: slot 0 when t is where c's
+// range begins, slot 1 when t is where it ends.
+__device__ __forceinline__ int part_slot(int c, int t, int KT, int total, int grid) {
+  return 2 * c + (sk_begin(c, total, grid) / KT == t ? 0 : 1);
+}
+
+constexpr int kDrainThreads = 128;     // warps 4, 5, 8, 9: accumulator rows 0..63
+// Named barriers (0 is __syncthreads).
+constexpr uint32_t kBarDrain = 2, kBarAll = 3;
+
 template <int kRowsA>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs g) {
   using C = Cfg<kRowsA>;
-  constexpr int kRowsPerWarp = kRowsA / 4;   // rows a quantizing warp covers per stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kRing);
@@ -133,7 +131,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   const int it0 = sk_begin(cta, g.total, g.grid);
   const int it1 = sk_begin(cta + 1, g.total, g.grid);
   const int n_iter = it1 - it0;
-  const bool local = g.mode == kQuantLocal;   // activations written into the stages here
   uint32_t* part_flag = g.ctrl + kCtrlPartFlags;
   uint32_t* unit_flag = g.ctrl + kCtrlUnitFlags;
   constexpr int kGroups = kRowsA / 8;         // 8-row quantization units per k-step (kQuantGlobal)
@@ -149,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      mbar_init(&full[s], local ? 2 : 1);    // copied bytes (+ activations written by the quantizing warps)
+      mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
@@ -195,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     auto stage_bytes = [&](int it) -> uint32_t {
       const int t = it / KT;
       const int nsub = (2 * t + 1 < g.w_tiles) ? 2 : 1;
-      return static_cast<uint32_t>((local ? 0 : C::kALoad + C::kSA) + nsub * (kTileBytes + 1024));
+      return static_cast<uint32_t>(C::kALoad + C::kSA + nsub * (kTileBytes + 1024));
     };
     const int npre = n_iter < C::kStages ? n_iter : C::kStages;
     // Lane i requests the weights of prologue stage i at once: the packed
@@ -220,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       __syncwarp();                  // every lane is ordered after every lane's acquire
       fence_proxy_async_global();    // ... and so are its bulk copies below
     }
-    if (!local && lane < npre) a_load(it0 + lane, smem + lane * C::kStageBytes, &full[lane]);
+    if (lane < npre) a_load(it0 + lane, smem + lane * C::kStageBytes, &full[lane]);
     __syncwarp();
     if (lane == 0) {
       for (int i = npre; i < n_iter; ++i) {
@@ -230,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         uint8_t* st = smem + s * C::kStageBytes;
         mbar_arrive_expect_tx(&full[s], stage_bytes(it0 + i));
         w_load(it0 + i, st, &full[s]);
-        if (!local) a_load(it0 + i, st, &full[s]);
+        a_load(it0 + i, st, &full[s]);
       }
     }
     __syncwarp();   // whole warp reaches the final barrier converged
@@ -247,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           const uint32_t ph = (i / C::kStages) & 1;
           if (!mbar_wait(&full[s], ph, abort)) break;
           tc_fence_after();
-          issue_stage_mma<kRowsA>(tmem, smem_u32(smem + s * C::kStageBytes), j != 0 ? 1u : 0u);
+          issue_stage_mma<C>(tmem, smem_u32(smem + s * C::kStageBytes), j != 0 ? 1u : 0u);
           mma_commit(&empty[s]);
         }
         mma_commit(acc_full);
@@ -315,86 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       }
     }
   if ((warp & 3) >= 2) {
-    // ---- warps 2, 3, 6, 7 (kQuantLocal): quantize each stage's activations
-    // (k-step kt, rows 0..kRowsA-1) straight into its shared-memory image.
-    // Warp qw takes rows qw, qw + 4, ...; lane l elements 8 l .. 8 l + 7,
-    // four lanes per 32-element block.  The loads of the next kDepth - 1
-    // chunks are in flight while a chunk is converted.
-    const int qw = (warp & 1) + 2 * ((warp - 2) >> 2);
-    const bool vec_ok = g.vec_ok != 0;
-    const int nb = (g.K + 31) >> 5;
-    if (local && lane == 0) {
-      // L2 prefetch of this CTA's first activation rows (a prefetch returns
-      // no data, so it may run before the dependency wait).
-      for (int i = 0; i < n_iter && i < 4; ++i) {
-        const int kt = (it0 + i) % KT;
-        const int n = g.K - kt * 256 < 256 ? g.K - kt * 256 : 256;
-        const uint32_t bytes = static_cast<uint32_t>(2 * n) & ~15u;
-        for (int j = 0; j < kRowsPerWarp; ++j) {
-          const int r = qw + 4 * j;
-          if (vec_ok && r < g.M && bytes != 0)
-            bulk_prefetch_l2(g.x + static_cast<size_t>(r) * g.ldx + kt * 256, bytes);
-        }
-      }
-    }
+    // ---- warps 2, 3, 6, 7: idle until the shared-tile sums.
     griddep_wait();
-    if (local) {
-      // Rows are handled in chunks of up to 8 per warp; kDepth chunks are in
-      // registers (16 x 16-byte loads per thread at most).
-      constexpr int kChunkRows = kRowsPerWarp < 8 ? kRowsPerWarp : 8;
-      constexpr int kChunks = kRowsPerWarp / kChunkRows;   // per stage
-      constexpr int kDepth = 16 / kChunkRows;
-      const int n_chunks = n_iter * kChunks;
-      auto load_chunk = [&](int c, uint4 (&buf)[kChunkRows]) {
-        const int i = c / kChunks, part = c - i * kChunks;
-        const int e0 = ((it0 + i) % KT) * 256 + lane * 8;
-#pragma unroll
-        for (int j = 0; j < kChunkRows; ++j)
-          buf[j] = load8_packed(g.x, qw + 4 * (part * kChunkRows + j), g.M, g.K, g.ldx, e0, vec_ok);
-      };
-      auto quant_chunk = [&](int c, const uint4 (&buf)[kChunkRows]) {
-        const int i = c / kChunks, part = c - i * kChunks;
-        const int s = i % C::kStages;
-        if (part == 0 && i >= C::kStages) mbar_wait(&empty[s], ((i / C::kStages) & 1) ^ 1, abort);
-        uint8_t* a_s = smem + s * C::kStageBytes + C::kW;
-        uint8_t* sa_s = a_s + C::kA;
-        const int blk = ((it0 + i) % KT) * 8 + (lane >> 2);
-#pragma unroll
-        for (int j = 0; j < kChunkRows; ++j) {
-          const int r = qw + 4 * (part * kChunkRows + j);
-          const uint16_t v[8] = {static_cast<uint16_t>(buf[j].x & 0xFFFF), static_cast<uint16_t>(buf[j].x >> 16),
-                                 static_cast<uint16_t>(buf[j].y & 0xFFFF), static_cast<uint16_t>(buf[j].y >> 16),
-                                 static_cast<uint16_t>(buf[j].z & 0xFFFF), static_cast<uint16_t>(buf[j].z >> 16),
-                                 static_cast<uint16_t>(buf[j].w & 0xFFFF), static_cast<uint16_t>(buf[j].w >> 16)};
-          uint32_t sbyte;
-          const uint32_t packed = quantize8(v, sbyte);
-          // row r of the 128-byte-swizzled K-major image; scale atom of
-          // blocks 0-3 / 4-7 of the k-step (row r: 16 (r % 32) + 4 (r / 32))
-          *reinterpret_cast<uint32_t*>(a_s + r * 128 + ((((lane >> 2) ^ (r & 7))) << 4) + (lane & 3) * 4) = packed;
-          if ((lane & 3) == 0)
-            sa_s[(lane >> 4) * 512 + 16 * (r & 31) + 4 * (r >> 5) + ((lane >> 2) & 3)] =
-                (r < g.M && blk < nb) ? static_cast<uint8_t>(sbyte) : 0x7F;
-        }
-        if (part == kChunks - 1) {
-          fence_proxy_async_smem();                // the MMA and tcgen05.cp read it
-          named_barrier(kBarQuant, kQuantThreads);
-          if (qw == 0 && lane == 0) mbar_arrive(&full[s]);
-        }
-      };
-      uint4 buf[kDepth][kChunkRows];
-#pragma unroll
-      for (int d = 0; d < kDepth - 1; ++d)
-        if (d < n_chunks) load_chunk(d, buf[d]);
-      for (int c0 = 0; c0 < n_chunks; c0 += kDepth) {
-#pragma unroll
-        for (int d = 0; d < kDepth; ++d) {
-          const int c = c0 + d;
-          if (c >= n_chunks) break;
-          if (c + kDepth - 1 < n_chunks) load_chunk(c + kDepth - 1, buf[(d + kDepth - 1) % kDepth]);
-          quant_chunk(c, buf[d]);
-        }
-      }
-    }
     if (g.mode != kQuantGlobal) epoch = ld_acquire_gpu(g.ctrl + kCtrlEpoch);
   } else {
     // ---- warps 4, 5, 8, 9 drain the accumulator: warp w rows 32 (w % 4)..,
@@ -549,7 +468,8 @@ static cudaError_t launch_rows(const DecodeArgs& a, const DeviceInfo& dev, cudaS
   using C = Cfg<kRowsA>;
   if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
   if (!g_attr_set[dev.device][which]) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<kRowsA>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_kernel<kRowsA>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     g_attr_set[dev.device][which] = true;
   }
@@ -561,7 +481,6 @@ cudaError_t launch_decode(const DecodeProblem& p, const DeviceInfo& dev, cudaStr
   const int64_t Np = padded_rows(p.N);
   const int64_t Kp = padded_k(p.K);
   a.x = static_cast<const uint16_t*>(p.x);
-  a.mode = p.x == nullptr ? kPrequantized : ((Kp / kKTile) > kMaxUnitKT ? kQuantLocal : kQuantGlobal);
   a.ldx = p.ldx;
   a.vec_ok = p.x != nullptr && (reinterpret_cast<uintptr_t>(p.x) & 15) == 0 && (p.ldx % 8) == 0;
   a.a_codes = const_cast<uint8_t*>(p.a_codes);
@@ -594,7 +513,20 @@ cudaError_t launch_decode(const DecodeProblem& p, const DeviceInfo& dev, cudaStr
   a.grid = grid;
   a.partials = p.partials;
   a.ctrl = p.ctrl;
-  switch (gemm_rows_a(p.M)) {
+  // Activation source: copied in when pre-quantized; else quantized by all
+  // CTAs with unit flags; past the flags' K range, by the standalone
+  // quantizer kernel first.
+  const int rows = gemm_rows_a(p.M);
+  if (p.x == nullptr) {
+    a.mode = kPrequantized;
+  } else if (a.KT <= kMaxUnitKT) {
+    a.mode = kQuantGlobal;
+  } else {
+    cudaError_t e = launch_quant(p.x, p.M, p.K, p.ldx, a.a_codes, a.a_scales, true, rows, dev, s);
+    if (e != cudaSuccess) return e;
+    a.mode = kPrequantized;
+  }
+  switch (rows) {
     case 16: return launch_rows<16>(a, dev, s, 0);
     case 32: return launch_rows<32>(a, dev, s, 1);
     default: return launch_rows<64>(a, dev, s, 2);

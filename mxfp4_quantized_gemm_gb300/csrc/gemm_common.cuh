@@ -26,9 +26,10 @@ struct Cfg {
   static constexpr int kW = 2 * kTileBytes;       // 256 weight rows of codes
   // Only the first kRowsA activation rows are loaded and reserved per stage.
   // The M = 128 MMA reads 16 KiB from the activation offset; for kRowsA <
-  // 128 the rows past kRowsA come from whatever follows (the next stage, or a
-  // tail pad after the last one, so every read stays inside the allocation)
-  // and feed only accumulator rows that are never read.
+  // 128 the rows past kRowsA come from whatever follows (the rest of the
+  // stage, the next stage, or a tail pad after the last one, so every read
+  // stays inside the allocation) and feed only accumulator rows that are
+  // never read.
   static constexpr int kALoad = kRowsA * 128;
   static constexpr int kA = kALoad;
   static constexpr int kTailPad = kTileBytes - kALoad;
@@ -117,9 +118,8 @@ __device__ __forceinline__ void store_quad(const OutView& o, int m, int n, float
 // of one stage: accumulator [128 act rows x 256 weight rows] at `tmem`,
 // activation scales at TMEM column sfa (2 atoms), weight scales at sfb
 // (2 atoms x 2 row halves).  `accumulate` = 0 starts a new tile.
-template <int kRowsA>
+template <typename C>
 __device__ __forceinline__ void issue_stage_mma(uint32_t tmem, uint32_t stage_base, uint32_t accumulate) {
-  using C = Cfg<kRowsA>;
   const uint32_t sfa = tmem + C::kSfa, sfb = tmem + C::kSfb;
   const uint32_t w_s = stage_base, a_s = stage_base + C::kW, sa_s = a_s + C::kA, sw_s = sa_s + C::kSA;
   tmem_cp_scales(sfa + 0, sdesc_scales(sa_s));

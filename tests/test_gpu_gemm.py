@@ -183,8 +183,8 @@ def test_tiles_shared_by_many_ctas(capi, M, N, K):
     """One or two output tiles over a long K: every tile's k-steps are split
     over dozens of CTAs (more than a warp's worth of parts to wait for and
     sum).  K = 98560 is past the longest K with a flag per activation unit,
-    so every CTA quantizes the activations of its own k-steps, also for
-    M = 33 (64-row tiles)."""
+    so the standalone quantizer kernel runs before the GEMM (M = 2 and the
+    64-row tiles of M = 33)."""
     full_check(capi, M, N, K, seed=21, with_bias=True)
 
 
@@ -232,3 +232,24 @@ def test_one_workspace_for_every_shape_and_graph_replays(capi):
         assert capi.mxfp4_get_device_error() == capi.OK
         for o, w in zip(outs, want):
             assert np.array_equal(host_bits(o), w)
+
+
+@pytest.mark.parametrize("M,N,K,pad", [(5, 300, 100, 0), (3, 520, 5120, 1), (16, 256, 1000, 3), (40, 700, 2056, 1)])
+def test_unaligned_activation_rows(capi, M, N, K, pad):
+    """bf16 rows that are not 16-byte aligned (lda = K + pad) or K % 8 != 0:
+    the quantizing CTAs fall back to element loads, and the results must
+    still match the oracle."""
+    x, wc, ws, b = make_problem(M, N, K, seed=77, with_bias=True)
+    packed = pack_weights(capi, wc, ws, K)
+    lda = K + pad
+    xpad = np.zeros((M, lda), dtype=np.uint16)
+    xpad[:, :K] = x
+    xd = dev_bf16(xpad)
+    out = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
+    wsb = capi.mxfp4_gemm_workspace_bytes(M, N, K)
+    work = gemm_workspace(capi, wsb)
+    capi.mxfp4_gemm(xd, lda, None, None, 0, packed, dev_bf16(b), out, N, M, N, K, work, wsb)
+    torch.cuda.synchronize()
+    assert capi.mxfp4_get_device_error() == capi.OK
+    acc, mag = oracle_gemm_rows(x, np.arange(M), wc, ws, K, b)
+    check_close(host_bits(out), acc, mag, n_acc(K), what=f"M={M} N={N} K={K} lda={lda}")
