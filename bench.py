@@ -91,8 +91,11 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """DRAM bytes per GEMM launch from the committed ncu summary, if taken on this source."""
+def recorded_traffic(cases):
+    """DRAM bytes per decode launch, averaged over `cases`: the DRAM/algorithmic
+    ratio ncu measured for each (N,K) (profiles/decode_gemm_traffic.txt) times
+    each case's algorithmic bytes.  None unless the ratios were taken on this
+    kernel source."""
     p = os.path.join(ROOT, "profiles", "decode_gemm_traffic.txt")
     try:
         fields = {}
@@ -100,11 +103,12 @@ def recorded_traffic():
             if "=" in line and not line.startswith("#"):
                 k, v = line.split("=", 1)
                 fields[k.strip()] = v.strip()
-        if fields.get("source_hash") == kernel_source_hash():
-            return float(fields["dram_bytes_per_step_gemm"])
+        if fields.get("source_hash") != kernel_source_hash():
+            return None
+        tot = sum(float(fields[f"ratio_{N}_{K}"]) * linear_bytes(M, N, K) for (M, N, K) in cases)
+        return round(tot / len(cases))
     except Exception:
-        pass
-    return None
+        return None
 
 
 # ------------------------------------------------------------------ clocks
@@ -305,7 +309,7 @@ def run_ours(args, world, rank, local):
     per_case_ms = [ev[j][0].elapsed_time(ev[j][1]) for j in range(len(state))]
     kbytes = [linear_bytes(c["M"], c["N"], c["K"]) for c in state]
     achieved = sum(kbytes) / (sum(per_case_ms) * 1e-3) / 1e9
-    traffic = recorded_traffic()
+    traffic = recorded_traffic([(c['M'], c['N'], c['K']) for c in state])
 
     # ---- e2e through the public API: H2D inputs, fused quant+GEMM call, D2H outputs
     e2e_steps = max(3, min(args.e2e_steps, K_steps))
