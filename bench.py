@@ -187,6 +187,12 @@ def dist_max(value: float, world: int) -> float:
     return float(t.item())
 
 
+def throughput_gbs(bytes_per_step: float, steps: int, world: int, ms_max: float) -> float:
+    """Whole-job GB/s: every rank runs `steps` steps of `bytes_per_step`; `ms_max` is
+    the slowest rank's time for them (weak scaling: work per rank is fixed)."""
+    return bytes_per_step * steps * world / (ms_max * 1e-3) / 1e9
+
+
 def dist_barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -303,7 +309,7 @@ def run_ours(args, world, rank, local):
     ms_total = dist_max(ms_total, world)
 
     bytes_step = sum(linear_bytes(c["M"], c["N"], c["K"]) for c in state)
-    value = bytes_step * K_steps * world / (ms_total * 1e-3) / 1e9
+    value = throughput_gbs(bytes_step, K_steps, world, ms_total)
 
     # per-case durations: events of the last step of the last replay (inside the timed region)
     per_case_ms = [ev[j][0].elapsed_time(ev[j][1]) for j in range(len(state))]
@@ -335,7 +341,7 @@ def run_ours(args, world, rank, local):
         e1.record(stream)
     stream.synchronize()
     e2e_ms = dist_max(e0.elapsed_time(e1), world)
-    e2e_value = bytes_step * e2e_steps * world / (e2e_ms * 1e-3) / 1e9
+    e2e_value = throughput_gbs(bytes_step, e2e_steps, world, e2e_ms)
 
     extra = {}
     if not args.no_secondary:
