@@ -12,7 +12,9 @@
 // and stays resident; activations stream through a ring of 128 x 64 bf16
 // slabs fed by TMA tensor loads; one thread issues tcgen05.mma.kind::f16
 // (bf16 x bf16 -> fp32 TMEM); four warps drain the double-buffered
-// accumulator while the next M tile is multiplied.
+// accumulator while the next M tile is multiplied, staging each 32-row x
+// 64-column piece in shared memory so that every warp store writes whole
+// 128-byte row segments.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -29,6 +31,7 @@ static __device__ uint32_t g_bmm_error;
 
 constexpr int kBmmStages = 4;
 constexpr int kSlabBytes = 128 * 128;      // 128 rows x 64 bf16
+constexpr int kStageOutBytes = 32 * 128;   // per epilogue warp: 32 rows x 64 bf16 of output
 
 struct BmmArgs {
   const uint8_t* w_packed;
@@ -38,6 +41,7 @@ struct BmmArgs {
   size_t w_batch_bytes, w_code_bytes;
   int KT;                    // Kp / 256 of the packed weights
   bool batch_major;
+  bool vec_out;              // out 16-byte aligned and N % 8 == 0: 16-byte output stores
 };
 
 __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, int c0, int c1, int c2,
@@ -70,7 +74,8 @@ __global__ void __launch_bounds__(192, 1) a16wfp4_bmm_kernel(const __grid_consta
   const int BN = g.BN;
   uint8_t* wsm = smem;                                       // KS slabs of BN rows x 128 B
   uint8_t* xsm = smem + static_cast<size_t>(g.KS) * BN * 128; // ring of x slabs
-  uint64_t* full = reinterpret_cast<uint64_t*>(xsm + kBmmStages * kSlabBytes);
+  uint8_t* osm = xsm + kBmmStages * kSlabBytes;               // 4 x kStageOutBytes output staging
+  uint64_t* full = reinterpret_cast<uint64_t*>(osm + 4 * kStageOutBytes);
   uint64_t* empty = full + kBmmStages;
   uint64_t* acc_full = empty + kBmmStages;
   uint64_t* acc_empty = acc_full + 2;
@@ -184,46 +189,63 @@ __global__ void __launch_bounds__(192, 1) a16wfp4_bmm_kernel(const __grid_consta
     }
     __syncwarp();
   } else {
-    // ---- epilogue
+    // ---- epilogue: warp q = warp % 4 drains accumulator rows 32 q .. 32 q + 31
+    // in pieces of 64 columns.  Lane l converts row l's piece to bf16 and
+    // writes it to the warp's staging area (16-byte chunk c of row r at
+    // chunk c ^ (r % 8): conflict-free both ways); then each pass stores 4
+    // rows x 128 contiguous bytes.
     const int q = warp & 3;
+    uint8_t* stg = osm + (warp - 2) * kStageOutBytes;
+    auto row_ptr = [&](int m) -> __nv_bfloat16* {
+      return g.batch_major ? g.out + (static_cast<size_t>(m) * g.B + b) * g.N
+                           : g.out + (static_cast<size_t>(b) * g.M + m) * g.N;
+    };
     for (int mt = mt0, i = 0; mt < mt1; ++mt, ++i) {
       const int buf = i & 1;
       const uint32_t use = i >> 1;
       const bool ok = mbar_wait(&acc_full[buf], use & 1, abort);
       tc_fence_after();
-      const int m = mt * 128 + q * 32 + lane;
-      __nv_bfloat16* dst_row =
-          g.batch_major ? g.out + (static_cast<size_t>(m) * g.B + b) * g.N + nt * BN
-                        : g.out + (static_cast<size_t>(b) * g.M + m) * g.N + nt * BN;
-      if (ok) {
-        for (int c0 = 0; c0 < BN; c0 += 16) {
-          uint32_t r[16];
-          tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + c0, r);
-          tmem_wait_ld();
-          const int n0 = nt * BN + c0;
-          if (m < g.M && n0 < g.N) {
-            __nv_bfloat16* dst = dst_row + c0;
-            if (n0 + 16 <= g.N && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
-              uint4 w0, w1;
-              w0.x = pack_bf16x2(__uint_as_float(r[0]), __uint_as_float(r[1]));
-              w0.y = pack_bf16x2(__uint_as_float(r[2]), __uint_as_float(r[3]));
-              w0.z = pack_bf16x2(__uint_as_float(r[4]), __uint_as_float(r[5]));
-              w0.w = pack_bf16x2(__uint_as_float(r[6]), __uint_as_float(r[7]));
-              w1.x = pack_bf16x2(__uint_as_float(r[8]), __uint_as_float(r[9]));
-              w1.y = pack_bf16x2(__uint_as_float(r[10]), __uint_as_float(r[11]));
-              w1.z = pack_bf16x2(__uint_as_float(r[12]), __uint_as_float(r[13]));
-              w1.w = pack_bf16x2(__uint_as_float(r[14]), __uint_as_float(r[15]));
-              reinterpret_cast<uint4*>(dst)[0] = w0;
-              reinterpret_cast<uint4*>(dst)[1] = w1;
+      const int mrow0 = mt * 128 + q * 32;
+      for (int c0 = 0; c0 < BN; c0 += 64) {
+        uint32_t r[64];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + c0 + 16 * j,
+                    *reinterpret_cast<uint32_t(*)[16]>(&r[16 * j]));
+        tmem_wait_ld();
+        if (c0 + 64 >= BN) {
+          tc_fence_before();
+          mbar_arrive(&acc_empty[buf]);          // accumulator fully read
+        }
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          uint4 w;
+          w.x = ok ? pack_bf16x2(__uint_as_float(r[8 * ch]), __uint_as_float(r[8 * ch + 1])) : 0u;
+          w.y = ok ? pack_bf16x2(__uint_as_float(r[8 * ch + 2]), __uint_as_float(r[8 * ch + 3])) : 0u;
+          w.z = ok ? pack_bf16x2(__uint_as_float(r[8 * ch + 4]), __uint_as_float(r[8 * ch + 5])) : 0u;
+          w.w = ok ? pack_bf16x2(__uint_as_float(r[8 * ch + 6]), __uint_as_float(r[8 * ch + 7])) : 0u;
+          *reinterpret_cast<uint4*>(stg + lane * 128 + ((ch ^ (lane & 7)) << 4)) = w;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int pss = 0; pss < 8; ++pss) {
+          const int rr = pss * 4 + (lane >> 3), ch = lane & 7;
+          const int m = mrow0 + rr;
+          const int n = nt * BN + c0 + ch * 8;
+          const uint4 w = *reinterpret_cast<const uint4*>(stg + rr * 128 + ((ch ^ (rr & 7)) << 4));
+          if (m < g.M && n < g.N) {
+            __nv_bfloat16* dst = row_ptr(m) + n;
+            if (g.vec_out && n + 8 <= g.N) {
+              *reinterpret_cast<uint4*>(dst) = w;
             } else {
-              for (int e = 0; e < 16; ++e)
-                if (n0 + e < g.N) dst[e] = __float2bfloat16_rn(__uint_as_float(r[e]));
+              const uint32_t h[4] = {w.x, w.y, w.z, w.w};
+              for (int e = 0; e < 8 && n + e < g.N; ++e)
+                reinterpret_cast<uint16_t*>(dst)[e] = static_cast<uint16_t>(h[e >> 1] >> (16 * (e & 1)));
             }
           }
         }
+        __syncwarp();
       }
-      tc_fence_before();
-      mbar_arrive(&acc_empty[buf]);
     }
   }
   __syncthreads();
@@ -280,6 +302,7 @@ cudaError_t launch_bmm(const void* x, const uint8_t* w_packed, void* out, int B,
   a.m_per_cta = static_cast<int>(ceil_div(a.m_tiles, m_groups));
   m_groups = static_cast<int>(ceil_div(a.m_tiles, a.m_per_cta));
   a.batch_major = batch_major;
+  a.vec_out = (reinterpret_cast<uintptr_t>(out) & 15) == 0 && (N % 8) == 0;
 
   CUtensorMap map;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(B)};
@@ -291,7 +314,7 @@ cudaError_t launch_bmm(const void* x, const uint8_t* w_packed, void* out, int B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
 
-  const int smem = a.KS * BN * 128 + kBmmStages * kSlabBytes + 1024 + 256;
+  const int smem = a.KS * BN * 128 + kBmmStages * kSlabBytes + 4 * kStageOutBytes + 1024 + 256;
   if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
   if (!g_bmm_attr[dev.device]) {
     cudaError_t e = cudaFuncSetAttribute(a16wfp4_bmm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
