@@ -98,3 +98,77 @@ def test_page_aiter_permutation_is_bijection(rows, cols):
     back = (p.reshape(rows // 32, cols // 8, 4, 16, 2, 2, 1)
             .transpose(0, 5, 3, 1, 4, 2, 6).reshape(rows, cols))
     assert np.array_equal(back, a)
+
+
+# ------------------------------------------------------------ weight layout
+@pytest.mark.parametrize("R,K", [(1, 32), (256, 256), (300, 544), (1000, 5152), (130, 5120)])
+def test_weight_offsets_partition_the_buffer(R, K):
+    co = tl.weight_code_offsets(R, K).ravel()
+    so = tl.weight_scale_offsets(R, K).ravel()
+    both = np.concatenate([co, so])
+    assert np.array_equal(np.sort(both), np.arange(tl.weight_packed_bytes(R, K)))
+    Np, Kp = tl.weight_padded_dims(R, K)
+    assert tl.weight_packed_bytes(R, K) == Np * Kp // 2 + Np * Kp // 32
+
+
+def expected_weight_pack_by_blocks(codes, scales, K):
+    """Independent restatement: per (row pair, k-tile) concatenate the two
+    address-bit-swizzled code tiles and the four scale atoms."""
+    R = codes.shape[0]
+    Np, Kp = tl.weight_padded_dims(R, K)
+    KT = Kp // 256
+    cpad = np.zeros((Np, Kp // 2), np.uint8)
+    cpad[:R, :codes.shape[1]] = codes
+    spad = np.full((Np, Kp // 32), 0x7F, np.uint8)
+    spad[:R, :scales.shape[1]] = scales
+    out = []
+    for p in range(Np // 256):
+        for kt in range(KT):
+            for h in range(2):
+                r0 = p * 256 + h * 128
+                tile = cpad[r0:r0 + 128, kt * 128:(kt + 1) * 128].ravel()
+                sw = np.empty_like(tile)
+                for o in range(16384):
+                    sw[o ^ (((o >> 7) & 7) << 4)] = tile[o]
+                out.append(sw)
+            for h in range(2):
+                r0 = p * 256 + h * 128
+                for gq in range(2):
+                    atom = np.empty((32, 4, 4), np.uint8)
+                    for i in range(128):
+                        for b in range(4):
+                            atom[i % 32, i // 32, b] = spad[r0 + i, kt * 8 + gq * 4 + b]
+                    out.append(atom.ravel())
+    return np.concatenate(out)
+
+
+@pytest.mark.parametrize("R,K", [(3, 64), (260, 544)])
+def test_weight_pack_matches_block_restatement(R, K):
+    g = np.random.default_rng(R * 3 + K)
+    codes = g.integers(0, 256, size=(R, K // 2), dtype=np.uint8)
+    scales = g.integers(0, 256, size=(R, -(-K // 32)), dtype=np.uint8)
+    assert np.array_equal(tl.pack_weights(codes, scales, K), expected_weight_pack_by_blocks(codes, scales, K))
+
+
+@pytest.mark.parametrize("R,K", [(1, 32), (17, 5152), (1000, 5152), (256, 5120)])
+def test_weight_unpack_inverts_pack_and_padding_values(R, K):
+    g = np.random.default_rng(R * 11 + K)
+    codes = g.integers(0, 256, size=(R, K // 2), dtype=np.uint8)
+    scales = g.integers(0, 255, size=(R, -(-K // 32)), dtype=np.uint8)
+    packed = tl.pack_weights(codes, scales, K)
+    c, s = tl.unpack_weights(packed, R, K)
+    assert np.array_equal(c[:R, :K // 2], codes)
+    assert np.array_equal(s[:R, :scales.shape[1]], scales)
+    assert np.all(c[R:] == 0) and np.all(c[:, K // 2:] == 0)
+    assert np.all(s[R:] == 0x7F) and np.all(s[:, scales.shape[1]:] == 0x7F)
+
+
+def test_weight_block_holds_whole_tiles_and_atoms():
+    """Rows 0..255 of k-tile 0 fill bytes [0, 34816) of the buffer: both code
+    tiles first, the four scale atoms after them."""
+    R, K = 512, 512
+    co = tl.weight_code_offsets(R, K)
+    so = tl.weight_scale_offsets(R, K)
+    assert co[:256, :128].min() == 0 and co[:256, :128].max() == 32767
+    assert so[:256, :8].min() == 32768 and so[:256, :8].max() == 34815
+    assert co[256:, :128].min() == 2 * 34816          # pair 1 starts after pair 0's two k-tiles
