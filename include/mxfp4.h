@@ -26,6 +26,14 @@
  *   Padding codes are 0 and padding scales 0x7F (E8M0 1.0; the pages pad
  *   with 1.0 because 0xFF is NaN).
  *
+ * Packed WEIGHTS use the same tiles and atoms grouped by pairs of row tiles
+ * (one bulk copy feeds one MMA stage): rows padded to Np = ceil(N/256)*256;
+ * for each pair p (rows 256p..256p+255) and k-tile kt, one 34816-byte block at
+ * (p*Kp/256 + kt)*34816 = [code tile of rows 256p.. | code tile of rows
+ * 256p+128.. | atoms (block groups 0, 1) of the first 128 rows | atoms of the
+ * second 128 rows], 16384 + 16384 + 1024 + 1024 bytes.  A batch of weight
+ * matrices is stored back to back.
+ *
  * Conventions.
  *   - Pointers named *_dev are device pointers; the caller owns all memory.
  *     Except for the workspace the caller passes, the library allocates
@@ -84,13 +92,13 @@ MXFP4_API const char* mxfp4_status_string(mxfp4_status status);
 
 /*
  * Bytes of the packed weight buffer for `batch` matrices of N rows x K
- * elements: batch * (Np*Kp/2 + Np*Kp/32).  Returns 0 when an argument is
- * not positive or K is odd.
+ * elements: batch * (Np*Kp/2 + Np*Kp/32) with Np = ceil(N/256)*256.  Returns
+ * 0 when an argument is not positive or K is odd.
  */
 MXFP4_API size_t mxfp4_packed_weight_bytes(int batch, int N, int K);
 
 /*
- * One-time repack of FP4 weights into the TILED layout — the counterpart of
+ * One-time repack of FP4 weights into the packed weight layout — the counterpart of
  * the pages' process_weights_after_loading step, which swizzles the E8M0
  * weight scales into AITER's tile order and preshuffles the FP4 weights
  * (PR #39598 blog analysis, section 2: _swizzle_asm_fp4_scale,

@@ -38,7 +38,7 @@ struct BmmArgs {
   __nv_bfloat16* out;
   int B, M, N, K, KS;        // KS = K / 64 slabs
   int BN, n_tiles, m_tiles, m_per_cta;
-  size_t w_batch_bytes, w_code_bytes;
+  size_t w_batch_bytes;      // packed weight bytes of one batch
   int KT;                    // Kp / 256 of the packed weights
   bool batch_major;
   bool vec_out;              // out 16-byte aligned and N % 8 == 0: 16-byte output stores
@@ -107,15 +107,14 @@ __global__ void __launch_bounds__(192, 1) a16wfp4_bmm_kernel(const __grid_consta
 
   // ---- dequantize this CTA's weight tile into the swizzled bf16 image
   {
-    const uint8_t* wc = g.w_packed + static_cast<size_t>(b) * g.w_batch_bytes;
-    const uint8_t* ws = wc + g.w_code_bytes;
+    const uint8_t* wb = g.w_packed + static_cast<size_t>(b) * g.w_batch_bytes;
     const int nblk = g.K >> 5;
     const int items = BN * nblk;
     for (int it = threadIdx.x; it < items; it += blockDim.x) {
       const int nl = it / nblk, blk = it - nl * nblk;
       const int n = nt * BN + nl;
-      const uint4 c = *reinterpret_cast<const uint4*>(wc + tiled_code_offset(n, blk * 16, g.KT));
-      const float sc = e8m0_to_float(ws[tiled_scale_offset(n, blk, g.KT)]);
+      const uint4 c = *reinterpret_cast<const uint4*>(wb + weight_code_offset(n, blk * 16, g.KT));
+      const float sc = e8m0_to_float(wb[weight_scale_offset(n, blk, g.KT)]);
       const uint32_t w32[4] = {c.x, c.y, c.z, c.w};
       uint32_t o[16];
 #pragma unroll
@@ -285,10 +284,9 @@ cudaError_t launch_bmm(const void* x, const uint8_t* w_packed, void* out, int B,
   a.N = N;
   a.K = K;
   a.KS = K / 64;
-  const int64_t Np = padded_rows(N), Kp = padded_k(K);
+  const int64_t Np = weight_rows(N), Kp = padded_k(K);
   a.KT = static_cast<int>(Kp / kKTile);
-  a.w_code_bytes = static_cast<size_t>(Np * Kp / 2);
-  a.w_batch_bytes = a.w_code_bytes + static_cast<size_t>(Np * Kp / 32);
+  a.w_batch_bytes = static_cast<size_t>(weight_packed_bytes(N, K));
   // widest weight tile whose bf16 image fits in 128 KiB (and divides Np)
   int BN = 256;
   while (BN > 64 && (static_cast<int64_t>(BN) * K * 2 > 128 * 1024 || Np % BN != 0)) BN /= 2;

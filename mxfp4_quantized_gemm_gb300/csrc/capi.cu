@@ -92,8 +92,7 @@ const char* mxfp4_status_string(mxfp4_status s) {
 
 size_t mxfp4_packed_weight_bytes(int batch, int N, int K) {
   if (batch <= 0 || N <= 0 || K <= 0 || (K & 1)) return 0;
-  return static_cast<size_t>(batch) *
-         static_cast<size_t>(tiled_code_bytes(N, K) + tiled_scale_bytes(N, K));
+  return static_cast<size_t>(batch) * static_cast<size_t>(weight_packed_bytes(N, K));
 }
 
 size_t mxfp4_act_code_bytes(int M, int K, mxfp4_layout layout) {
@@ -119,7 +118,7 @@ mxfp4_status mxfp4_pack_weights(const uint8_t* w_codes, const uint8_t* w_scales,
   DeviceInfo dev;
   mxfp4_status st = device_ready(&dev);
   if (st != MXFP4_OK) return st;
-  return from_cuda(launch_pack(w_codes, w_scales, batch, N, K, static_cast<uint8_t*>(packed), dev,
+  return from_cuda(launch_pack_weights(w_codes, w_scales, batch, N, K, static_cast<uint8_t*>(packed), dev,
                                static_cast<cudaStream_t>(stream)));
 }
 

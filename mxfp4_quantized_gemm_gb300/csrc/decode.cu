@@ -65,11 +65,9 @@ struct DecodeArgs {
   int mode;                // kPrequantized or kQuantGlobal
   uint8_t* a_codes;        // TILED activation codes (read; written first in mode kQuantGlobal)
   uint8_t* a_scales;       // TILED activation scales
-  const uint8_t* w_codes;
-  const uint8_t* w_scales;
+  const uint8_t* w_packed;         // packed weight blocks
   OutView o;
   int M, K, KT;
-  int w_tiles;             // Np / 128: 128-row tiles of the packed weights
   int n_tiles;             // ceil(N / 256)
   int total;               // n_tiles x KT iterations
   int grid;
@@ -173,15 +171,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     const uint64_t evict_first = policy_evict_first();
     auto w_load = [&](int it, uint8_t* st, uint64_t* bar) {
       const int t = it / KT, kt = it - t * KT;
-      for (int q = 0; q < 2; ++q) {
-        const int rt = 2 * t + q;
-        if (rt < g.w_tiles) {
-          bulk_g2s_hint(st + q * kTileBytes, g.w_codes + (static_cast<size_t>(rt * KT + kt) << 14), kTileBytes, bar,
-                        evict_first);
-          bulk_g2s_hint(st + C::kW + C::kA + C::kSA + q * 1024,
-                        g.w_scales + (static_cast<size_t>(rt * KT + kt) << 10), 1024, bar, evict_first);
-        }
-      }
+      bulk_g2s_hint(st, g.w_packed + static_cast<size_t>(t * KT + kt) * kWeightBlockBytes, kWeightBlockBytes, bar,
+                    evict_first);
     };
     // Pre-quantized activations (TILED, rows 0..kRowsA-1 of row tile 0).
     auto a_load = [&](int it, uint8_t* st, uint64_t* bar) {
@@ -189,11 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       bulk_g2s(st + C::kW, g.a_codes + (static_cast<size_t>(kt) << 14), C::kALoad, bar);
       bulk_g2s(st + C::kW + C::kA, g.a_scales + (static_cast<size_t>(kt) << 10), 1024, bar);
     };
-    auto stage_bytes = [&](int it) -> uint32_t {
-      const int t = it / KT;
-      const int nsub = (2 * t + 1 < g.w_tiles) ? 2 : 1;
-      return static_cast<uint32_t>(C::kALoad + C::kSA + nsub * (kTileBytes + 1024));
-    };
+    auto stage_bytes = [&](int) -> uint32_t { return static_cast<uint32_t>(C::kW + C::kALoad + C::kSA); };
     const int npre = n_iter < C::kStages ? n_iter : C::kStages;
     // Lane i requests the weights of prologue stage i at once: the packed
     // weights are never written by the kernel this one follows (the repack
@@ -478,15 +465,13 @@ static cudaError_t launch_rows(const DecodeArgs& a, const DeviceInfo& dev, cudaS
 
 cudaError_t launch_decode(const DecodeProblem& p, const DeviceInfo& dev, cudaStream_t s) {
   DecodeArgs a{};
-  const int64_t Np = padded_rows(p.N);
   const int64_t Kp = padded_k(p.K);
   a.x = static_cast<const uint16_t*>(p.x);
   a.ldx = p.ldx;
   a.vec_ok = p.x != nullptr && (reinterpret_cast<uintptr_t>(p.x) & 15) == 0 && (p.ldx % 8) == 0;
   a.a_codes = const_cast<uint8_t*>(p.a_codes);
   a.a_scales = const_cast<uint8_t*>(p.a_scales);
-  a.w_codes = p.w_packed;
-  a.w_scales = p.w_packed + Np * Kp / 2;
+  a.w_packed = p.w_packed;
   a.o.out = static_cast<__nv_bfloat16*>(p.out);
   a.o.bias = static_cast<const __nv_bfloat16*>(p.bias);
   a.o.ldo = p.ldo;
@@ -494,7 +479,6 @@ cudaError_t launch_decode(const DecodeProblem& p, const DeviceInfo& dev, cudaStr
   a.M = p.M;
   a.K = p.K;
   a.KT = static_cast<int>(Kp / kKTile);
-  a.w_tiles = static_cast<int>(Np / 128);
   a.n_tiles = static_cast<int>(ceil_div(p.N, kTileN));
   a.total = a.n_tiles * a.KT;
   // With fewer 256-row tiles than SMs, split every tile into the same number

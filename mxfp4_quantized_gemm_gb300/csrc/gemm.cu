@@ -40,11 +40,9 @@ static __device__ uint32_t g_gemm_error;
 struct GemmArgs {
   const uint8_t* a_codes;
   const uint8_t* a_scales;
-  const uint8_t* w_codes;
-  const uint8_t* w_scales;
+  const uint8_t* w_packed;         // packed weight blocks
   OutView o;
   int M, KT;
-  int w_tiles;                     // Np / 128: 128-row tiles of the packed weights
   int n_tiles;                     // ceil(N / 256)
   int total;                       // output tiles x KT
   int grid;
@@ -100,14 +98,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const GemmArgs g) {
     auto w_load = [&](int it, uint8_t* st, uint64_t* bar) {
       const int t = it / KT, kt = it - t * KT;
       const int nt = t % g.n_tiles;
-      for (int q = 0; q < 2; ++q) {
-        const int rt = 2 * nt + q;
-        if (rt < g.w_tiles) {
-          bulk_g2s(st + q * kTileBytes, g.w_codes + (static_cast<size_t>(rt * KT + kt) << 14), kTileBytes, bar);
-          bulk_g2s(st + C::kW + C::kA + C::kSA + q * 1024, g.w_scales + (static_cast<size_t>(rt * KT + kt) << 10),
-                   1024, bar);
-        }
-      }
+      bulk_g2s(st, g.w_packed + static_cast<size_t>(nt * KT + kt) * kWeightBlockBytes, kWeightBlockBytes, bar);
     };
     auto a_load = [&](int it, uint8_t* st, uint64_t* bar) {
       const int t = it / KT, kt = it - t * KT;
@@ -115,11 +106,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const GemmArgs g) {
       bulk_g2s(st + C::kW, g.a_codes + (static_cast<size_t>(mt * KT + kt) << 14), C::kALoad, bar);
       bulk_g2s(st + C::kW + C::kA, g.a_scales + (static_cast<size_t>(mt * KT + kt) << 10), 1024, bar);
     };
-    auto stage_bytes = [&](int it) -> uint32_t {
-      const int nt = (it / KT) % g.n_tiles;
-      const int nsub = (2 * nt + 1 < g.w_tiles) ? 2 : 1;
-      return static_cast<uint32_t>(C::kALoad + C::kSA + nsub * (kTileBytes + 1024));
-    };
+    auto stage_bytes = [&](int) -> uint32_t { return static_cast<uint32_t>(C::kW + C::kALoad + C::kSA); };
     const int n_iter = it1 - it0;
     const int npre = n_iter < C::kStages ? n_iter : C::kStages;
     // Lane i issues prologue stage i (one copy instruction per lane rather
@@ -310,19 +297,16 @@ int gemm_grid(const DeviceInfo& dev) { return dev.sm_count < kMaxStreamKCtas ? d
 
 cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_t s) {
   GemmArgs a{};
-  const int64_t Np = padded_rows(p.N);
   const int64_t Kp = padded_k(p.K);
   a.a_codes = p.a_codes;
   a.a_scales = p.a_scales;
-  a.w_codes = p.w_packed;
-  a.w_scales = p.w_packed + Np * Kp / 2;
+  a.w_packed = p.w_packed;
   a.o.bias = static_cast<const __nv_bfloat16*>(p.bias);
   a.o.out = static_cast<__nv_bfloat16*>(p.out);
   a.o.ldo = p.ldo;
   a.o.N = p.N;
   a.M = p.M;
   a.KT = static_cast<int>(Kp / kKTile);
-  a.w_tiles = static_cast<int>(Np / 128);
   a.n_tiles = static_cast<int>(ceil_div(p.N, kTileN));
   const int64_t tiles = ceil_div(p.M, 128) * static_cast<int64_t>(a.n_tiles);
   a.total = static_cast<int>(tiles * a.KT);

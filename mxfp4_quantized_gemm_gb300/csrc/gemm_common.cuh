@@ -18,12 +18,13 @@ constexpr int kThreads = 320;        // producer warp, MMA warp, 8 epilogue warp
 constexpr int kEpiThreads = 256;
 constexpr int kMaxSmem = 232448;     // 227 KiB of dynamic shared memory per CTA
 
-// One pipeline stage = one 256-wide k-step of one output tile: 256 weight
-// rows of codes (two 16 KiB tiles), kRowsA activation rows of codes, two
-// activation scale atoms and 2 x 2 weight scale atoms.
+// One pipeline stage = one 256-wide k-step of one output tile: the packed
+// weight block of the tile's 256 rows (two 16 KiB code tiles, then 2 x 2
+// scale atoms: one bulk copy), kRowsA activation rows of codes and two
+// activation scale atoms.
 template <int kRowsA>
 struct Cfg {
-  static constexpr int kW = 2 * kTileBytes;       // 256 weight rows of codes
+  static constexpr int kW = kWeightBlockBytes;    // 256 weight rows: codes + scales
   // Only the first kRowsA activation rows are loaded and reserved per stage.
   // The M = 128 MMA reads 16 KiB from the activation offset; for kRowsA <
   // 128 the rows past kRowsA come from whatever follows (the rest of the
@@ -34,8 +35,7 @@ struct Cfg {
   static constexpr int kA = kALoad;
   static constexpr int kTailPad = kTileBytes - kALoad;
   static constexpr int kSA = 1024;                // 2 activation scale atoms
-  static constexpr int kSW = 2048;                // 2 x 2 weight scale atoms
-  static constexpr int kStageBytes = kW + kA + kSA + kSW;
+  static constexpr int kStageBytes = kW + kA + kSA;
   static constexpr int kStagesFit = (kMaxSmem - 1024 - 512 - kTailPad) / kStageBytes;
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   static constexpr int kRing = kStages * kStageBytes + kTailPad;
@@ -117,11 +117,12 @@ __device__ __forceinline__ void store_quad(const OutView& o, int m, int n, float
 // Issues the tcgen05.cp scale copies and the four K = 64 block-scaled MMAs
 // of one stage: accumulator [128 act rows x 256 weight rows] at `tmem`,
 // activation scales at TMEM column sfa (2 atoms), weight scales at sfb
-// (2 atoms x 2 row halves).  `accumulate` = 0 starts a new tile.
+// (2 atoms x 2 row halves; atom of half q, block group a at q * 1024 +
+// a * 512 after the codes).  `accumulate` = 0 starts a new tile.
 template <typename C>
 __device__ __forceinline__ void issue_stage_mma(uint32_t tmem, uint32_t stage_base, uint32_t accumulate) {
   const uint32_t sfa = tmem + C::kSfa, sfb = tmem + C::kSfb;
-  const uint32_t w_s = stage_base, a_s = stage_base + C::kW, sa_s = a_s + C::kA, sw_s = sa_s + C::kSA;
+  const uint32_t w_s = stage_base, sw_s = w_s + 2 * kTileBytes, a_s = stage_base + C::kW, sa_s = a_s + C::kA;
   tmem_cp_scales(sfa + 0, sdesc_scales(sa_s));
   tmem_cp_scales(sfa + 4, sdesc_scales(sa_s + 512));
 #pragma unroll

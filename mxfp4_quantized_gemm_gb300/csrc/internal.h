@@ -19,6 +19,15 @@ inline int64_t padded_k(int64_t K) { return ceil_div(K, kKTile) * kKTile; }
 inline int64_t tiled_code_bytes(int64_t R, int64_t K) { return padded_rows(R) * padded_k(K) / 2; }
 inline int64_t tiled_scale_bytes(int64_t R, int64_t K) { return padded_rows(R) * padded_k(K) / 32; }
 
+// Packed weights (see include/mxfp4.h): one block per (256-row pair, k-tile)
+// holding the pair's two code tiles and four scale atoms.
+constexpr int kPairRows = 256;
+constexpr int kWeightBlockBytes = 2 * kTileBytes + 4 * kAtomBytes;   // 34816
+inline int64_t weight_rows(int64_t R) { return ceil_div(R, kPairRows) * kPairRows; }
+inline int64_t weight_packed_bytes(int64_t R, int64_t K) {
+  return weight_rows(R) / kPairRows * (padded_k(K) / kKTile) * kWeightBlockBytes;
+}
+
 // Error bits recorded in a translation unit's device error word.
 constexpr uint32_t kErrTimeout = 1u;
 
@@ -55,8 +64,12 @@ cudaError_t current_device_info(DeviceInfo* out);
 // tiled_rows: rows of the tiled output to write (0 = all Rp rows).
 cudaError_t launch_quant(const void* x, int M, int K, int ldx, uint8_t* codes, uint8_t* scales, bool tiled,
                          int tiled_rows, const DeviceInfo& dev, cudaStream_t s);
+// Row-major codes/scales -> TILED activation layout (codes region, then scales).
 cudaError_t launch_pack(const uint8_t* codes, const uint8_t* scales, int batch, int R, int K, uint8_t* packed,
                         const DeviceInfo& dev, cudaStream_t s);
+// Row-major codes/scales -> packed weight blocks.
+cudaError_t launch_pack_weights(const uint8_t* codes, const uint8_t* scales, int batch, int N, int K,
+                                uint8_t* packed, const DeviceInfo& dev, cudaStream_t s);
 uint32_t quant_read_clear_error();
 
 // gemm.cu

@@ -1,4 +1,5 @@
-// Device-side offsets of the TILED layout (see include/mxfp4.h).
+// Device-side offsets of the TILED activation layout and of the packed
+// weight layout (see include/mxfp4.h).
 #pragma once
 
 #include <cstdint>
@@ -14,6 +15,21 @@ __device__ __forceinline__ size_t tiled_code_offset(int r, int j, int KT) {
 __device__ __forceinline__ size_t tiled_scale_offset(int r, int b, int KT) {
   const int rt = r >> 7, i = r & 127;
   return (static_cast<size_t>(rt * 2 * KT + (b >> 2)) << 9) + ((i & 31) << 4) + ((i >> 5) << 2) + (b & 3);
+}
+
+// Packed weights: blocks of 34816 bytes, one per (256-row pair p, k-tile kt)
+// at (p * KT + kt) * 34816, each [code tile of rows 0-127 | code tile of rows
+// 128-255 | 2 scale atoms of rows 0-127 | 2 scale atoms of rows 128-255].
+// Byte offset of code byte j (0 <= j < Kp/2) of row r:
+__device__ __forceinline__ size_t weight_code_offset(int r, int j, int KT) {
+  const int p = r >> 8, h = (r >> 7) & 1, i = r & 127, kt = j >> 7, jj = j & 127;
+  return static_cast<size_t>(p * KT + kt) * 34816 + (h << 14) + (i << 7) + (((jj >> 4) ^ (i & 7)) << 4) + (jj & 15);
+}
+// Byte offset of the scale of row r, block b (0 <= b < Kp/32):
+__device__ __forceinline__ size_t weight_scale_offset(int r, int b, int KT) {
+  const int p = r >> 8, h = (r >> 7) & 1, i = r & 127, kt = b >> 3, bb = b & 7;
+  return static_cast<size_t>(p * KT + kt) * 34816 + 32768 + (h << 10) + ((bb >> 2) << 9) + ((i & 31) << 4) +
+         ((i >> 5) << 2) + (bb & 3);
 }
 
 }  // namespace mx

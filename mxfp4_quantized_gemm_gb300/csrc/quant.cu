@@ -1,4 +1,4 @@
-// Per-1x32 MXFP4 activation quantization and the one-time tile repack.
+// Per-1x32 MXFP4 activation quantization and the one-time repacks.
 //
 // Quantization follows the OCP MX conversion the pages' per_1x32_f4_quant
 // implements (sglang PR #39598 blog analysis, section 2): one E8M0 scale per
@@ -139,6 +139,56 @@ __global__ void __launch_bounds__(256) pack_scales_kernel(const uint8_t* __restr
   }
 }
 
+// Repack row-major weight codes and scales into the packed weight blocks:
+// one thread per 16-byte output chunk, written in storage order.  A block is
+// 2176 chunks: 2048 of codes (two 128-row tiles, 1024 chunks each: row i,
+// physical chunk pc holds logical chunk pc ^ (i % 8)), then 128 of scales
+// (four 512-byte atoms; byte o of an atom is row (o / 16) + 32 ((o / 4) % 4),
+// block o % 4 of its group of four).
+__global__ void __launch_bounds__(256) pack_weights_kernel(const uint8_t* __restrict__ codes,
+                                                           const uint8_t* __restrict__ scales, int batch, int R,
+                                                           int K, uint8_t* __restrict__ packed, int KT,
+                                                           int64_t blocks_per_batch) {
+  const int row_bytes = K >> 1;
+  const int nb = (K + 31) >> 5;
+  constexpr int kChunksPerBlock = 2176;
+  const int64_t total = static_cast<int64_t>(batch) * blocks_per_batch * kChunksPerBlock;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t blk = t / kChunksPerBlock;
+    const int c = static_cast<int>(t - blk * kChunksPerBlock);
+    const int bi = static_cast<int>(blk / blocks_per_batch);
+    const int64_t pb = blk - static_cast<int64_t>(bi) * blocks_per_batch;
+    const int pair = static_cast<int>(pb / KT), kt = static_cast<int>(pb - static_cast<int64_t>(pair) * KT);
+    uint8_t v[16];
+    if (c < 2048) {
+      const int h = c >> 10, rem = c & 1023, i = rem >> 3, pc = rem & 7;
+      const int r = pair * 256 + h * 128 + i;
+      const int j = kt * 128 + ((pc ^ (i & 7)) << 4);
+      const uint8_t* src = codes + (static_cast<size_t>(bi) * R + r) * row_bytes + j;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) v[e] = (r < R && j + e < row_bytes) ? src[e] : static_cast<uint8_t>(0);
+    } else {
+      const int s0 = (c - 2048) * 16;            // byte offset in the 2 KiB scale part
+      const int h = s0 >> 10, gq = (s0 >> 9) & 1;
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int o = (s0 & 511) + e;
+        const int i = (o >> 4) + 32 * ((o >> 2) & 3);
+        const int r = pair * 256 + h * 128 + i;
+        const int b = kt * 8 + gq * 4 + (o & 3);
+        v[e] = (r < R && b < nb) ? scales[(static_cast<size_t>(bi) * R + r) * nb + b] : static_cast<uint8_t>(0x7F);
+      }
+    }
+    uint4 w;
+    w.x = v[0] | (v[1] << 8) | (v[2] << 16) | (static_cast<uint32_t>(v[3]) << 24);
+    w.y = v[4] | (v[5] << 8) | (v[6] << 16) | (static_cast<uint32_t>(v[7]) << 24);
+    w.z = v[8] | (v[9] << 8) | (v[10] << 16) | (static_cast<uint32_t>(v[11]) << 24);
+    w.w = v[12] | (v[13] << 8) | (v[14] << 16) | (static_cast<uint32_t>(v[15]) << 24);
+    *reinterpret_cast<uint4*>(packed + static_cast<size_t>(blk) * 34816 + static_cast<size_t>(c) * 16) = w;
+  }
+}
+
 static int grid_for(int64_t work_items, int per_block, const DeviceInfo& dev) {
   int64_t blocks = (work_items + per_block - 1) / per_block;
   const int64_t cap = static_cast<int64_t>(dev.sm_count) * 16;
@@ -205,6 +255,18 @@ cudaError_t launch_pack(const uint8_t* codes, const uint8_t* scales, int batch, 
   pack_scales_kernel<<<grid_for(sb * batch, 256, dev), 256, 0, s>>>(scales, batch, R, K, packed, per_batch,
                                                                     static_cast<size_t>(cb), KT, sb);
   e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ordering_kernel<<<1, 32, 0, s>>>();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_weights(const uint8_t* codes, const uint8_t* scales, int batch, int N, int K,
+                                uint8_t* packed, const DeviceInfo& dev, cudaStream_t s) {
+  const int KT = static_cast<int>(padded_k(K) / kKTile);
+  const int64_t blocks = weight_rows(N) / kPairRows * KT;
+  pack_weights_kernel<<<grid_for(blocks * batch * 2176, 256, dev), 256, 0, s>>>(codes, scales, batch, N, K, packed, KT,
+                                                                                blocks);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ordering_kernel<<<1, 32, 0, s>>>();
   return cudaGetLastError();

@@ -47,7 +47,7 @@ def test_abi_version_and_status_strings(capi):
 @pytest.mark.parametrize("B,N,K", [(1, 1024, 5120), (1, 1000, 5152), (64, 512, 192), (3, 5, 40)])
 def test_packed_size_matches_layout_statement(capi, B, N, K):
     from oracle import tile_layout as tl
-    assert capi.mxfp4_packed_weight_bytes(B, N, K) == B * tl.packed_bytes(N, K)
+    assert capi.mxfp4_packed_weight_bytes(B, N, K) == B * tl.weight_packed_bytes(N, K)
 
 
 def test_size_queries(capi):

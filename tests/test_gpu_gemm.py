@@ -130,8 +130,7 @@ def test_padding_scales_never_change_results(capi, M):
     x, wc, ws, b = make_problem(M, N, K, seed=5)
     packed = pack_weights(capi, wc, ws, K)
     base = run_gemm(capi, x, packed, b, M, N, K)
-    cb = tl.code_bytes(N, K)
-    offs = cb + tl.scale_offsets(N, K)
+    offs = tl.weight_scale_offsets(N, K)
     pad = np.ones(offs.shape, bool)
     pad[:N, : -(-K // 32)] = False
     g = np.random.default_rng(0)

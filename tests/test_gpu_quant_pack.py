@@ -102,4 +102,4 @@ def test_pack_bit_exact(capi, B, N, K):
     scales = synth.weight_scales(N, K, -8, 2, seed=N, batch=B)
     packed = pack_weights(capi, codes, scales, K)
     torch.cuda.synchronize()
-    assert np.array_equal(packed.cpu().numpy(), tl.pack_batched(codes, scales, K))
+    assert np.array_equal(packed.cpu().numpy(), tl.pack_weights_batched(codes, scales, K))
