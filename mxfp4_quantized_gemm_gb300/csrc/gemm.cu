@@ -50,11 +50,11 @@ struct GemmArgs {
   float* partials;                 // 2 slots per CTA, rows_a x 256 floats each
 };
 
-// At most 96 registers per thread (the bound asks for two CTAs' worth; the
-// shared-memory ring still allows one CTA per SM): the fix-up blocks of the
-// previous call then fit on the SM beside it.
+// One CTA per SM (the ring takes the shared memory), so the full register
+// budget of a 320-thread block is available: the epilogue holds a whole
+// 128-column accumulator row in registers.
 template <int kRowsA>
-__global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const GemmArgs g) {
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs g) {
   using C = Cfg<kRowsA>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
@@ -174,40 +174,38 @@ __global__ void __launch_bounds__(kThreads, 2) gemm_kernel(const GemmArgs g) {
       const bool live = warp_live && rl < kRowsA && m < g.M;
       const bool whole = kt == 0 && len == KT;
       const int slot = 2 * cta + (it == it0 ? 0 : 1);
-      // Two passes of 64 columns; the accumulator is released right after the
-      // second pass is loaded.  A whole tile is stored; a part of a tile is
-      // published as fp32 for the fix-up kernel that follows.
+      // All 128 columns of this thread's row are read into registers and the
+      // accumulator is released before anything is stored, so the next
+      // segment's MMAs do not wait on the stores.  A whole tile is stored
+      // (+ bias, bf16); a part of a tile is published as fp32 for the fix-up
+      // kernel that follows.
+      uint32_t r[128];
+      if (warp_live) {
 #pragma unroll
-      for (int pass = 0; pass < 2; ++pass) {
-        float v[64];
-        if (warp_live) {
-          uint32_t r[64];
+        for (int c0 = 0; c0 < 128; c0 += 16)
+          tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128 + c0,
+                    *reinterpret_cast<uint32_t(*)[16]>(&r[c0]));
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      mbar_arrive(acc_empty);                     // accumulator free for the next segment
+      if (live) {
+        if (!ok) {
 #pragma unroll
-          for (int c0 = 0; c0 < 64; c0 += 16)
-            tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128 + pass * 64 + c0,
-                      *reinterpret_cast<uint32_t(*)[16]>(&r[c0]));
-          tmem_wait_ld();
-#pragma unroll
-          for (int c = 0; c < 64; ++c) v[c] = ok ? __uint_as_float(r[c]) : 0.f;
+          for (int c = 0; c < 128; ++c) r[c] = 0u;
         }
-        if (pass == 1) {
-          tc_fence_before();
-          mbar_arrive(acc_empty);                 // accumulator free for the next segment
-        }
-        if (!live) continue;
         if (whole) {
 #pragma unroll
-          for (int c0 = 0; c0 < 64; c0 += 32) {
+          for (int c0 = 0; c0 < 128; c0 += 32) {
             float chunk[32];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) chunk[c] = v[c0 + c];
-            store_chunk(g.o, m, n0 + pass * 64 + c0, chunk);
+            for (int c = 0; c < 32; ++c) chunk[c] = __uint_as_float(r[c0 + c]);
+            store_chunk(g.o, m, n0 + c0, chunk);
           }
         } else {
-          float4* P = reinterpret_cast<float4*>(g.partials + (static_cast<size_t>(slot) * kRowsA + rl) * kTileN +
-                                                h * 128 + pass * 64);
+          uint4* P = reinterpret_cast<uint4*>(g.partials + (static_cast<size_t>(slot) * kRowsA + rl) * kTileN + h * 128);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) __stcg(P + c, make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]));
+          for (int c = 0; c < 32; ++c) __stcg(P + c, make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]));
         }
       }
       it += len;
