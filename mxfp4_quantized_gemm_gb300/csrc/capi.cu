@@ -133,7 +133,7 @@ mxfp4_status mxfp4_quant_act(const void* x, int M, int K, int ldx, uint8_t* code
   DeviceInfo dev;
   mxfp4_status st = device_ready(&dev);
   if (st != MXFP4_OK) return st;
-  return from_cuda(launch_quant(x, M, K, ldx, codes, scales, layout == MXFP4_LAYOUT_TILED, 0, dev,
+  return from_cuda(launch_quant(x, M, K, ldx, codes, scales, layout == MXFP4_LAYOUT_TILED ? ActLayout::kTiled : ActLayout::kRowMajor, 0, dev,
                                 static_cast<cudaStream_t>(stream)));
 }
 
@@ -207,9 +207,11 @@ mxfp4_status mxfp4_gemm(const void* a_bf16, int lda, const uint8_t* a_codes, con
 
   GemmProblem p{};
   if (from_bf16) {
+    // quantized into the workspace in the blocked form (one copy per stage)
     p.a_codes = ws + wl.codes_off;
-    p.a_scales = ws + wl.scales_off;
-    cudaError_t e = launch_quant(a_bf16, M, K, lda, ws + wl.codes_off, ws + wl.scales_off, true, 0, dev, s);
+    p.a_scales = nullptr;
+    p.a_blocked = true;
+    cudaError_t e = launch_quant(a_bf16, M, K, lda, ws + wl.codes_off, nullptr, ActLayout::kBlocked, kRowTile, dev, s);
     if (e != cudaSuccess) return MXFP4_ERR_CUDA;
   } else if (a_layout == MXFP4_LAYOUT_ROWMAJOR) {
     // the pages' pre-quantized (x_fp4, x_scales) input: re-lay out, pad scales with 0x7F

@@ -24,7 +24,7 @@
 //    soon as it has an SM, usually while the previous call is still running
 //    (the packed weights are never written by the kernel this one follows);
 //  * the activations are quantized inside the kernel: every CTA quantizes a
-//    share of the (k-step, 8-row) units into the TILED workspace image and
+//    share of the (k-step, 8-row) units into the workspace (blocked form) and
 //    publishes a flag per unit, and producers copy a k-step in once its
 //    units are flagged;
 //  * tiles cut by CTA boundaries are summed inside the kernel: every part is
@@ -63,8 +63,9 @@ struct DecodeArgs {
   int ldx;
   int vec_ok;              // x and ldx allow 16-byte row loads
   int mode;                // kPrequantized or kQuantGlobal
-  uint8_t* a_codes;        // TILED activation codes (read; written first in mode kQuantGlobal)
-  uint8_t* a_scales;       // TILED activation scales
+  uint8_t* a_codes;        // TILED codes, or blocked activations (a_blocked; kRowsA-row blocks)
+  uint8_t* a_scales;       // TILED activation scales (unused when a_blocked)
+  int a_blocked;           // set when the kernel or the quantizer wrote the blocked form
   const uint8_t* w_packed;         // packed weight blocks
   OutView o;
   int M, K, KT;
@@ -95,7 +96,7 @@ __device__ __forceinline__ uint4 load8_packed(const uint16_t* __restrict__ x, in
 // Where the activation codes of a stage come from.
 //  kPrequantized: the caller's TILED codes/scales, copied in by the producer.
 //  kQuantGlobal:  every CTA first quantizes a share of the (k-step, 8-row)
-//                 units into the TILED workspace image and publishes a flag
+//                 units into the workspace (blocked form) and publishes a flag
 //                 per unit; producers wait for the flags of their k-steps and
 //                 copy the codes in.  x is read once in all.
 // (Quantizing inside each CTA from its own copy of x was measured slower at
@@ -174,11 +175,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       bulk_g2s_hint(st, g.w_packed + static_cast<size_t>(t * KT + kt) * kWeightBlockBytes, kWeightBlockBytes, bar,
                     evict_first);
     };
-    // Pre-quantized activations (TILED, rows 0..kRowsA-1 of row tile 0).
+    // Activations of the stage's k-step (rows 0..kRowsA-1 of row tile 0):
+    // one copy of the blocked form, or codes + scales of the TILED form.
     auto a_load = [&](int it, uint8_t* st, uint64_t* bar) {
       const int kt = it % KT;
-      bulk_g2s(st + C::kW, g.a_codes + (static_cast<size_t>(kt) << 14), C::kALoad, bar);
-      bulk_g2s(st + C::kW + C::kA, g.a_scales + (static_cast<size_t>(kt) << 10), 1024, bar);
+      if (g.a_blocked) {
+        bulk_g2s(st + C::kW, g.a_codes + static_cast<size_t>(kt) * (C::kALoad + C::kSA), C::kALoad + C::kSA, bar);
+      } else {
+        bulk_g2s(st + C::kW, g.a_codes + (static_cast<size_t>(kt) << 14), C::kALoad, bar);
+        bulk_g2s(st + C::kW + C::kA, g.a_scales + (static_cast<size_t>(kt) << 10), 1024, bar);
+      }
     };
     auto stage_bytes = [&](int) -> uint32_t { return static_cast<uint32_t>(C::kW + C::kALoad + C::kSA); };
     const int npre = n_iter < C::kStages ? n_iter : C::kStages;
@@ -257,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     if (g.mode == kQuantGlobal) {
       griddep_wait();
       epoch = ld_acquire_gpu(g.ctrl + kCtrlEpoch);
-      // Quantize this CTA's units into the TILED workspace image: unit
+      // Quantize this CTA's units into the workspace (blocked form): unit
       // u = rg * KT + kt is rows 8 rg .. 8 rg + 7 of k-step kt; warp 2 + w
       // takes row 8 rg + w, lane l elements 8 l .. 8 l + 7.  Up to four units
       // per pass have their loads in flight together.
@@ -283,9 +289,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           uint32_t sbyte;
           const uint32_t packed = quantize8(v, sbyte);
           const int blk = kt * 8 + (lane >> 2);
-          *reinterpret_cast<uint32_t*>(g.a_codes + tiled_code_offset(r, kt * 128 + lane * 4, KT)) = packed;
+          *reinterpret_cast<uint32_t*>(g.a_codes + blocked_code_offset(r, kt * 128 + lane * 4, KT, kRowsA)) = packed;
           if ((lane & 3) == 0)
-            g.a_scales[tiled_scale_offset(r, blk, KT)] = (r < g.M && blk < nb) ? static_cast<uint8_t>(sbyte) : 0x7F;
+            g.a_codes[blocked_scale_offset(r, blk, KT, kRowsA)] =
+                (r < g.M && blk < nb) ? static_cast<uint8_t>(sbyte) : 0x7F;
         }
         // The units are read by other CTAs' bulk copies (async proxy).
         fence_proxy_async_global();
@@ -502,13 +509,16 @@ cudaError_t launch_decode(const DecodeProblem& p, const DeviceInfo& dev, cudaStr
   // quantizer kernel first.
   const int rows = gemm_rows_a(p.M);
   if (p.x == nullptr) {
-    a.mode = kPrequantized;
+    a.mode = kPrequantized;            // the caller's TILED codes and scales
+    a.a_blocked = 0;
   } else if (a.KT <= kMaxUnitKT) {
-    a.mode = kQuantGlobal;
+    a.mode = kQuantGlobal;             // blocked form, written by this kernel
+    a.a_blocked = 1;
   } else {
-    cudaError_t e = launch_quant(p.x, p.M, p.K, p.ldx, a.a_codes, a.a_scales, true, rows, dev, s);
+    cudaError_t e = launch_quant(p.x, p.M, p.K, p.ldx, a.a_codes, nullptr, ActLayout::kBlocked, rows, dev, s);
     if (e != cudaSuccess) return e;
     a.mode = kPrequantized;
+    a.a_blocked = 1;
   }
   switch (rows) {
     case 16: return launch_rows<16>(a, dev, s, 0);

@@ -38,8 +38,9 @@ namespace mx {
 static __device__ uint32_t g_gemm_error;
 
 struct GemmArgs {
-  const uint8_t* a_codes;
+  const uint8_t* a_codes;          // TILED codes, or blocked activations (a_blocked)
   const uint8_t* a_scales;
+  int a_blocked;
   const uint8_t* w_packed;         // packed weight blocks
   OutView o;
   int M, KT;
@@ -103,8 +104,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs g) {
     auto a_load = [&](int it, uint8_t* st, uint64_t* bar) {
       const int t = it / KT, kt = it - t * KT;
       const int mt = t / g.n_tiles;
-      bulk_g2s(st + C::kW, g.a_codes + (static_cast<size_t>(mt * KT + kt) << 14), C::kALoad, bar);
-      bulk_g2s(st + C::kW + C::kA, g.a_scales + (static_cast<size_t>(mt * KT + kt) << 10), 1024, bar);
+      if (g.a_blocked) {
+        bulk_g2s(st + C::kW, g.a_codes + static_cast<size_t>(mt * KT + kt) * (C::kALoad + C::kSA), C::kALoad + C::kSA,
+                 bar);
+      } else {
+        bulk_g2s(st + C::kW, g.a_codes + (static_cast<size_t>(mt * KT + kt) << 14), C::kALoad, bar);
+        bulk_g2s(st + C::kW + C::kA, g.a_scales + (static_cast<size_t>(mt * KT + kt) << 10), 1024, bar);
+      }
     };
     auto stage_bytes = [&](int) -> uint32_t { return static_cast<uint32_t>(C::kW + C::kALoad + C::kSA); };
     const int n_iter = it1 - it0;
@@ -298,6 +304,7 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
   const int64_t Kp = padded_k(p.K);
   a.a_codes = p.a_codes;
   a.a_scales = p.a_scales;
+  a.a_blocked = p.a_blocked ? 1 : 0;
   a.w_packed = p.w_packed;
   a.o.bias = static_cast<const __nv_bfloat16*>(p.bias);
   a.o.out = static_cast<__nv_bfloat16*>(p.out);

@@ -61,9 +61,17 @@ struct DeviceInfo {
 cudaError_t current_device_info(DeviceInfo* out);
 
 // quant.cu
-// tiled_rows: rows of the tiled output to write (0 = all Rp rows).
-cudaError_t launch_quant(const void* x, int M, int K, int ldx, uint8_t* codes, uint8_t* scales, bool tiled,
-                         int tiled_rows, const DeviceInfo& dev, cudaStream_t s);
+// Output layout of the activation quantizer: row-major, TILED (public), or
+// blocked (the library's own workspace form: per (row tile, k-tile) the code
+// rows followed by the two scale atoms, one bulk copy per GEMM stage).
+enum class ActLayout { kRowMajor, kTiled, kBlocked };
+inline int64_t blocked_bytes(int64_t M, int64_t K, int block_rows) {
+  return ceil_div(M, kRowTile) * (padded_k(K) / kKTile) * (static_cast<int64_t>(block_rows) * 128 + 1024);
+}
+// rows: kTiled: rows of the tiled output to write (0 = all Rp rows);
+// kBlocked: rows per block (128 for any M; 16/32/64 when M <= that).
+cudaError_t launch_quant(const void* x, int M, int K, int ldx, uint8_t* codes, uint8_t* scales, ActLayout layout,
+                         int rows, const DeviceInfo& dev, cudaStream_t s);
 // Row-major codes/scales -> TILED activation layout (codes region, then scales).
 cudaError_t launch_pack(const uint8_t* codes, const uint8_t* scales, int batch, int R, int K, uint8_t* packed,
                         const DeviceInfo& dev, cudaStream_t s);
@@ -74,8 +82,9 @@ uint32_t quant_read_clear_error();
 
 // gemm.cu
 struct GemmProblem {
-  const uint8_t* a_codes;   // TILED activation codes
-  const uint8_t* a_scales;  // TILED activation scales
+  const uint8_t* a_codes;   // TILED activation codes, or the blocked activations (a_blocked)
+  const uint8_t* a_scales;  // TILED activation scales (unused when a_blocked)
+  bool a_blocked;           // a_codes holds blocked activations with 128-row blocks
   const uint8_t* w_packed;  // packed weights (codes region then scales region)
   const void* bias;         // bf16 [N] or null
   void* out;                // bf16 [M][ldo]

@@ -17,6 +17,23 @@ __device__ __forceinline__ size_t tiled_scale_offset(int r, int b, int KT) {
   return (static_cast<size_t>(rt * 2 * KT + (b >> 2)) << 9) + ((i & 31) << 4) + ((i >> 5) << 2) + (b & 3);
 }
 
+// Activations the library quantizes into its own workspace ("blocked"):
+// per (128-row tile mt, k-tile kt) one block of rows * 128 + 1024 bytes at
+// (mt * KT + kt) * (rows * 128 + 1024), holding the first `rows` rows of the
+// code tile (same swizzle as TILED) followed by the tile's two scale atoms
+// (same atom layout; the atoms always take 1024 bytes).  One bulk copy then
+// brings a stage its activation codes and scales.  Requires r % 128 < rows.
+__device__ __forceinline__ size_t blocked_code_offset(int r, int j, int KT, int rows) {
+  const int mt = r >> 7, i = r & 127, kt = j >> 7, jj = j & 127;
+  return static_cast<size_t>(mt * KT + kt) * (rows * 128 + 1024) + (i << 7) + (((jj >> 4) ^ (i & 7)) << 4) +
+         (jj & 15);
+}
+__device__ __forceinline__ size_t blocked_scale_offset(int r, int b, int KT, int rows) {
+  const int mt = r >> 7, i = r & 127, kt = b >> 3, bb = b & 7;
+  return static_cast<size_t>(mt * KT + kt) * (rows * 128 + 1024) + rows * 128 + ((bb >> 2) << 9) +
+         ((i & 31) << 4) + ((i >> 5) << 2) + (bb & 3);
+}
+
 // Packed weights: blocks of 34816 bytes, one per (256-row pair p, k-tile kt)
 // at (p * KT + kt) * 34816, each [code tile of rows 0-127 | code tile of rows
 // 128-255 | 2 scale atoms of rows 0-127 | 2 scale atoms of rows 128-255].

@@ -22,10 +22,12 @@ static __device__ uint32_t g_quant_error;
 // elements 8l..8l+7, four lanes form one 32-element block.
 // At most 64 registers per thread, so a quantizer block fits on an SM next
 // to a resident GEMM CTA.
-template <bool kTiled>
+// kLayout: ActLayout::kRowMajor, kTiled or kBlocked (block_rows rows per
+// block; the rows written are 0..rows-1).
+template <ActLayout kLayout>
 __global__ void __launch_bounds__(256, 4) quant_kernel(const uint16_t* __restrict__ x, int M, int K, int ldx,
                                                     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                                                    int rows, int KT, bool vec_ok) {
+                                                    int rows, int KT, bool vec_ok, int block_rows) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -61,10 +63,14 @@ __global__ void __launch_bounds__(256, 4) quant_kernel(const uint16_t* __restric
       const int blk = kt * 8 + (lane >> 2);
       const bool blk_real = r < M && blk < nb;
       const int j0 = kt * 128 + lane * 4;   // first code byte of this lane in the row
-      if (kTiled) {
+      if (kLayout == ActLayout::kTiled) {
         *reinterpret_cast<uint32_t*>(codes + tiled_code_offset(r, j0, KT)) = packed;
         if ((lane & 3) == 0)
           scales[tiled_scale_offset(r, blk, KT)] = blk_real ? static_cast<uint8_t>(sbyte) : 0x7F;
+      } else if (kLayout == ActLayout::kBlocked) {
+        *reinterpret_cast<uint32_t*>(codes + blocked_code_offset(r, j0, KT, block_rows)) = packed;
+        if ((lane & 3) == 0)
+          codes[blocked_scale_offset(r, blk, KT, block_rows)] = blk_real ? static_cast<uint8_t>(sbyte) : 0x7F;
       } else if (r < M) {
         const int row_bytes = K >> 1;
         uint8_t* dst = codes + static_cast<size_t>(r) * row_bytes + j0;
@@ -222,19 +228,28 @@ static int quant_grid(int64_t units, int M, const DeviceInfo& dev) {
   return static_cast<int>(blocks < 1 ? 1 : blocks);
 }
 
-cudaError_t launch_quant(const void* x, int M, int K, int ldx, uint8_t* codes, uint8_t* scales, bool tiled,
-                         int tiled_rows, const DeviceInfo& dev, cudaStream_t s) {
+cudaError_t launch_quant(const void* x, int M, int K, int ldx, uint8_t* codes, uint8_t* scales, ActLayout layout,
+                         int rows_arg, const DeviceInfo& dev, cudaStream_t s) {
   const bool vec_ok = (reinterpret_cast<uintptr_t>(x) & 15) == 0 && (ldx % 8) == 0;
   const uint16_t* xs = static_cast<const uint16_t*>(x);
-  if (tiled) {
-    const int rows = tiled_rows > 0 ? tiled_rows : static_cast<int>(padded_rows(M));
-    const int KT = static_cast<int>(padded_k(K) / kKTile);
+  const int KT = static_cast<int>(padded_k(K) / kKTile);
+  if (layout == ActLayout::kTiled) {
+    const int rows = rows_arg > 0 ? rows_arg : static_cast<int>(padded_rows(M));
     const int grid = quant_grid(static_cast<int64_t>(rows) * KT, M, dev);
-    return launch_dependent(quant_kernel<true>, grid, s, xs, M, K, ldx, codes, scales, rows, KT, vec_ok);
+    return launch_dependent(quant_kernel<ActLayout::kTiled>, grid, s, xs, M, K, ldx, codes, scales, rows, KT, vec_ok,
+                            0);
   }
-  const int KT = static_cast<int>(ceil_div(K, kKTile));
-  const int grid = quant_grid(static_cast<int64_t>(M) * KT, M, dev);
-  return launch_dependent(quant_kernel<false>, grid, s, xs, M, K, ldx, codes, scales, M, KT, vec_ok);
+  if (layout == ActLayout::kBlocked) {
+    if (rows_arg <= 0 || rows_arg > kRowTile || (rows_arg < kRowTile && M > rows_arg)) return cudaErrorInvalidValue;
+    const int rows = rows_arg == kRowTile ? static_cast<int>(padded_rows(M)) : rows_arg;
+    const int grid = quant_grid(static_cast<int64_t>(rows) * KT, M, dev);
+    return launch_dependent(quant_kernel<ActLayout::kBlocked>, grid, s, xs, M, K, ldx, codes, scales, rows, KT,
+                            vec_ok, rows_arg);
+  }
+  const int KTr = static_cast<int>(ceil_div(K, kKTile));
+  const int grid = quant_grid(static_cast<int64_t>(M) * KTr, M, dev);
+  return launch_dependent(quant_kernel<ActLayout::kRowMajor>, grid, s, xs, M, K, ldx, codes, scales, M, KTr, vec_ok,
+                          0);
 }
 
 // Empty kernel launched (normally) after the repack: a programmatic
