@@ -138,17 +138,13 @@ MXFP4_API mxfp4_status mxfp4_quant_act(const void* x_dev, int M, int K, int ldx,
                              uint8_t* codes_dev, uint8_t* scales_dev,
                              mxfp4_layout layout, void* stream);
 
-/* Workspace bytes mxfp4_gemm needs for this problem (any input form). */
-MXFP4_API size_t mxfp4_gemm_workspace_bytes(int M, int N, int K);
-
 /*
- * Prepares a GEMM workspace for its first use: zeroes its control words
- * (the first 16 KiB), stream-ordered on `stream`.  Needed once per
- * workspace, before its first mxfp4_gemm call, unless the memory was
- * allocated zeroed; never needed again while it is used only by mxfp4_gemm.
- * Errors: INVALID_ARG, WORKSPACE (fewer than 16 KiB), MISALIGNED, CUDA.
+ * Workspace bytes mxfp4_gemm needs for this problem (any input form): room
+ * for the quantized or re-laid-out activations and, for M > 64, the fp32
+ * partial sums of output tiles split between thread blocks.  Its contents
+ * need no initialization.
  */
-MXFP4_API mxfp4_status mxfp4_gemm_workspace_init(void* workspace_dev, size_t workspace_bytes, void* stream);
+MXFP4_API size_t mxfp4_gemm_workspace_bytes(int M, int N, int K);
 
 /*
  * W4A4 MXFP4 GEMM with fused bias — the pages' gemm_a4w4 followed by
@@ -167,19 +163,16 @@ MXFP4_API mxfp4_status mxfp4_gemm_workspace_init(void* workspace_dev, size_t wor
  *   bias_dev       bf16 [N] or NULL
  *   out_dev        bf16 [M][ldo], ldo >= N
  *   workspace_dev  >= mxfp4_gemm_workspace_bytes(M, N, K) bytes of device
- *                  scratch owned by the caller.  Its first 16 KiB hold
- *                  control words (flags between the kernel's thread blocks
- *                  and an epoch counter) that must be zero before the
- *                  workspace's first use (mxfp4_gemm_workspace_init, or
- *                  zeroed memory) and that the caller must not write
- *                  afterwards; the rest is clobbered by every call.  One
- *                  workspace may serve calls of any shape.
- * Calls sharing one workspace must be ordered on the GPU.
- * For M <= 64 the whole call is one kernel launch (a bf16 input is
- * quantized inside the GEMM kernel) whose thread blocks,
- * at most one per SM, must all be resident together; if work on other
- * streams keeps SMs occupied for about a second, the call gives up and
- * mxfp4_get_device_error reports MXFP4_ERR_TIMEOUT.
+ *                  scratch owned by the caller, clobbered by every call (no
+ *                  initialization needed).  One workspace may serve calls of
+ *                  any shape; calls sharing one must be ordered on the GPU.
+ * For M <= 8 with a bf16 input the whole call is one kernel launch (each
+ * thread block quantizes the activations of its own k-range); for
+ * 8 < M <= 64 the activation quantizer runs first.  The GEMM kernel is a
+ * programmatic dependent launch that reads the packed weights before the
+ * previous kernel in the stream has finished: the weights must not be
+ * written by the kernel immediately before the call (mxfp4_pack_weights
+ * ends with a launch that keeps this true).
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, WORKSPACE, CUDA.
  */
 MXFP4_API mxfp4_status mxfp4_gemm(const void* a_bf16_dev, int lda,
@@ -221,10 +214,10 @@ MXFP4_API mxfp4_status a16wfp4_bmm(const void* x_dev, const void* w_packed_dev, 
  * MXFP4_ERR_WORKSPACE.  Nothing is allocated or freed.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress); make that first call before any stream capture.
- *   - All calls share the one array and it keeps the last call's contents.
- *     It starts zeroed (its control words need that), and calls that
- *     overlap on the GPU — on different streams, or from several host
- *     threads without ordering — race on it.
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (no call needs it cleared); calls that overlap on the GPU — on
+ *     different streams, or from several host threads without ordering —
+ *     race on it.
  */
 MXFP4_API mxfp4_status mxfp4_gemm_noalloc(const void* a_bf16_dev, int lda, const void* w_packed_dev,
                                           const void* bias_dev, void* out_dev, int ldo, int M, int N, int K,

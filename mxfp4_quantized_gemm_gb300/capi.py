@@ -38,7 +38,6 @@ _SIGNATURES = {
     "mxfp4_act_scale_bytes": (_sz, [_i, _i, _i]),
     "mxfp4_quant_act": (_i, [_p, _i, _i, _i, _p, _p, _i, _p]),
     "mxfp4_gemm_workspace_bytes": (_sz, [_i, _i, _i]),
-    "mxfp4_gemm_workspace_init": (_i, [_p, _sz, _p]),
     "mxfp4_gemm": (_i, [_p, _i, _p, _p, _i, _p, _p, _p, _i, _i, _i, _i, _p, _sz, _p]),
     "a16wfp4_bmm": (_i, [_p, _p, _p, _i, _i, _i, _i, _i, _p]),
     "mxfp4_get_device_error": (_i, [_p]),
@@ -101,11 +100,6 @@ def mxfp4_act_scale_bytes(M: int, K: int, layout: int) -> int:
 
 def mxfp4_gemm_workspace_bytes(M: int, N: int, K: int) -> int:
     return lib.mxfp4_gemm_workspace_bytes(M, N, K)
-
-
-def mxfp4_gemm_workspace_init(workspace, workspace_bytes: int, stream=None) -> None:
-    _check(lib.mxfp4_gemm_workspace_init(_ptr(workspace), workspace_bytes, _stream(stream)),
-           "mxfp4_gemm_workspace_init")
 
 
 def mxfp4_pack_weights(w_codes, w_scales, batch: int, N: int, K: int, packed, stream=None) -> None:

@@ -45,15 +45,14 @@ static mxfp4_status device_ready(DeviceInfo* dev) {
 
 static mxfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA; }
 
-// Workspace carve-up of mxfp4_gemm: control words (flags and epoch, fixed
-// size and offset so that calls of any shape may share one workspace), tiled
-// activation codes, tiled scales, stream-K partial sums, each 1 KiB aligned.
+// Workspace carve-up of mxfp4_gemm: tiled (or blocked) activation codes,
+// tiled scales, stream-K partial sums, each 1 KiB aligned.
 struct GemmWorkspace {
   size_t codes_off, scales_off, streamk_off, total;
 };
 static GemmWorkspace gemm_workspace_layout(int M, int N, int K, int grid) {
   GemmWorkspace w{};
-  w.codes_off = kDecodeCtrlBytes;
+  w.codes_off = 0;
   w.scales_off = w.codes_off + round_up(static_cast<size_t>(tiled_code_bytes(M, K)), 1024);
   w.streamk_off = w.scales_off + round_up(static_cast<size_t>(tiled_scale_bytes(M, K)), 1024);
   w.total = w.streamk_off + round_up(gemm_streamk_workspace_bytes(M, N, K, grid), 1024);
@@ -74,7 +73,7 @@ using namespace mx;
 
 extern "C" {
 
-int mxfp4_abi_version(void) { return 1; }
+int mxfp4_abi_version(void) { return 2; }
 
 const char* mxfp4_status_string(mxfp4_status s) {
   switch (s) {
@@ -186,17 +185,21 @@ mxfp4_status mxfp4_gemm(const void* a_bf16, int lda, const uint8_t* a_codes, con
     d.M = M;
     d.N = N;
     d.K = K;
-    d.ctrl = reinterpret_cast<uint32_t*>(ws);
-    d.partials = reinterpret_cast<float*>(ws + wl.streamk_off);
-    d.a_codes = ws + wl.codes_off;
-    d.a_scales = ws + wl.scales_off;
-    if (from_bf16) {
+    if (from_bf16 && M <= kDecodeLocalQuantMaxM) {
       d.x = a_bf16;   // quantized inside the GEMM kernel
       d.ldx = lda;
+    } else if (from_bf16) {
+      // quantized by the standalone quantizer first, into the blocked form
+      cudaError_t e =
+          launch_quant(a_bf16, M, K, lda, ws + wl.codes_off, nullptr, ActLayout::kBlocked, gemm_rows_a(M), dev, s);
+      if (e != cudaSuccess) return MXFP4_ERR_CUDA;
+      d.a_codes = ws + wl.codes_off;
+      d.a_blocked = true;
     } else if (a_layout == MXFP4_LAYOUT_ROWMAJOR) {
       // the pages' pre-quantized (x_fp4, x_scales) input: re-lay out, pad scales with 0x7F
       cudaError_t e = launch_pack(a_codes, a_scales, 1, M, K, ws + wl.codes_off, dev, s);
       if (e != cudaSuccess) return MXFP4_ERR_CUDA;
+      d.a_codes = ws + wl.codes_off;
       d.a_scales = ws + wl.codes_off + tiled_code_bytes(M, K);
     } else {
       d.a_codes = a_codes;
@@ -233,16 +236,6 @@ mxfp4_status mxfp4_gemm(const void* a_bf16, int lda, const uint8_t* a_codes, con
   p.workspace = ws + wl.streamk_off;
   p.workspace_bytes = wl.total - wl.streamk_off;
   return from_cuda(launch_gemm(p, dev, s));
-}
-
-mxfp4_status mxfp4_gemm_workspace_init(void* workspace, size_t workspace_bytes, void* stream) {
-  if (workspace == nullptr) return MXFP4_ERR_INVALID_ARG;
-  if (workspace_bytes < kDecodeCtrlBytes) return MXFP4_ERR_WORKSPACE;
-  if (!aligned16(workspace)) return MXFP4_ERR_MISALIGNED;
-  DeviceInfo dev;
-  mxfp4_status st = device_ready(&dev);
-  if (st != MXFP4_OK) return st;
-  return from_cuda(cudaMemsetAsync(workspace, 0, kDecodeCtrlBytes, static_cast<cudaStream_t>(stream)));
 }
 
 mxfp4_status a16wfp4_bmm(const void* x, const void* w_packed, void* out, int B, int M, int N, int K,

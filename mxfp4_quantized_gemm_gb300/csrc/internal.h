@@ -33,21 +33,13 @@ constexpr uint32_t kErrTimeout = 1u;
 
 // Largest stream-K grid the decode GEMM uses; sizes its partial-sum slots.
 constexpr int kMaxStreamKCtas = 256;
-// Largest activation row count served by the one-launch decode kernel.
+// Largest activation row count served by the decode kernel.
 constexpr int kDecodeMaxM = 64;
+// Largest activation row count the decode kernel quantizes itself (each CTA
+// its own k-steps, every quantizing warp one row); above it the standalone
+// quantizer runs first and the kernel copies the quantized rows in.
+constexpr int kDecodeLocalQuantMaxM = 8;
 
-// Control words at the start of every GEMM workspace (must be zero before
-// the workspace's first use): word 0 epoch, word 1 CTAs done, words
-// kCtrlPartFlags.. one flag per stream-K partial slot (2 per CTA), words
-// kCtrlUnitFlags.. one flag per (activation k-step, 8-row unit).
-constexpr size_t kDecodeCtrlBytes = 16384;
-constexpr int kCtrlEpoch = 0;
-constexpr int kCtrlDone = 1;
-constexpr int kCtrlPartFlags = 256;
-constexpr int kCtrlUnitFlags = 1024;
-// Largest K / 256 with unit flags for every k-step (8 per k-step).
-constexpr int kMaxUnitKT = static_cast<int>((kDecodeCtrlBytes / 4 - kCtrlUnitFlags) / 8);
-static_assert(kCtrlPartFlags + 2 * kMaxStreamKCtas <= kCtrlUnitFlags, "part flags overlap unit flags");
 // Activation rows of a 128-row tile the GEMM loads: 16, 32 or 64 when
 // M <= kDecodeMaxM (only those rows of the tiled activations are read), else 128.
 inline int gemm_rows_a(int M) { return M <= 16 ? 16 : (M <= 32 ? 32 : (M <= 64 ? 64 : 128)); }
@@ -103,14 +95,13 @@ uint32_t gemm_read_clear_error();
 struct DecodeProblem {
   const void* x;            // bf16 activations [M][ldx] (quantized by the kernel); null when a_codes/a_scales hold them
   int ldx;
-  const uint8_t* a_codes;   // TILED activation codes (input when x == null, else scratch)
-  const uint8_t* a_scales;  // TILED activation scales
+  const uint8_t* a_codes;   // x == null: TILED activation codes, or the blocked activations (a_blocked)
+  const uint8_t* a_scales;  // x == null: TILED activation scales (unused when a_blocked)
+  bool a_blocked;           // a_codes holds blocked activations with gemm_rows_a(M)-row blocks
   const uint8_t* w_packed;
   const void* bias;
   void* out;
   int ldo, M, N, K;
-  uint32_t* ctrl;           // kDecodeCtrlBytes of control words
-  float* partials;          // gemm_streamk_workspace_bytes(M, N, K, grid)
 };
 cudaError_t launch_decode(const DecodeProblem& p, const DeviceInfo& dev, cudaStream_t s);
 uint32_t decode_read_clear_error();

@@ -6,8 +6,8 @@
 // serving loops that must never hit cudaMalloc's implicit synchronisation,
 // and host applications whose memory is owned by a foreign allocator that
 // this library cannot reach.  For them, the scratch that mxfp4_gemm needs
-// (control words, tiled activation codes and scales, stream-K partial sums)
-// lives in one file-scope device array of fixed size instead.
+// (quantized activation codes and scales, stream-K partial sums) lives in one
+// file-scope device array of fixed size instead.
 //
 // The array exists on every GPU where this library's module is loaded, from
 // the first use on that device until the process exits.  Its address is

@@ -10,42 +10,41 @@
 
 namespace mx {
 
-// E2M1 magnitude index of a non-negative float by round-to-nearest-even on
-// the grid {0, .5, 1, 1.5, 2, 3, 4, 6}, saturating at 6.  Each comparison is
-// one midpoint of the grid; a value exactly on a midpoint goes to the
-// neighbour with the even code (the comparison is strict towards the odd
-// code: 0.25 -> 0, 0.75 -> 2, 1.25 -> 2, 1.75 -> 4, 2.5 -> 4, 3.5 -> 6, 5 -> 6).
-__device__ __forceinline__ uint32_t e2m1_magnitude(float a) {
-  return static_cast<uint32_t>(a > 0.25f) + static_cast<uint32_t>(a >= 0.75f) +
-         static_cast<uint32_t>(a > 1.25f) + static_cast<uint32_t>(a >= 1.75f) +
-         static_cast<uint32_t>(a > 2.5f) + static_cast<uint32_t>(a >= 3.5f) + static_cast<uint32_t>(a > 5.0f);
-}
-
-// Loads this lane's 8 bf16 values of row r, elements [e0, e0 + 8) (zeros past
-// K or for r >= M).
-__device__ __forceinline__ void load8_bf16(const uint16_t* __restrict__ x, int r, int M, int K, int ldx, int e0,
-                                           bool vec_ok, uint16_t (&v)[8]) {
-  if (r < M && vec_ok && e0 + 8 <= K) {
-    const uint4 q = __ldg(reinterpret_cast<const uint4*>(x + static_cast<size_t>(r) * ldx + e0));
-    v[0] = q.x & 0xFFFF; v[1] = q.x >> 16; v[2] = q.y & 0xFFFF; v[3] = q.y >> 16;
-    v[4] = q.z & 0xFFFF; v[5] = q.z >> 16; v[6] = q.w & 0xFFFF; v[7] = q.w >> 16;
-  } else {
+// Loads this lane's 8 bf16 values of row r, elements [e0, e0 + 8), as four
+// words (element e0 + 2i in the low half of word i; zeros past K or for
+// r >= M).  L2-cached loads: x may have been written by the kernel this one
+// depends on.
+__device__ __forceinline__ uint4 load8_words(const uint16_t* __restrict__ x, int r, int M, int K, int ldx, int e0,
+                                             bool vec_ok) {
+  if (r >= M) return make_uint4(0, 0, 0, 0);
+  const uint16_t* src = x + static_cast<size_t>(r) * ldx + e0;
+  if (vec_ok && e0 + 8 <= K) return __ldcg(reinterpret_cast<const uint4*>(src));
+  uint32_t w[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      v[i] = (r < M && e0 + i < K) ? x[static_cast<size_t>(r) * ldx + e0 + i] : static_cast<uint16_t>(0);
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t lo = e0 + 2 * i < K ? src[2 * i] : 0u;
+    const uint32_t hi = e0 + 2 * i + 1 < K ? src[2 * i + 1] : 0u;
+    w[i] = lo | (hi << 16);
   }
+  return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
-// Quantizes one 32-element block held by 4 consecutive lanes (8 values each;
-// all 32 lanes of the warp call this together).  Returns this lane's 4 code
-// bytes (element 2j in the low nibble) and, through sbyte, the block's E8M0
-// scale byte (0xFF with zero codes for a block holding Inf or NaN).
-__device__ __forceinline__ uint32_t quantize8(const uint16_t (&v)[8], uint32_t& sbyte) {
-  // Block amax on the magnitude bits (bf16 magnitudes order like integers;
-  // Inf and NaN sort above every finite value).
-  uint32_t am = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) am = max(am, static_cast<uint32_t>(v[i] & 0x7FFF));
+// Quantizes one 32-element block held by 4 consecutive lanes (8 values each,
+// as four bf16 pairs; all 32 lanes of the warp call this together).
+// Returns this lane's 4 code bytes (element 2j in the low nibble) and,
+// through sbyte, the block's E8M0 scale byte (0xFF with zero codes for a
+// block holding Inf or NaN).
+//
+// amax: bf16 magnitudes order like unsigned integers (Inf and NaN above
+// every finite value), so a SIMD max over the sign-cleared halves finds it.
+// Each value is multiplied by 2^(127 - sbyte), exact in fp32 (the power is
+// a normal float and no flush to zero applies), and the hardware E2M1
+// conversion rounds to nearest, ties to even, saturating at 6; a value that
+// rounds to zero keeps its sign (-0 encodes as 0x8).
+__device__ __forceinline__ uint32_t quantize8_words(uint4 v, uint32_t& sbyte) {
+  const uint32_t m2 = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                               __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+  uint32_t am = max(m2 & 0xFFFFu, m2 >> 16);
   am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 1));
   am = max(am, __shfl_xor_sync(0xFFFFFFFFu, am, 2));
   const uint32_t ef = am >> 7;                 // biased exponent field of amax
@@ -53,15 +52,37 @@ __device__ __forceinline__ uint32_t quantize8(const uint16_t (&v)[8], uint32_t& 
   // floor(log2 amax) - 2 as an E8M0 byte, clamped at 0 (zero / subnormal amax)
   sbyte = nonfinite ? 0xFFu : (ef > 2 ? ef - 2 : 0u);
   const float inv = __uint_as_float((254u - (nonfinite ? 0u : sbyte)) << 23);   // 2^(127 - sbyte)
-  uint32_t packed = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float a = __uint_as_float(static_cast<uint32_t>(v[i] & 0x7FFF) << 16) * inv;
-    uint32_t c = e2m1_magnitude(a) | ((v[i] >> 12) & 8u);
-    if (nonfinite) c = 0;
-    packed |= c << (4 * i);
-  }
-  return packed;
+  const float f0 = __uint_as_float(v.x << 16) * inv, f1 = __uint_as_float(v.x & 0xFFFF0000u) * inv;
+  const float f2 = __uint_as_float(v.y << 16) * inv, f3 = __uint_as_float(v.y & 0xFFFF0000u) * inv;
+  const float f4 = __uint_as_float(v.z << 16) * inv, f5 = __uint_as_float(v.z & 0xFFFF0000u) * inv;
+  const float f6 = __uint_as_float(v.w << 16) * inv, f7 = __uint_as_float(v.w & 0xFFFF0000u) * inv;
+  uint32_t packed;
+  // cvt.rn.satfinite.e2m1x2.f32 d, a, b puts a in the high nibble, b in the low.
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(packed)
+      : "f"(f0), "f"(f1), "f"(f2), "f"(f3), "f"(f4), "f"(f5), "f"(f6), "f"(f7));
+  return nonfinite ? 0u : packed;
+}
+
+// Same for 8 values given one by one.
+__device__ __forceinline__ uint32_t quantize8(const uint16_t (&v)[8], uint32_t& sbyte) {
+  const uint4 w = make_uint4(v[0] | (static_cast<uint32_t>(v[1]) << 16), v[2] | (static_cast<uint32_t>(v[3]) << 16),
+                             v[4] | (static_cast<uint32_t>(v[5]) << 16), v[6] | (static_cast<uint32_t>(v[7]) << 16));
+  return quantize8_words(w, sbyte);
+}
+
+// Loads this lane's 8 bf16 values of row r, elements [e0, e0 + 8) (zeros past
+// K or for r >= M).
+__device__ __forceinline__ void load8_bf16(const uint16_t* __restrict__ x, int r, int M, int K, int ldx, int e0,
+                                           bool vec_ok, uint16_t (&v)[8]) {
+  const uint4 q = load8_words(x, r, M, K, ldx, e0, vec_ok);
+  v[0] = q.x & 0xFFFF; v[1] = q.x >> 16; v[2] = q.y & 0xFFFF; v[3] = q.y >> 16;
+  v[4] = q.z & 0xFFFF; v[5] = q.z >> 16; v[6] = q.w & 0xFFFF; v[7] = q.w >> 16;
 }
 
 }  // namespace mx

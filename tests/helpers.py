@@ -39,10 +39,8 @@ def empty_u8(n: int) -> torch.Tensor:
 
 def gemm_workspace(capi, n: int) -> torch.Tensor:
     """A GEMM workspace as a caller would set one up: arbitrary contents
-    (filled with 0xA5 here), then mxfp4_gemm_workspace_init."""
-    ws = torch.full((max(int(n), 1),), 0xA5, dtype=torch.uint8, device="cuda")
-    capi.mxfp4_gemm_workspace_init(ws, ws.numel())
-    return ws
+    (filled with 0xA5 here; the GEMM needs no initialization)."""
+    return torch.full((max(int(n), 1),), 0xA5, dtype=torch.uint8, device="cuda")
 
 
 def pack_weights(capi, codes: np.ndarray, scales: np.ndarray, K: int) -> torch.Tensor:

@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(capi):
 
 
 def test_abi_version_and_status_strings(capi):
-    assert capi.mxfp4_abi_version() == 1
+    assert capi.mxfp4_abi_version() == 2
     for s in range(8):
         assert capi.mxfp4_status_string(s).startswith("MXFP4_")
     assert capi.mxfp4_status_string(99) == "MXFP4_ERR_UNKNOWN"
