@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           const int s = i % C::kStages;
           if (!mbar_wait(&full[s], (i / C::kStages) & 1, abort)) break;
           tc_fence_after();
-          issue_stage_mma<C>(tmem, smem_u32(smem + s * C::kStageBytes), j != 0 ? 1u : 0u);
+          issue_stage_mma<C>(tmem, smem_u32(smem + s * C::kStageBytes), s, j != 0 ? 1u : 0u);
           mma_commit(&empty[s]);
         }
         mma_commit(acc_full);

@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs g) {
           const uint32_t ph = (i / C::kStages) & 1;
           if (!mbar_wait(&full[s], ph, abort)) break;
           tc_fence_after();
-          issue_stage_mma<C>(tmem, smem_u32(smem + s * C::kStageBytes), j != 0 ? 1u : 0u);
+          issue_stage_mma<C>(tmem, smem_u32(smem + s * C::kStageBytes), s, j != 0 ? 1u : 0u);
           mma_commit(&empty[s]);
         }
         mma_commit(acc_full);

@@ -40,8 +40,14 @@ struct Cfg {
   static constexpr int kStages = kStagesFit > 8 ? 8 : kStagesFit;
   static constexpr int kRing = kStages * kStageBytes + kTailPad;
   static constexpr int kSmem = kRing + 1024 + 512;
-  static constexpr uint32_t kTmemCols = 512;      // accumulator 256 + scales 24
-  static constexpr uint32_t kSfa = 256, kSfb = 264;
+  // TMEM: the 128 x 256 fp32 accumulator in columns 0..255, then one
+  // 32-column scale slot per ring stage (activation scales in its first 8
+  // columns, weight scales in the next 16).  A stage's scales never share
+  // columns with the stage before it, so copying them in does not wait for
+  // the previous stage's MMAs to finish reading theirs.
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kSfBase = 256, kSfSlot = 32, kSfbOff = 8;
+  static_assert(kSfBase + kStages * kSfSlot <= kTmemCols, "scale slots exceed TMEM");
 };
 
 __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
@@ -115,13 +121,14 @@ __device__ __forceinline__ void store_quad(const OutView& o, int m, int n, float
 }
 
 // Issues the tcgen05.cp scale copies and the four K = 64 block-scaled MMAs
-// of one stage: accumulator [128 act rows x 256 weight rows] at `tmem`,
-// activation scales at TMEM column sfa (2 atoms), weight scales at sfb
-// (2 atoms x 2 row halves; atom of half q, block group a at q * 1024 +
-// a * 512 after the codes).  `accumulate` = 0 starts a new tile.
+// of one stage held in ring slot `slot`: accumulator [128 act rows x 256
+// weight rows] at `tmem`, activation scales at TMEM column sfa (2 atoms),
+// weight scales at sfb (2 atoms x 2 row halves; atom of half q, block group
+// a at q * 1024 + a * 512 after the codes), both in the slot's scale
+// columns.  `accumulate` = 0 starts a new tile.
 template <typename C>
-__device__ __forceinline__ void issue_stage_mma(uint32_t tmem, uint32_t stage_base, uint32_t accumulate) {
-  const uint32_t sfa = tmem + C::kSfa, sfb = tmem + C::kSfb;
+__device__ __forceinline__ void issue_stage_mma(uint32_t tmem, uint32_t stage_base, int slot, uint32_t accumulate) {
+  const uint32_t sfa = tmem + C::kSfBase + static_cast<uint32_t>(slot) * C::kSfSlot, sfb = sfa + C::kSfbOff;
   const uint32_t w_s = stage_base, sw_s = w_s + 2 * kTileBytes, a_s = stage_base + C::kW, sa_s = a_s + C::kA;
   tmem_cp_scales(sfa + 0, sdesc_scales(sa_s));
   tmem_cp_scales(sfa + 4, sdesc_scales(sa_s + 512));
