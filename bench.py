@@ -555,6 +555,29 @@ def run_reference(args, world, rank):
     return line, rank
 
 
+def run_single_bmm(args):
+    """Run one MLA absorbed BMM (`kup` or `vup`, B = 64) `calls` times (for ncu captures)."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from mxfp4_quantized_gemm_gb300 import capi, synth
+    kind, M = args.single_bmm.split(",")
+    M = int(M)
+    B, N, K, layout = (64, 512, 192, capi.OUT_BMN) if kind == "kup" else (64, 256, 512, capi.OUT_MBN)
+    wc = synth.weight_codes(N, K, seed=N, batch=B)
+    ws = synth.weight_scales(N, K, -6, 0, seed=N, batch=B)
+    pk = torch.empty(capi.mxfp4_packed_weight_bytes(B, N, K), dtype=torch.uint8, device="cuda")
+    capi.mxfp4_pack_weights(torch.from_numpy(wc).cuda(), torch.from_numpy(ws).cuda(), B, N, K, pk)
+    x = synth.bf16_tensor(synth.bmm_activations(B, M, K, seed=M)).cuda()
+    out = torch.empty(B * M * N, dtype=torch.bfloat16, device="cuda")
+    for _ in range(args.calls):
+        capi.a16wfp4_bmm(x, pk, out, B, M, N, K, layout)
+    torch.cuda.synchronize()
+    assert capi.mxfp4_get_device_error() == capi.OK
+    print(f"single bmm {kind} M={M}: {args.calls} calls ok")
+
+
 def run_single(args):
     """Run one dense-linear shape `calls` times over `copies` weight copies (for ncu captures)."""
     import torch
@@ -591,11 +614,16 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--single", type=str, default=None,
                     help="profiling mode: M,N,K of one dense-linear call (bf16 input), no JSON line")
+    ap.add_argument("--single-bmm", type=str, default=None,
+                    help="profiling mode: kup,M or vup,M of one A16WFP4 BMM call, no JSON line")
     ap.add_argument("--calls", type=int, default=6)
     ap.add_argument("--copies", type=int, default=4)
     args = ap.parse_args()
     if args.single:
         run_single(args)
+        return
+    if args.single_bmm:
+        run_single_bmm(args)
         return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

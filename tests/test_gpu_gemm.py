@@ -179,12 +179,20 @@ def test_tiny_shape_sweep(capi):
 
 @pytest.mark.parametrize("M,N,K", [(64, 256, 32768), (5, 300, 65536), (2, 256, 98560), (33, 256, 98560)])
 def test_tiles_shared_by_many_ctas(capi, M, N, K):
-    """One or two output tiles over a long K: every tile's k-steps are split
-    over dozens of CTAs (more than a warp's worth of parts to wait for and
-    sum).  K = 98560 is past the longest K with a flag per activation unit,
-    so the standalone quantizer kernel runs before the GEMM (M = 2 and the
-    64-row tiles of M = 33)."""
+    """One or two output tiles over a long K: for M <= 64 every tile's
+    k-steps are split over a cluster of 8 CTAs whose parts are summed in
+    shared memory (M = 2 and 5 quantized by the GEMM kernel itself, M = 33
+    and 64 by the quantizer first); for larger M, stream-K parts."""
     full_check(capi, M, N, K, seed=21, with_bias=True)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 40000, 512), (8, 39168, 1024), (12, 40960, 768), (64, 39000, 512)])
+def test_more_tiles_than_sms(capi, M, N, K):
+    """More 256-row weight tiles than SMs (152 on GB300): each decode CTA
+    takes whole tiles in turn, draining the accumulator between them, with
+    the activations quantized by four of its warps (M <= 8) or by the
+    quantizer kernel first."""
+    full_check(capi, M, N, K, seed=31, with_bias=True)
 
 
 def test_one_workspace_for_every_shape_and_graph_replays(capi):
