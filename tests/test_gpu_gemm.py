@@ -196,9 +196,10 @@ def test_more_tiles_than_sms(capi, M, N, K):
 
 
 def test_one_workspace_for_every_shape_and_graph_replays(capi):
-    """Calls of different shapes and input forms share one workspace (its
-    control words carry over from call to call), eagerly and replayed from a
-    CUDA graph, and give the bits of the same calls on fresh workspaces."""
+    """Calls of different shapes and input forms share one workspace (whatever
+    one call leaves in it, the next may not depend on), eagerly and replayed
+    from a CUDA graph, and give the bits of the same calls on fresh
+    workspaces."""
     shapes = [(1, 14336, 5120), (64, 5120, 14336), (200, 1024, 5120), (16, 1000, 5152), (33, 128, 256),
               (2, 256, 98560)]
     probs, want = [], []
