@@ -141,18 +141,41 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs g) {
     __syncwarp();   // whole warp reaches the final barrier converged
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---- MMA issuer: one accumulator, one segment (part of a tile) at a time
+      // ---- MMA issuer: one accumulator, one segment (part of a tile) at a
+      // time.  Consecutive tiles of a CTA share their activation rows (tile
+      // t = mt * n_tiles + nt), so when every k-step's activation scales fit
+      // in TMEM past the accumulator and 16-column weight-scale slots
+      // (K <= 6144) they are copied once per activation row tile and k-step
+      // and reused: four scale copies per stage instead of six.  (The tensor
+      // pipe runs copies and MMAs in issue order, so a row tile's scales
+      // overwrite the previous one's only after the MMAs that read them.)
+      constexpr uint32_t kSfaRes = C::kSfBase + C::kStages * 16u;
+      const bool resident = kSfaRes + 8u * static_cast<uint32_t>(KT) <= C::kTmemCols;
+      int cur_mt = -1;
+      uint32_t have = 0;   // k-steps whose activation scales of row tile cur_mt are in TMEM
       int i = 0, seg = 0, kt = it0 % KT;
       for (int it = it0; it < it1 && !abort; ++seg) {
         const int len = (KT - kt) < (it1 - it) ? (KT - kt) : (it1 - it);
         if (!mbar_wait(acc_empty, (seg & 1) ^ 1, abort)) break;
         tc_fence_after();
+        const int mt = (it / KT) / g.n_tiles;
+        if (mt != cur_mt) {
+          cur_mt = mt;
+          have = 0;
+        }
         for (int j = 0; j < len; ++j, ++i) {
           const int s = i % C::kStages;
           const uint32_t ph = (i / C::kStages) & 1;
           if (!mbar_wait(&full[s], ph, abort)) break;
           tc_fence_after();
-          issue_stage_mma<C>(tmem, smem_u32(smem + s * C::kStageBytes), s, j != 0 ? 1u : 0u);
+          if (resident) {
+            const int k = kt + j;
+            issue_stage_mma_sfa<C>(tmem, smem_u32(smem + s * C::kStageBytes), C::kSfBase + 16u * s,
+                                   kSfaRes + 8u * k, ((have >> k) & 1u) == 0, j != 0 ? 1u : 0u);
+            have |= 1u << k;
+          } else {
+            issue_stage_mma<C>(tmem, smem_u32(smem + s * C::kStageBytes), s, j != 0 ? 1u : 0u);
+          }
           mma_commit(&empty[s]);
         }
         mma_commit(acc_full);

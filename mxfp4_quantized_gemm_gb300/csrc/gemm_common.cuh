@@ -144,6 +144,32 @@ __device__ __forceinline__ void issue_stage_mma(uint32_t tmem, uint32_t stage_ba
   }
 }
 
+// The stage with its activation scales already in TMEM at column `sfa_col`
+// (copied there for an earlier tile of the same activation rows): four
+// weight-scale copies to column `sfb_col`, then the four MMAs.  `copy_a`
+// also copies the stage's activation scales to sfa_col first.
+template <typename C>
+__device__ __forceinline__ void issue_stage_mma_sfa(uint32_t tmem, uint32_t stage_base, uint32_t sfb_col,
+                                                    uint32_t sfa_col, bool copy_a, uint32_t accumulate) {
+  const uint32_t sfa = tmem + sfa_col;
+  const uint32_t sfb = tmem + sfb_col;
+  const uint32_t w_s = stage_base, sw_s = w_s + 2 * kTileBytes, a_s = stage_base + C::kW, sa_s = a_s + C::kA;
+  if (copy_a) {
+    tmem_cp_scales(sfa + 0, sdesc_scales(sa_s));
+    tmem_cp_scales(sfa + 4, sdesc_scales(sa_s + 512));
+  }
+#pragma unroll
+  for (int a = 0; a < 2; ++a)
+#pragma unroll
+    for (int q = 0; q < 2; ++q) tmem_cp_scales(sfb + a * 8 + q * 4, sdesc_scales(sw_s + q * 1024 + a * 512));
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t id = idesc_mxf4(128, kTileN, (q & 1) * 2, (q & 1) * 2);
+    mma_mxf4(tmem, sdesc_sw128(a_s + 32 * q), sdesc_sw128(w_s + 32 * q), id, sfa + 4 * (q >> 1), sfb + 8 * (q >> 1),
+             (accumulate != 0 || q != 0) ? 1u : 0u);
+  }
+}
+
 // Launch as a programmatic dependent of the previous kernel in the stream.
 template <typename Kern, typename Args>
 static cudaError_t launch_pdl(Kern k, int grid, int threads, int smem, cudaStream_t s, const Args& a) {
