@@ -21,6 +21,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstdint>
 
 #include "internal.h"
@@ -288,20 +289,21 @@ __global__ void __launch_bounds__(kBmmThreads, 1) a16wfp4_bmm_kernel(const __gri
 }
 
 // ------------------------------------------------------------------ host
+// The driver's tensor-map encoder, looked up once (thread-safe static init).
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (fn == nullptr) {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return nullptr;
+  }();
   return fn;
 }
 
-static bool g_bmm_attr[64];
+static std::atomic<bool> g_bmm_attr[64];   // kernel attribute set on this device
 
 cudaError_t launch_bmm(const void* x, const uint8_t* w_packed, void* out, int B, int M, int N, int K,
                        bool batch_major, const DeviceInfo& dev, cudaStream_t s) {
@@ -352,11 +354,11 @@ cudaError_t launch_bmm(const void* x, const uint8_t* w_packed, void* out, int B,
   a.stages = stages;
   const int smem = fixed + stages * kSlabBytes;
   if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
-  if (!g_bmm_attr[dev.device]) {
+  if (!g_bmm_attr[dev.device].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(a16wfp4_bmm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          227 * 1024);
     if (e != cudaSuccess) return e;
-    g_bmm_attr[dev.device] = true;
+    g_bmm_attr[dev.device].store(true, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(pairs), static_cast<unsigned>(m_groups), 1);

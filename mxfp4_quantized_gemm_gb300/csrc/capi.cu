@@ -2,22 +2,32 @@
 // the host, workspace carving, dispatch to the kernels of quant.cu, gemm.cu
 // and bmm.cu.  No entry point allocates device memory.
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstdint>
+#include <mutex>
 
 #include "mxfp4.h"
 #include "internal.h"
 
 namespace mx {
 
+// Per-device properties, filled once under a lock; the flag is published
+// with release order so that a thread that sees it set sees the entry.
 static DeviceInfo g_dev_cache[64];
-static bool g_dev_cached[64];
+static std::atomic<bool> g_dev_cached[64];
+static std::mutex g_dev_mutex;
 
 cudaError_t current_device_info(DeviceInfo* out) {
   int d = -1;
   cudaError_t e = cudaGetDevice(&d);
   if (e != cudaSuccess) return e;
   if (d < 0 || d >= 64) return cudaErrorInvalidDevice;
-  if (!g_dev_cached[d]) {
+  if (!g_dev_cached[d].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (g_dev_cached[d].load(std::memory_order_relaxed)) {
+      *out = g_dev_cache[d];
+      return cudaSuccess;
+    }
     DeviceInfo info{d, 0, false};
     int major = 0, minor = 0;
     if ((e = cudaDeviceGetAttribute(&info.sm_count, cudaDevAttrMultiProcessorCount, d)) != cudaSuccess) return e;
@@ -25,7 +35,7 @@ cudaError_t current_device_info(DeviceInfo* out) {
     if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, d)) != cudaSuccess) return e;
     info.ok = (major == 10 && minor == 3);
     g_dev_cache[d] = info;
-    g_dev_cached[d] = true;
+    g_dev_cached[d].store(true, std::memory_order_release);
   }
   *out = g_dev_cache[d];
   return cudaSuccess;

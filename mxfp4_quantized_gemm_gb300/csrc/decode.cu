@@ -36,6 +36,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "gemm_common.cuh"
@@ -375,18 +376,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 }
 
 // ===================================================================== host
-static bool g_attr_set[64][3];
-static int g_max_clusters[64][3][9];   // max co-resident clusters of size S (0: not yet queried)
+// Per-device, per-kernel host caches; several host threads may fill them
+// at once, each writing the same value.
+static std::atomic<bool> g_attr_set[64][3];
+static std::atomic<int> g_max_clusters[64][3][9];   // co-resident clusters of size S (0: not yet queried)
 
 template <int kRowsA>
 static cudaError_t prepare(const DeviceInfo& dev, int which) {
   using C = Cfg<kRowsA>;
   if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
-  if (!g_attr_set[dev.device][which]) {
+  if (!g_attr_set[dev.device][which].load(std::memory_order_acquire)) {
     cudaError_t e =
         cudaFuncSetAttribute(decode_kernel<kRowsA>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
-    g_attr_set[dev.device][which] = true;
+    g_attr_set[dev.device][which].store(true, std::memory_order_release);
   }
   return cudaSuccess;
 }
@@ -395,7 +398,8 @@ static cudaError_t prepare(const DeviceInfo& dev, int which) {
 template <int kRowsA>
 static int max_clusters(int S, const DeviceInfo& dev, int which) {
   using C = Cfg<kRowsA>;
-  int& cached = g_max_clusters[dev.device][which][S];
+  std::atomic<int>& slot = g_max_clusters[dev.device][which][S];
+  int cached = slot.load(std::memory_order_acquire);
   if (cached == 0) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(S), 1, 1);
@@ -414,6 +418,7 @@ static int max_clusters(int S, const DeviceInfo& dev, int which) {
       n = 0;
     }
     cached = n > 0 ? n : -1;
+    slot.store(cached, std::memory_order_release);
   }
   return cached;
 }

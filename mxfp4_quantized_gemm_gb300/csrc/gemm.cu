@@ -27,6 +27,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "gemm_common.cuh"
@@ -310,7 +311,7 @@ __global__ void __launch_bounds__(256, 4) gemm_fixup_kernel(const __grid_constan
 }
 
 // ===================================================================== host
-static bool g_attr_set[64];
+static std::atomic<bool> g_attr_set[64];   // kernel attribute set on this device
 
 
 size_t gemm_streamk_workspace_bytes(int M, int N, int K, int grid) {
@@ -347,10 +348,10 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
   if (a.rows_a != 128) return cudaErrorInvalidValue;   // M <= 64 runs in decode.cu
   using C = Cfg<128>;
   if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
-  if (!g_attr_set[dev.device]) {
+  if (!g_attr_set[dev.device].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
-    g_attr_set[dev.device] = true;
+    g_attr_set[dev.device].store(true, std::memory_order_release);
   }
   cudaError_t e = launch_pdl(gemm_kernel<128>, a.grid, kThreads, C::kSmem, s, a);
   if (e != cudaSuccess) return e;

@@ -261,3 +261,43 @@ def test_unaligned_activation_rows(capi, M, N, K, pad):
     assert capi.mxfp4_get_device_error() == capi.OK
     acc, mag = oracle_gemm_rows(x, np.arange(M), wc, ws, K, b)
     check_close(host_bits(out), acc, mag, n_acc(K), what=f"M={M} N={N} K={K} lda={lda}")
+
+
+def test_concurrent_host_threads(capi):
+    """The entry points are re-entrant: four host threads (ctypes releases
+    the GIL during the call) each run a different shape on their own stream
+    and workspace, twenty calls each, and get the bits of the same calls made
+    one after another."""
+    import threading
+
+    shapes = [(1, 14336, 5120), (16, 5120, 14336), (300, 1024, 5120), (64, 256, 32768)]
+    jobs = []
+    for i, (M, N, K) in enumerate(shapes):
+        x, wc, ws, b = make_problem(M, N, K, seed=60 + i, with_bias=True)
+        packed = pack_weights(capi, wc, ws, K)
+        want = run_gemm(capi, x, packed, b, M, N, K)
+        wsb = capi.mxfp4_gemm_workspace_bytes(M, N, K)
+        jobs.append(dict(M=M, N=N, K=K, x=dev_bf16(x), packed=packed, bias=dev_bf16(b), want=want,
+                         ws=gemm_workspace(capi, wsb), wsb=wsb, stream=torch.cuda.Stream(),
+                         out=torch.empty(M, N, dtype=torch.bfloat16, device="cuda")))
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(j):
+        try:
+            for _ in range(20):
+                capi.mxfp4_gemm(j["x"], j["K"], None, None, 0, j["packed"], j["bias"], j["out"], j["N"], j["M"],
+                                j["N"], j["K"], j["ws"], j["wsb"], j["stream"])
+        except Exception as e:   # reported below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(j,)) for j in jobs]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    assert capi.mxfp4_get_device_error() == capi.OK
+    for j in jobs:
+        assert np.array_equal(host_bits(j["out"]), j["want"]), (j["M"], j["N"], j["K"])
