@@ -157,8 +157,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs g) {
       int i = 0, seg = 0, kt = it0 % KT;
       for (int it = it0; it < it1 && !abort; ++seg) {
         const int len = (KT - kt) < (it1 - it) ? (KT - kt) : (it1 - it);
-        if (!mbar_wait(acc_empty, (seg & 1) ^ 1, abort)) break;
-        tc_fence_after();
         const int mt = (it / KT) / g.n_tiles;
         if (mt != cur_mt) {
           cur_mt = mt;
@@ -169,14 +167,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs g) {
           const uint32_t ph = (i / C::kStages) & 1;
           if (!mbar_wait(&full[s], ph, abort)) break;
           tc_fence_after();
-          if (resident) {
-            const int k = kt + j;
-            issue_stage_mma_sfa<C>(tmem, smem_u32(smem + s * C::kStageBytes), C::kSfBase + 16u * s,
-                                   kSfaRes + 8u * k, ((have >> k) & 1u) == 0, j != 0 ? 1u : 0u);
-            have |= 1u << k;
-          } else {
-            issue_stage_mma<C>(tmem, smem_u32(smem + s * C::kStageBytes), s, j != 0 ? 1u : 0u);
+          const uint32_t st = smem_u32(smem + s * C::kStageBytes);
+          const int k = kt + j;
+          const uint32_t sfa_col = resident ? kSfaRes + 8u * k : C::kSfBase + s * C::kSfSlot;
+          const uint32_t sfb_col = resident ? C::kSfBase + 16u * s : sfa_col + C::kSfbOff;
+          // the scale copies first: at a segment start they run while the
+          // epilogue still drains the previous segment's accumulator
+          issue_stage_scales_sfa<C>(tmem, st, sfb_col, sfa_col, !resident || ((have >> k) & 1u) == 0);
+          if (resident) have |= 1u << k;
+          if (j == 0) {
+            if (!mbar_wait(acc_empty, (seg & 1) ^ 1, abort)) break;
+            tc_fence_after();
           }
+          issue_stage_mmas_sfa<C>(tmem, st, sfb_col, sfa_col, j != 0 ? 1u : 0u);
           mma_commit(&empty[s]);
         }
         mma_commit(acc_full);

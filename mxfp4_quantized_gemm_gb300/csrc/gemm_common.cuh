@@ -120,40 +120,21 @@ __device__ __forceinline__ void store_quad(const OutView& o, int m, int n, float
   }
 }
 
-// Issues the tcgen05.cp scale copies and the four K = 64 block-scaled MMAs
-// of one stage held in ring slot `slot`: accumulator [128 act rows x 256
-// weight rows] at `tmem`, activation scales at TMEM column sfa (2 atoms),
-// weight scales at sfb (2 atoms x 2 row halves; atom of half q, block group
-// a at q * 1024 + a * 512 after the codes), both in the slot's scale
-// columns.  `accumulate` = 0 starts a new tile.
+// One stage of the MMA pipeline: the tcgen05.cp copies of its scales into
+// TMEM -- activation scales (2 atoms) at column sfa_col, weight scales (2
+// atoms x 2 row halves; atom of half q, block group a at q * 1024 + a * 512
+// after the codes) at sfb_col -- then the four K = 64 block-scaled MMAs into
+// the accumulator [128 act rows x 256 weight rows] at `tmem`; `accumulate` =
+// 0 starts a new tile.  The copies write only scale columns, so at a tile
+// boundary they may go out before the accumulator is free again.
+// `copy_a` = false reuses activation scales already at sfa_col (copied for
+// an earlier tile of the same activation rows).
 template <typename C>
-__device__ __forceinline__ void issue_stage_mma(uint32_t tmem, uint32_t stage_base, int slot, uint32_t accumulate) {
-  const uint32_t sfa = tmem + C::kSfBase + static_cast<uint32_t>(slot) * C::kSfSlot, sfb = sfa + C::kSfbOff;
-  const uint32_t w_s = stage_base, sw_s = w_s + 2 * kTileBytes, a_s = stage_base + C::kW, sa_s = a_s + C::kA;
-  tmem_cp_scales(sfa + 0, sdesc_scales(sa_s));
-  tmem_cp_scales(sfa + 4, sdesc_scales(sa_s + 512));
-#pragma unroll
-  for (int a = 0; a < 2; ++a)
-#pragma unroll
-    for (int q = 0; q < 2; ++q) tmem_cp_scales(sfb + a * 8 + q * 4, sdesc_scales(sw_s + q * 1024 + a * 512));
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint32_t id = idesc_mxf4(128, kTileN, (q & 1) * 2, (q & 1) * 2);
-    mma_mxf4(tmem, sdesc_sw128(a_s + 32 * q), sdesc_sw128(w_s + 32 * q), id, sfa + 4 * (q >> 1), sfb + 8 * (q >> 1),
-             (accumulate != 0 || q != 0) ? 1u : 0u);
-  }
-}
-
-// The stage with its activation scales already in TMEM at column `sfa_col`
-// (copied there for an earlier tile of the same activation rows): four
-// weight-scale copies to column `sfb_col`, then the four MMAs.  `copy_a`
-// also copies the stage's activation scales to sfa_col first.
-template <typename C>
-__device__ __forceinline__ void issue_stage_mma_sfa(uint32_t tmem, uint32_t stage_base, uint32_t sfb_col,
-                                                    uint32_t sfa_col, bool copy_a, uint32_t accumulate) {
+__device__ __forceinline__ void issue_stage_scales_sfa(uint32_t tmem, uint32_t stage_base, uint32_t sfb_col,
+                                                       uint32_t sfa_col, bool copy_a) {
   const uint32_t sfa = tmem + sfa_col;
   const uint32_t sfb = tmem + sfb_col;
-  const uint32_t w_s = stage_base, sw_s = w_s + 2 * kTileBytes, a_s = stage_base + C::kW, sa_s = a_s + C::kA;
+  const uint32_t sw_s = stage_base + 2 * kTileBytes, sa_s = stage_base + C::kW + C::kA;
   if (copy_a) {
     tmem_cp_scales(sfa + 0, sdesc_scales(sa_s));
     tmem_cp_scales(sfa + 4, sdesc_scales(sa_s + 512));
@@ -162,12 +143,43 @@ __device__ __forceinline__ void issue_stage_mma_sfa(uint32_t tmem, uint32_t stag
   for (int a = 0; a < 2; ++a)
 #pragma unroll
     for (int q = 0; q < 2; ++q) tmem_cp_scales(sfb + a * 8 + q * 4, sdesc_scales(sw_s + q * 1024 + a * 512));
+}
+template <typename C>
+__device__ __forceinline__ void issue_stage_mmas_sfa(uint32_t tmem, uint32_t stage_base, uint32_t sfb_col,
+                                                     uint32_t sfa_col, uint32_t accumulate) {
+  const uint32_t sfa = tmem + sfa_col;
+  const uint32_t sfb = tmem + sfb_col;
+  const uint32_t w_s = stage_base, a_s = stage_base + C::kW;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const uint32_t id = idesc_mxf4(128, kTileN, (q & 1) * 2, (q & 1) * 2);
     mma_mxf4(tmem, sdesc_sw128(a_s + 32 * q), sdesc_sw128(w_s + 32 * q), id, sfa + 4 * (q >> 1), sfb + 8 * (q >> 1),
              (accumulate != 0 || q != 0) ? 1u : 0u);
   }
+}
+
+template <typename C>
+__device__ __forceinline__ void issue_stage_mma_sfa(uint32_t tmem, uint32_t stage_base, uint32_t sfb_col,
+                                                    uint32_t sfa_col, bool copy_a, uint32_t accumulate) {
+  issue_stage_scales_sfa<C>(tmem, stage_base, sfb_col, sfa_col, copy_a);
+  issue_stage_mmas_sfa<C>(tmem, stage_base, sfb_col, sfa_col, accumulate);
+}
+
+// The same with both scale sets in ring slot `slot`'s 32 TMEM columns.
+template <typename C>
+__device__ __forceinline__ void issue_stage_scales(uint32_t tmem, uint32_t stage_base, int slot) {
+  const uint32_t sfa = tmem + C::kSfBase + static_cast<uint32_t>(slot) * C::kSfSlot;
+  issue_stage_scales_sfa<C>(tmem, stage_base, sfa + C::kSfbOff - tmem, sfa - tmem, true);
+}
+template <typename C>
+__device__ __forceinline__ void issue_stage_mmas(uint32_t tmem, uint32_t stage_base, int slot, uint32_t accumulate) {
+  const uint32_t sfa_col = C::kSfBase + static_cast<uint32_t>(slot) * C::kSfSlot;
+  issue_stage_mmas_sfa<C>(tmem, stage_base, sfa_col + C::kSfbOff, sfa_col, accumulate);
+}
+template <typename C>
+__device__ __forceinline__ void issue_stage_mma(uint32_t tmem, uint32_t stage_base, int slot, uint32_t accumulate) {
+  issue_stage_scales<C>(tmem, stage_base, slot);
+  issue_stage_mmas<C>(tmem, stage_base, slot, accumulate);
 }
 
 // Launch as a programmatic dependent of the previous kernel in the stream.
