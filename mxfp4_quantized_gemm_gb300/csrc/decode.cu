@@ -1,6 +1,7 @@
-// W4A4 MXFP4 GEMM for decode-sized activations (M <= 64): the whole linear
-// layer -- activation quantization, GEMM, split-K reduction, bias and bf16
-// store -- in one kernel launch.
+// W4A4 MXFP4 GEMM for decode-sized activations (M <= 64): the linear layer
+// -- activation quantization (for M <= 8; above that the quantizer kernel
+// runs first), GEMM, split-K reduction, bias and bf16 store -- in one kernel
+// launch.
 //
 //   out[m][n] = bf16_RNE( sum_k deq(Q(x))[m][k] * deq(W)[n][k] + bias[n] )
 //

@@ -4,10 +4,11 @@
 //   out[m][n] = bf16_RNE( sum_k deq(A)[m][k] * deq(W)[n][k] + bias[n] )
 //
 // the gemm_a4w4 + bias step of sglang PR #39598 (blog analysis, section 2,
-// apply_weights).  Both operands arrive in the TILED layout, so every stage
-// is a few contiguous 1-D bulk copies: 16 KiB code tiles already in the
-// 128-byte-swizzled K-major image, 512-byte scale atoms already in the
-// tcgen05.cp source layout.
+// apply_weights).  The weights arrive packed and the activations in the
+// library's blocked form (from the quantizer) or the caller's TILED layout,
+// so every stage is one or two contiguous 1-D bulk copies: code tiles
+// already in the 128-byte-swizzled K-major image, 512-byte scale atoms
+// already in the tcgen05.cp source layout.
 //
 // An output tile is 128 activation rows (the MMA's M) by 256 weight rows
 // (its N): a tcgen05.mma.kind::mxf4.block_scale instruction costs about the
@@ -21,7 +22,10 @@
 // tcgen05.cp (scales -> TMEM) and the MMAs into one 128 x 256 fp32 TMEM
 // accumulator; warps 2..9 drain it (each 32 rows x 128 columns) with
 // tcgen05.ld, release it at once, then add the bias and store bf16 (or
-// publish the part).  The kernel is launched as a programmatic dependent:
+// publish the part).  The tensor pipe bounds the kernel: per 256-wide
+// k-step its four MMAs and the scale copies run back to back, so for
+// K <= 6144 the activation scales of every k-step stay in TMEM across the
+// tiles of one activation row tile (four copies per k-step instead of six).  The kernel is launched as a programmatic dependent:
 // it sets up and requests its first weight stages while the activation
 // quantizer before it finishes, and lets the next kernel launch early.
 #include <cuda_bf16.h>
