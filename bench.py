@@ -363,6 +363,7 @@ def run_ours(args, world, rank, local):
     if not args.no_secondary:
         extra["prefill"] = run_prefill(args, torch, np, capi, synth, dev, stream, bf16_peak, peak_src)
         extra["bmm"] = run_bmm(args, torch, np, capi, synth, dev, stream, hbm_peak, bf16_sust)
+        extra["rmsnorm_quant"] = run_norm_quant(args, torch, np, capi, synth, dev, stream, hbm_peak)
 
     line = {
         "metric": METRIC,
@@ -504,6 +505,63 @@ def run_bmm(args, torch, np, capi, synth, dev, stream, hbm_peak, bf16_sust):
             "l2": "back-to-back calls; x and out exceed L2 at M=4096"}
 
 
+def run_norm_quant(args, torch, np, capi, synth, dev, stream, hbm_peak):
+    """The fused RMSNorm -> MXFP4 producer (TILED output, K = 5120), with and
+    without the fused residual add; 4 rotating input copies per case so that
+    the M = 8192 inputs come from HBM."""
+    sptr = stream.cuda_stream
+    K, copies, reps = 5120, 4, 20
+    res = {}
+    big_bytes, big_ms = 0.0, 0.0
+    for M in (1, 16, 64, 8192):
+        for with_res in (False, True):
+            xs = [synth.bf16_tensor(synth.activations(M, K, seed=M + i)).to(dev) for i in range(copies)]
+            rs = [synth.bf16_tensor(synth.residual(M, K, seed=M + i)).to(dev) if with_res else None
+                  for i in range(copies)]
+            g = synth.bf16_tensor(synth.norm_gamma(K, seed=M)).to(dev)
+            nc, ns = capi.mxfp4_act_code_bytes(M, K, 1), capi.mxfp4_act_scale_bytes(M, K, 1)
+            codes = torch.empty(nc, dtype=torch.uint8, device=dev)
+            scales = torch.empty(ns, dtype=torch.uint8, device=dev)
+
+            def call(i):
+                capi.mxfp4_rmsnorm_quant_act(xs[i % copies], K, rs[i % copies], K, g, 1e-6, M, K, codes, scales,
+                                             1, None, 0, sptr)
+
+            with torch.cuda.stream(stream):
+                for i in range(3):
+                    call(i)
+            stream.synchronize()
+            # the calls replay from a CUDA graph: device time, not host launch cost
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                with torch.cuda.graph(graph, stream=stream):
+                    for i in range(reps):
+                        call(i)
+            stream.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                graph.replay()
+                a.record(stream)
+                graph.replay()
+                b.record(stream)
+            stream.synchronize()
+            assert capi.mxfp4_get_device_error(sptr) == capi.OK
+            ms = a.elapsed_time(b) / reps
+            nbytes = M * K * 2 * (3 if with_res else 1) + K * 2 + nc + ns
+            res[f"M{M}{'_res' if with_res else ''}"] = {"us": round(ms * 1e3, 2),
+                                                        "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+            if M == 8192:
+                big_bytes += nbytes
+                big_ms += ms
+            del xs, rs, graph
+    gbs = big_bytes / (big_ms * 1e-3) / 1e9
+    return {"metric": "fused RMSNorm -> MXFP4 producer GB/s (M = 8192, K = 5120, TILED out, with and without "
+                      "the residual add)", "value": round(gbs, 1), "unit": "GB/s", "peak": hbm_peak,
+            "frac": round(gbs / hbm_peak, 4),
+            "bytes_per_launch": "2*M*K (x) [+ 4*M*K residual read+write] + 2*K (gamma) + TILED codes + scales",
+            "cases": res, "l2": "4 rotating input copies per case; 20 back-to-back calls replayed from a CUDA graph"}
+
+
 # ------------------------------------------------------------------ oracle timing
 def oracle_sample_step(ref, synth, np, M, N, K, rows_w):
     """The oracle's dense linear on M activation rows against a `rows_w`-row slice of the weights."""
@@ -591,6 +649,27 @@ def run_single_bmm(args):
     print(f"single bmm {kind} M={M}: {args.calls} calls ok")
 
 
+def run_single_norm(args):
+    """Run the fused RMSNorm -> MXFP4 producer on M rows of K = 5120 `calls` times (for ncu captures)."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from mxfp4_quantized_gemm_gb300 import capi, synth
+    M, with_res = int(args.single_norm.split(",")[0]), args.single_norm.endswith(",res")
+    K = 5120
+    x = synth.bf16_tensor(synth.activations(M, K, seed=M)).cuda()
+    r = synth.bf16_tensor(synth.residual(M, K, seed=M)).cuda() if with_res else None
+    g = synth.bf16_tensor(synth.norm_gamma(K, seed=M)).cuda()
+    codes = torch.empty(capi.mxfp4_act_code_bytes(M, K, 1), dtype=torch.uint8, device="cuda")
+    scales = torch.empty(capi.mxfp4_act_scale_bytes(M, K, 1), dtype=torch.uint8, device="cuda")
+    for _ in range(args.calls):
+        capi.mxfp4_rmsnorm_quant_act(x, K, r, K, g, 1e-6, M, K, codes, scales, 1)
+    torch.cuda.synchronize()
+    assert capi.mxfp4_get_device_error() == capi.OK
+    print(f"single rmsnorm_quant M={M} K={K} residual={with_res}: {args.calls} calls ok")
+
+
 def run_single(args):
     """Run one dense-linear shape `calls` times over `copies` weight copies (for ncu captures)."""
     import torch
@@ -629,6 +708,8 @@ def main():
                     help="profiling mode: M,N,K of one dense-linear call (bf16 input), no JSON line")
     ap.add_argument("--single-bmm", type=str, default=None,
                     help="profiling mode: kup,M or vup,M of one A16WFP4 BMM call, no JSON line")
+    ap.add_argument("--single-norm", type=str, default=None,
+                    help="profiling mode: M or M,res of one fused RMSNorm -> MXFP4 call (K = 5120), no JSON line")
     ap.add_argument("--calls", type=int, default=6)
     ap.add_argument("--copies", type=int, default=4)
     args = ap.parse_args()
@@ -637,6 +718,9 @@ def main():
         return
     if args.single_bmm:
         run_single_bmm(args)
+        return
+    if args.single_norm:
+        run_single_norm(args)
         return
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

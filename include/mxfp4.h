@@ -139,6 +139,40 @@ MXFP4_API mxfp4_status mxfp4_quant_act(const void* x_dev, int M, int K, int ldx,
                              mxfp4_layout layout, void* stream);
 
 /*
+ * Fused RMSNorm -> per-1x32 MXFP4 activation producer: the upstream
+ * normalization emits the GEMM's quantized input directly, the tuple input
+ * the pages' layer code takes "e.g. from fused RMSNorm" (PR #39598 blog
+ * analysis, section 2, apply_weights).  The pages do not print the
+ * normalization; it is RMSNorm (Zhang and Sennrich, 2019) with eps inside
+ * the root, applied row by row:
+ *   h = x                      (residual_dev == NULL), or
+ *   h = bf16_RNE(x + residual) (then written back into residual_dev);
+ *   y = bf16_RNE( h / sqrt(mean_k(h^2) + eps) * gamma )
+ * and y is quantized exactly as mxfp4_quant_act quantizes a bf16 input, so
+ * the result equals RMSNorm-to-bf16 followed by mxfp4_quant_act (up to the
+ * fp32 evaluation of y: squares and sums in fp32, 1/sqrt by the hardware
+ * reciprocal square root; y is within 1 bf16 ulp of the exact value).
+ *
+ *   x_dev         bf16 [M][ldx], ldx >= K
+ *   residual_dev  bf16 [M][ldr], ldr >= K, read and overwritten; or NULL
+ *   gamma_dev     bf16 [K]
+ *   eps           added to the mean square (>= 0)
+ *   codes_dev     mxfp4_act_code_bytes(M, K, layout) bytes (output)
+ *   scales_dev    mxfp4_act_scale_bytes(M, K, layout) bytes (output)
+ *   y_dev         bf16 [M][ldy], ldy >= K: the bf16 y that was quantized
+ *                 (output); or NULL
+ * K must be even.  y, codes and scales must not overlap the inputs.  Rows
+ * whose mean square leaves the fp32 range (RMS above about 2^63 or below
+ * about 2^-63) are outside the supported range.  Launched as a programmatic
+ * dependent of the previous kernel on the stream, like mxfp4_quant_act.
+ * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA.
+ */
+MXFP4_API mxfp4_status mxfp4_rmsnorm_quant_act(const void* x_dev, int ldx, void* residual_dev, int ldr,
+                                               const void* gamma_dev, float eps, int M, int K,
+                                               uint8_t* codes_dev, uint8_t* scales_dev, mxfp4_layout layout,
+                                               void* y_dev, int ldy, void* stream);
+
+/*
  * Workspace bytes mxfp4_gemm needs for this problem (any input form): room
  * for the quantized or re-laid-out activations and, for M > 64, the fp32
  * partial sums of output tiles split between thread blocks.  Its contents

@@ -18,7 +18,7 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 INCLUDE_DIR = os.path.join(os.path.dirname(PKG_DIR), "include")
 LIB_NAME = "libmxfp4_gb300.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
-SOURCES = ("quant.cu", "gemm.cu", "decode.cu", "bmm.cu", "capi.cu", "noalloc.cu")
+SOURCES = ("quant.cu", "norm_quant.cu", "gemm.cu", "decode.cu", "bmm.cu", "capi.cu", "noalloc.cu")
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -37,6 +37,7 @@ _SIGNATURES = {
     "mxfp4_act_code_bytes": (_sz, [_i, _i, _i]),
     "mxfp4_act_scale_bytes": (_sz, [_i, _i, _i]),
     "mxfp4_quant_act": (_i, [_p, _i, _i, _i, _p, _p, _i, _p]),
+    "mxfp4_rmsnorm_quant_act": (_i, [_p, _i, _p, _i, _p, ctypes.c_float, _i, _i, _p, _p, _i, _p, _i, _p]),
     "mxfp4_gemm_workspace_bytes": (_sz, [_i, _i, _i]),
     "mxfp4_gemm": (_i, [_p, _i, _p, _p, _i, _p, _p, _p, _i, _i, _i, _i, _p, _sz, _p]),
     "a16wfp4_bmm": (_i, [_p, _p, _p, _i, _i, _i, _i, _i, _p]),
@@ -96,6 +97,13 @@ def mxfp4_act_code_bytes(M: int, K: int, layout: int) -> int:
 
 def mxfp4_act_scale_bytes(M: int, K: int, layout: int) -> int:
     return lib.mxfp4_act_scale_bytes(M, K, layout)
+
+
+def mxfp4_rmsnorm_quant_act(x, ldx: int, residual, ldr: int, gamma, eps: float, M: int, K: int, codes, scales,
+                            layout: int, y=None, ldy: int = 0, stream=None) -> None:
+    _check(lib.mxfp4_rmsnorm_quant_act(_ptr(x), ldx, _ptr(residual), ldr, _ptr(gamma), eps, M, K, _ptr(codes),
+                                       _ptr(scales), layout, _ptr(y), ldy, _stream(stream)),
+           "mxfp4_rmsnorm_quant_act")
 
 
 def mxfp4_gemm_workspace_bytes(M: int, N: int, K: int) -> int:

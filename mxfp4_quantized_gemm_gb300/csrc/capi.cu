@@ -8,6 +8,7 @@
 
 #include "mxfp4.h"
 #include "internal.h"
+#include "norm_quant.h"
 
 namespace mx {
 
@@ -146,6 +147,25 @@ mxfp4_status mxfp4_quant_act(const void* x, int M, int K, int ldx, uint8_t* code
                                 static_cast<cudaStream_t>(stream)));
 }
 
+mxfp4_status mxfp4_rmsnorm_quant_act(const void* x, int ldx, void* residual, int ldr, const void* gamma, float eps,
+                                     int M, int K, uint8_t* codes, uint8_t* scales, mxfp4_layout layout, void* y,
+                                     int ldy, void* stream) {
+  if (x == nullptr || gamma == nullptr || codes == nullptr || scales == nullptr) return MXFP4_ERR_INVALID_ARG;
+  if (M <= 0 || K <= 0 || !(eps >= 0.f)) return MXFP4_ERR_INVALID_ARG;
+  if (layout != MXFP4_LAYOUT_ROWMAJOR && layout != MXFP4_LAYOUT_TILED) return MXFP4_ERR_INVALID_ARG;
+  if ((K & 1) || ldx < K || (residual != nullptr && ldr < K) || (y != nullptr && ldy < K))
+    return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  auto odd = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1) != 0; };
+  if (odd(x) || odd(gamma) || (residual != nullptr && odd(residual)) || (y != nullptr && odd(y)))
+    return MXFP4_ERR_MISALIGNED;
+  if (layout == MXFP4_LAYOUT_TILED && (!aligned16(codes) || !aligned16(scales))) return MXFP4_ERR_MISALIGNED;
+  DeviceInfo dev;
+  mxfp4_status st = device_ready(&dev);
+  if (st != MXFP4_OK) return st;
+  NormQuantProblem p{x, ldx, residual, ldr, gamma, eps, M, K, codes, scales, layout == MXFP4_LAYOUT_TILED, y, ldy};
+  return from_cuda(launch_rmsnorm_quant(p, dev, static_cast<cudaStream_t>(stream)));
+}
+
 size_t mxfp4_gemm_workspace_bytes(int M, int N, int K) {
   if (M <= 0 || N <= 0 || K <= 0 || (K & 1)) return 0;
   return gemm_workspace_layout(M, N, K, current_gemm_grid()).total;
@@ -268,7 +288,7 @@ mxfp4_status mxfp4_get_device_error(void* stream) {
   if (st != MXFP4_OK) return st;
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MXFP4_ERR_CUDA;
   const uint32_t err = quant_read_clear_error() | gemm_read_clear_error() | decode_read_clear_error() |
-                       bmm_read_clear_error();
+                       bmm_read_clear_error() | norm_read_clear_error();
   return (err & kErrTimeout) ? MXFP4_ERR_TIMEOUT : MXFP4_OK;
 }
 

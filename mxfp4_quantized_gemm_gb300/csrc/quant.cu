@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "act_store.cuh"
 #include "internal.h"
 #include "layout.cuh"
 #include "ptx.cuh"
@@ -32,7 +33,6 @@ __global__ void __launch_bounds__(256, 4) quant_kernel(const uint16_t* __restric
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int64_t units = static_cast<int64_t>(rows) * KT;
-  const int nb = (K + 31) >> 5;   // scale blocks per row
   // Launched as a programmatic dependent: let the GEMM behind this kernel
   // start its set-up and weight prefetch now, but touch memory only after the
   // kernel before this one (which may produce x or still read the outputs'
@@ -56,33 +56,9 @@ __global__ void __launch_bounds__(256, 4) quant_kernel(const uint16_t* __restric
       if (u >= units) break;     // warp-uniform
       const int r = static_cast<int>(u / KT);
       const int kt = static_cast<int>(u - static_cast<int64_t>(r) * KT);
-      const int e0 = kt * 256 + lane * 8;
       uint32_t sbyte;
       const uint32_t packed = quantize8(v[j], sbyte);
-
-      const int blk = kt * 8 + (lane >> 2);
-      const bool blk_real = r < M && blk < nb;
-      const int j0 = kt * 128 + lane * 4;   // first code byte of this lane in the row
-      if (kLayout == ActLayout::kTiled) {
-        *reinterpret_cast<uint32_t*>(codes + tiled_code_offset(r, j0, KT)) = packed;
-        if ((lane & 3) == 0)
-          scales[tiled_scale_offset(r, blk, KT)] = blk_real ? static_cast<uint8_t>(sbyte) : 0x7F;
-      } else if (kLayout == ActLayout::kBlocked) {
-        *reinterpret_cast<uint32_t*>(codes + blocked_code_offset(r, j0, KT, block_rows)) = packed;
-        if ((lane & 3) == 0)
-          codes[blocked_scale_offset(r, blk, KT, block_rows)] = blk_real ? static_cast<uint8_t>(sbyte) : 0x7F;
-      } else if (r < M) {
-        const int row_bytes = K >> 1;
-        uint8_t* dst = codes + static_cast<size_t>(r) * row_bytes + j0;
-        if (e0 + 8 <= K && (reinterpret_cast<uintptr_t>(dst) & 3) == 0) {
-          *reinterpret_cast<uint32_t*>(dst) = packed;
-        } else {
-#pragma unroll
-          for (int b = 0; b < 4; ++b)
-            if (j0 + b < row_bytes) dst[b] = static_cast<uint8_t>(packed >> (8 * b));
-        }
-        if ((lane & 3) == 0 && blk_real) scales[static_cast<size_t>(r) * nb + blk] = static_cast<uint8_t>(sbyte);
-      }
+      store_act8<kLayout>(codes, scales, r, M, K, KT, block_rows, kt * 32 + lane, (lane & 3) == 0, packed, sbyte);
     }
   }
 }

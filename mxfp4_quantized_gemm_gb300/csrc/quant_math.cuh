@@ -2,8 +2,8 @@
 // pages' per_1x32_f4_quant implements (sglang PR #39598 blog analysis,
 // section 2): one E8M0 scale per 32 K-elements with exponent
 // floor(log2 amax) - 2, elements rounded to the nearest E2M1 value (ties to
-// even) and saturated at +-6.  Shared by the standalone quantizer and the
-// GEMM's fused activation quantization.
+// even) and saturated at +-6.  Shared by the standalone quantizer, the
+// GEMM's fused activation quantization and the fused RMSNorm producer.
 #pragma once
 
 #include <cstdint>
@@ -37,10 +37,12 @@ __device__ __forceinline__ uint4 load8_words(const uint16_t* __restrict__ x, int
 //
 // amax: bf16 magnitudes order like unsigned integers (Inf and NaN above
 // every finite value), so a SIMD max over the sign-cleared halves finds it.
-// Each value is multiplied by 2^(127 - sbyte), exact in fp32 (the power is
-// a normal float and no flush to zero applies), and the hardware E2M1
-// conversion rounds to nearest, ties to even, saturating at 6; a value that
-// rounds to zero keeps its sign (-0 encodes as 0x8).
+// Each value is multiplied by 2^(127 - sbyte) with the mixed-precision
+// bf16 x bf16 -> f32 FMA (adding -0 keeps the product's sign): the product of
+// a bf16 value and a power of two is exact in fp32 (the power is a normal
+// number and no flush to zero applies).  The hardware E2M1 conversion then
+// rounds to nearest, ties to even, saturating at 6; a value that rounds to
+// zero keeps its sign (-0 encodes as 0x8).
 __device__ __forceinline__ uint32_t quantize8_words(uint4 v, uint32_t& sbyte) {
   const uint32_t m2 = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
                                __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
@@ -51,21 +53,32 @@ __device__ __forceinline__ uint32_t quantize8_words(uint4 v, uint32_t& sbyte) {
   const bool nonfinite = ef == 0xFF;
   // floor(log2 amax) - 2 as an E8M0 byte, clamped at 0 (zero / subnormal amax)
   sbyte = nonfinite ? 0xFFu : (ef > 2 ? ef - 2 : 0u);
-  const float inv = __uint_as_float((254u - (nonfinite ? 0u : sbyte)) << 23);   // 2^(127 - sbyte)
-  const float f0 = __uint_as_float(v.x << 16) * inv, f1 = __uint_as_float(v.x & 0xFFFF0000u) * inv;
-  const float f2 = __uint_as_float(v.y << 16) * inv, f3 = __uint_as_float(v.y & 0xFFFF0000u) * inv;
-  const float f4 = __uint_as_float(v.z << 16) * inv, f5 = __uint_as_float(v.z & 0xFFFF0000u) * inv;
-  const float f6 = __uint_as_float(v.w << 16) * inv, f7 = __uint_as_float(v.w & 0xFFFF0000u) * inv;
+  const uint32_t inv = (254u - (nonfinite ? 0u : sbyte)) << 7;   // bf16 bits of 2^(127 - sbyte)
   uint32_t packed;
   // cvt.rn.satfinite.e2m1x2.f32 d, a, b puts a in the high nibble, b in the low.
-  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+  asm("{\n\t.reg .b16 s, l0, h0, l1, h1, l2, h2, l3, h3;\n\t"
+      ".reg .f32 f0, f1, f2, f3, f4, f5, f6, f7;\n\t"
+      ".reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.u16.u32 s, %5;\n\t"
+      "mov.b32 {l0, h0}, %1;\n\t"
+      "mov.b32 {l1, h1}, %2;\n\t"
+      "mov.b32 {l2, h2}, %3;\n\t"
+      "mov.b32 {l3, h3}, %4;\n\t"
+      "fma.rn.f32.bf16 f0, l0, s, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 f1, h0, s, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 f2, l1, s, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 f3, h1, s, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 f4, l2, s, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 f5, h2, s, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 f6, l3, s, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 f7, h3, s, 0f80000000;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, f1, f0;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, f3, f2;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, f5, f4;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, f7, f6;\n\t"
       "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
       : "=r"(packed)
-      : "f"(f0), "f"(f1), "f"(f2), "f"(f3), "f"(f4), "f"(f5), "f"(f6), "f"(f7));
+      : "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(inv));
   return nonfinite ? 0u : packed;
 }
 

@@ -13,6 +13,7 @@ including the pages' flattening of 3-D activations to 2-D for the GEMM.
 
     torch.ops.mxfp4.pack_weights(codes, scales, K) -> packed
     torch.ops.mxfp4.quant_act(x, layout) -> (codes, scales)
+    torch.ops.mxfp4.rmsnorm_quant_act(x, gamma, eps, layout, residual) -> (codes, scales)   # residual updated
     torch.ops.mxfp4.linear(x, w_packed, bias, N) -> out          # x [..., K] bf16
     torch.ops.mxfp4.linear_prequant(codes, scales, layout, w_packed, bias, M, N, K) -> out
     torch.ops.mxfp4.a16wfp4_bmm(x, w_packed, N, batch_major) -> out
@@ -123,6 +124,45 @@ def quant_act(x: Tensor, layout: int) -> tuple[Tensor, Tensor]:
 @quant_act.register_fake
 def _(x, layout):
     _check_args("mxfp4::quant_act", x, dtypes=(torch.bfloat16,))
+    K = x.shape[-1]
+    M = x.numel() // K
+    nc, ns = _act_bytes(M, K, layout)
+    if layout == LAYOUT_ROWMAJOR:
+        return x.new_empty(M, K // 2, dtype=torch.uint8), x.new_empty(M, _cdiv(K, 32), dtype=torch.uint8)
+    return x.new_empty(nc, dtype=torch.uint8), x.new_empty(ns, dtype=torch.uint8)
+
+
+# --------------------------------------------- fused RMSNorm -> quantizer
+@custom_op("mxfp4::rmsnorm_quant_act", mutates_args=("residual",))
+def rmsnorm_quant_act(x: Tensor, gamma: Tensor, eps: float, layout: int,
+                      residual: Optional[Tensor]) -> tuple[Tensor, Tensor]:
+    """RMSNorm of x [..., K] (or of x + residual, stored back into residual)
+    times gamma, quantized per 1x32 like quant_act; returns (codes, scales)."""
+    _check_args("mxfp4::rmsnorm_quant_act", x, gamma, residual,
+                dtypes=(torch.bfloat16, torch.bfloat16, torch.bfloat16))
+    c = _capi()
+    K = x.shape[-1]
+    x2 = x.reshape(-1, K).contiguous()
+    M = x2.shape[0]
+    res2 = None
+    if residual is not None:
+        torch._check(residual.is_contiguous() and residual.shape == x.shape,
+                     lambda: "mxfp4::rmsnorm_quant_act: residual must be contiguous and shaped like x")
+        res2 = residual.view(M, K)
+    nc, ns = _act_bytes(M, K, layout)
+    codes = torch.empty(nc, dtype=torch.uint8, device=x.device)
+    scales = torch.empty(ns, dtype=torch.uint8, device=x.device)
+    c.mxfp4_rmsnorm_quant_act(x2, K, res2, K, gamma.contiguous(), eps, M, K, codes, scales, layout, None, 0,
+                              _stream(x))
+    if layout == LAYOUT_ROWMAJOR:
+        return codes.view(M, K // 2), scales.view(M, _cdiv(K, 32))
+    return codes, scales
+
+
+@rmsnorm_quant_act.register_fake
+def _(x, gamma, eps, layout, residual):
+    _check_args("mxfp4::rmsnorm_quant_act", x, gamma, residual,
+                dtypes=(torch.bfloat16, torch.bfloat16, torch.bfloat16))
     K = x.shape[-1]
     M = x.numel() // K
     nc, ns = _act_bytes(M, K, layout)

@@ -14,6 +14,8 @@ Recipes (stand-ins for the pages' model checkpoints, which are not available):
 * weights: FP4 codes uniform over all 16 nibbles (two per byte), E8M0 scale
   bytes 127 + U{lo..hi};
 * bias: N(0, 0.1) rounded to bfloat16;
+* RMSNorm weights: uniform in [0.25, 2) rounded to bfloat16; residual
+  stream: N(0, 16) rounded to bfloat16;
 * edge rows: all +0, all -0, blocks whose largest magnitude is exactly 2**k or
   the bfloat16 just below it, blocks holding every rounding tie, blocks with
   values in (6, 8) times a power of two, and blocks of bfloat16 subnormals.
@@ -72,6 +74,16 @@ def weight_scales(N: int, K: int, lo: int, hi: int, seed: int, tensor_id: int = 
 def bias(N: int, seed: int, tensor_id: int = 4, sigma: float = 0.1) -> np.ndarray:
     g = rng(seed, tensor_id)
     return f32_to_bf16_bits(g.standard_normal(N, dtype=np.float32) * np.float32(sigma))
+
+
+def norm_gamma(K: int, seed: int, tensor_id: int = 7) -> np.ndarray:
+    """bf16 bits [K] of RMSNorm weights, uniform in [0.25, 2)."""
+    return f32_to_bf16_bits(rng(seed, tensor_id).uniform(0.25, 2.0, K).astype(np.float32))
+
+
+def residual(M: int, K: int, seed: int, tensor_id: int = 8, sigma: float = 4.0) -> np.ndarray:
+    """bf16 bits [M, K] of a residual stream, N(0, sigma^2)."""
+    return f32_to_bf16_bits(rng(seed, tensor_id).standard_normal((M, K), dtype=np.float32) * np.float32(sigma))
 
 
 def bmm_activations(B: int, M: int, K: int, seed: int, tensor_id: int = 5) -> np.ndarray:

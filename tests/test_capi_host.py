@@ -94,6 +94,35 @@ def test_argument_checks_precede_any_launch(capi):
     assert lib.mxfp4_gemm(A, 64, None, None, 0, A + 2, None, A, 8, 4, 8, 64, A, ws, None) == capi.ERR_MISALIGNED
 
 
+def test_rmsnorm_quant_argument_checks(capi):
+    lib, A = capi.lib, 1 << 20
+    f = lib.mxfp4_rmsnorm_quant_act
+    ok = (A, 64, None, 0, A, 1e-6, 4, 64, A, A, 1, None, 0, None)
+
+    def call(**kw):
+        names = ("x", "ldx", "res", "ldr", "gamma", "eps", "M", "K", "codes", "scales", "layout", "y", "ldy", "s")
+        args = dict(zip(names, ok))
+        args.update(kw)
+        return f(*args.values())
+
+    assert call(x=None) == capi.ERR_INVALID_ARG
+    assert call(gamma=None) == capi.ERR_INVALID_ARG
+    assert call(scales=None) == capi.ERR_INVALID_ARG
+    assert call(M=0) == capi.ERR_INVALID_ARG
+    assert call(eps=-1.0) == capi.ERR_INVALID_ARG
+    assert call(eps=float("nan")) == capi.ERR_INVALID_ARG
+    assert call(layout=2) == capi.ERR_INVALID_ARG
+    assert call(K=63, ldx=64) == capi.ERR_UNSUPPORTED_SHAPE
+    assert call(ldx=32) == capi.ERR_UNSUPPORTED_SHAPE
+    assert call(res=A, ldr=8) == capi.ERR_UNSUPPORTED_SHAPE
+    assert call(y=A, ldy=8) == capi.ERR_UNSUPPORTED_SHAPE
+    assert call(x=A + 1) == capi.ERR_MISALIGNED
+    assert call(gamma=A + 1) == capi.ERR_MISALIGNED
+    assert call(codes=A + 4) == capi.ERR_MISALIGNED          # TILED wants 16-byte alignment
+    if not torch.cuda.is_available():
+        assert call(codes=A + 4, layout=0) in (capi.ERR_NO_DEVICE, capi.ERR_CUDA)
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device answer")
 def test_valid_call_without_device_reports_no_device(capi):
     A = 1 << 20

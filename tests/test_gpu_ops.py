@@ -89,6 +89,22 @@ def test_prequant_op_matches_fused(capi, M, layout):
     assert torch.equal(y, torch.ops.mxfp4.linear(xd, packed, bd, N))
 
 
+def test_rmsnorm_quant_op_matches_capi(capi):
+    M, K = 6, 5120
+    x = dev_bf16(synth.activations(M, K, seed=21)).view(2, 3, K)
+    gamma = dev_bf16(synth.norm_gamma(K, seed=21))
+    res0 = dev_bf16(synth.residual(M, K, seed=21)).view(2, 3, K)
+    res = res0.clone()
+    codes, scales = torch.ops.mxfp4.rmsnorm_quant_act(x, gamma, 1e-6, 1, res)
+    res2 = res0.clone().view(M, K)
+    c2 = torch.empty_like(codes)
+    s2 = torch.empty_like(scales)
+    capi.mxfp4_rmsnorm_quant_act(x.view(M, K), K, res2, K, gamma, 1e-6, M, K, c2, s2, 1)
+    torch.cuda.synchronize()
+    assert torch.equal(codes, c2) and torch.equal(scales, s2) and torch.equal(res.view(M, K), res2)
+    assert not torch.equal(res, res0)
+
+
 @pytest.mark.parametrize("batch_major", [False, True])
 def test_bmm_op_matches_capi(capi, batch_major):
     B, M, N, K = 16, 40, 512, 192

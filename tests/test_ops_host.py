@@ -46,6 +46,13 @@ def test_prequant_and_bmm_shapes():
     assert torch.ops.mxfp4.a16wfp4_bmm(x, packed_meta(16, 128, 512), 128, True).shape == (40, 16, 128)
 
 
+def test_rmsnorm_quant_shapes():
+    c, s = torch.ops.mxfp4.rmsnorm_quant_act(meta(2, 3, 5120), meta(5120), 1e-6, ops.LAYOUT_TILED, meta(2, 3, 5120))
+    assert c.numel() == 128 * 5120 // 2 and s.numel() == 128 * 5120 // 32
+    c, s = torch.ops.mxfp4.rmsnorm_quant_act(meta(7, 100), meta(100), 1e-6, ops.LAYOUT_ROWMAJOR, None)
+    assert c.shape == (7, 50) and s.shape == (7, 4)
+
+
 def test_pack_weights_shape():
     w = torch.ops.mxfp4.pack_weights(meta(3, 300, 256, dtype=U8), meta(3, 300, 16, dtype=U8), 512)
     assert w.numel() == 3 * 2 * 2 * 34816
