@@ -140,9 +140,10 @@ MXFP4_API mxfp4_status mxfp4_quant_act(const void* x_dev, int M, int K, int ldx,
 
 /*
  * Fused RMSNorm -> per-1x32 MXFP4 activation producer: the upstream
- * normalization emits the GEMM's quantized input directly, the tuple input
- * the pages' layer code takes "e.g. from fused RMSNorm" (PR #39598 blog
- * analysis, section 2, apply_weights).  The pages do not print the
+ * normalization emits the GEMM's quantized input directly.  The pages' layer
+ * code accepts such a pre-quantized (codes, scales) tuple and names a fused
+ * RMSNorm as one source of it (PR #39598 blog analysis, section 2,
+ * apply_weights).  The pages do not print the
  * normalization; it is RMSNorm (Zhang and Sennrich, 2019) with eps inside
  * the root, applied row by row:
  *   h = x                      (residual_dev == NULL), or

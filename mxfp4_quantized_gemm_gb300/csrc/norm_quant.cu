@@ -1,7 +1,7 @@
 // Fused RMSNorm -> per-1x32 MXFP4 activation producer: the kernel that hands
-// the GEMM its input already quantized, the tuple input the pages' layer code
-// accepts "e.g. from fused RMSNorm" (sglang PR #39598 blog analysis,
-// section 2, apply_weights).  The pages do not print the normalization; it is
+// the GEMM its input already quantized.  The pages' layer code accepts such a
+// (codes, scales) tuple and names a fused RMSNorm as one source of it (sglang
+// PR #39598 blog analysis, section 2, apply_weights).  The pages do not print the normalization; it is
 // RMSNorm as Zhang and Sennrich (2019) define it, eps inside the root:
 //   h = x, or bf16(x + residual) (then also stored as the new residual),
 //   y = bf16(h / sqrt(mean(h^2) + eps) * gamma),
@@ -9,23 +9,25 @@
 // (quant_math.cuh), so the producer equals RMSNorm-to-bf16 followed by
 // mxfp4_quant_act.
 //
-// One CTA of 256 threads per row (grid-stride over rows).  A thread owns the
-// 8-element chunks c = tid + 256 i; four consecutive lanes hold one 32-element
-// scale block.  Pass 1 takes the row (with the residual: adds, rounds, stores
-// the sum) and sums squares; one block reduction gives 1/rms; pass 2 scales by
-// gamma, rounds to bf16 and quantizes.
+// One CTA per row (grid-stride over rows); four consecutive lanes hold one
+// 32-element scale block.  Pass 1 takes the row (with the residual: adds,
+// rounds, stores the sum) and sums squares; one block reduction gives 1/rms;
+// pass 2 multiplies by gamma and 1/rms, rounds to bf16 and quantizes.
 //   rmsnorm_quant_tma_kernel (K <= 8192, K % 8 == 0, 16-byte aligned rows):
-//     one thread keeps the CTA's next rows in flight as 1-D bulk copies into a
-//     4-stage shared-memory ring (x row, then the residual row), so the
-//     loads of later rows overlap the reduction and quantization of this
-//     one; a stage is refilled right after the row's reduction barrier.
-//   rmsnorm_quant_kernel<kRegs = true> (other rows with K <= 8192): plain
-//     vector loads into registers; x is read from HBM once.
+//     thread 0 keeps the CTA's next row in flight as 1-D bulk copies into a
+//     2-stage shared-memory ring (x row, then the residual row), refilling a
+//     stage right after the row's reduction barrier, so loads overlap the
+//     quantization of the row before.  The CTA is sized to the row: each
+//     thread owns 2 (up to 256 rows: shorter rows of work) or 4 (more rows:
+//     per-row work spread over more elements) 8-element chunks.
+//   rmsnorm_quant_kernel<kRegs = true> (other rows with K <= 8192): 256
+//     threads, plain vector loads into registers; x is read from HBM once.
 //   rmsnorm_quant_kernel<kRegs = false> (K > 8192): pass 2 reads the row
 //     again, from L2.
-// Squares and sums are fp32: rows whose mean square leaves the fp32 range
-// (RMS beyond about 2^63 or below about 2^-63) are outside the supported
-// range.
+// The element arithmetic uses the Blackwell mixed-precision FMA (bf16 x bf16
+// -> f32): squares and h * gamma are exact products.  Squares and sums are
+// fp32: rows whose mean square leaves the fp32 range (RMS beyond about 2^63
+// or below about 2^-63) are outside the supported range.
 #include <cuda_runtime.h>
 
 #include <atomic>

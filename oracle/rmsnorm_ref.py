@@ -4,9 +4,10 @@ TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports this module:
 only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may call it.  It shares no code with the CUDA path.
 
-The pages let the GEMM take its activations already quantized, "e.g. from
-fused RMSNorm" (sglang PR #39598 blog analysis, section 2, apply_weights:
-the tuple input), but print neither the normalization nor its rounding.  The
+The pages let the GEMM take its activations already quantized and name a
+fused RMSNorm as one producer of that (codes, scales) tuple (sglang PR #39598
+blog analysis, section 2, apply_weights), but print neither the
+normalization nor its rounding.  The
 plainest reading, used here and listed in the design doc:
 
 * RMSNorm as defined by Zhang and Sennrich (2019), with the usual epsilon
