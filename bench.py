@@ -29,6 +29,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -120,7 +121,9 @@ class ClockSampler:
     def __init__(self, device_index: int):
         self.idx = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        # raw samples: $BENCH_CLOCK_DIR/clocks_<pid>.csv if set, else a temporary file
+        d = os.environ.get("BENCH_CLOCK_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(d, f"clocks_{os.getpid()}.csv")
 
     def start(self):
         try:

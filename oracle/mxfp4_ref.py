@@ -29,7 +29,7 @@ Everything here is written in float64 numpy, straight from the definitions:
   absorbed BMM" (Modifications): bf16 activations against FP4 weights with
   E8M0 scales, the V-up output written batch-major ``[M, B, N]``.
 
-Readings where the pages are silent (each listed in the design doc):
+Readings where the pages are silent:
 
 * nibble order: element 2j in the low nibble, element 2j+1 in the high nibble
   of byte j;

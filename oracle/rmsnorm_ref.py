@@ -7,8 +7,7 @@ only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 The pages let the GEMM take its activations already quantized and name a
 fused RMSNorm as one producer of that (codes, scales) tuple (sglang PR #39598
 blog analysis, section 2, apply_weights), but print neither the
-normalization nor its rounding.  The
-plainest reading, used here and listed in the design doc:
+normalization nor its rounding.  The plainest reading, used here:
 
 * RMSNorm as defined by Zhang and Sennrich (2019), with the usual epsilon
   inside the root:  y_i = h_i / sqrt(mean_j(h_j**2) + eps) * gamma_i;
