@@ -367,6 +367,7 @@ def run_ours(args, world, rank, local):
         extra["prefill"] = run_prefill(args, torch, np, capi, synth, dev, stream, bf16_peak, peak_src)
         extra["bmm"] = run_bmm(args, torch, np, capi, synth, dev, stream, hbm_peak, bf16_sust)
         extra["rmsnorm_quant"] = run_norm_quant(args, torch, np, capi, synth, dev, stream, hbm_peak)
+        extra["gemm_mxfp4_out"] = run_mxfp4_out(args, torch, np, capi, synth, dev, stream, hbm_peak)
 
     line = {
         "metric": METRIC,
@@ -506,6 +507,65 @@ def run_bmm(args, torch, np, capi, synth, dev, stream, hbm_peak, bf16_sust):
     return {"metric": "A16WFP4 MLA absorbed BMM GB/s, B=64, M in {16, 4096}", "value": round(gbs, 1),
             "unit": "GB/s", "peak": hbm_peak, "frac": round(gbs / hbm_peak, 4), "cases": res,
             "l2": "back-to-back calls; x and out exceed L2 at M=4096"}
+
+
+def run_mxfp4_out(args, torch, np, capi, synth, dev, stream, hbm_peak):
+    """mxfp4_gemm_mxfp4_out against mxfp4_gemm (bf16 out) on decode and prefill
+    shapes (bf16 activations, N = 14336, K = 5120, no bias); 4 weight copies
+    rotate so that every call reads its weights from HBM; 20 calls replay from
+    a CUDA graph."""
+    sptr = stream.cuda_stream
+    N, K, copies, reps = 14336, 5120, 4, 20
+    wc = synth.weight_codes(N, K, seed=0)
+    ws = synth.weight_scales(N, K, *W_SCALE_DECODE, seed=0)
+    pk0 = torch.empty(capi.mxfp4_packed_weight_bytes(1, N, K), dtype=torch.uint8, device=dev)
+    capi.mxfp4_pack_weights(torch.from_numpy(wc).to(dev), torch.from_numpy(ws).to(dev), 1, N, K, pk0)
+    pks = [pk0] + [pk0.clone() for _ in range(copies - 1)]
+    res = {}
+    for M in (1, 16, 64, 8192):
+        x = synth.bf16_tensor(synth.activations(M, K, seed=M, outlier_frac=0.01)).to(dev)
+        wsb = capi.mxfp4_gemm_workspace_bytes(M, N, K)
+        work = torch.zeros(max(wsb, 1), dtype=torch.uint8, device=dev)
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        codes = torch.empty(M, N // 2, dtype=torch.uint8, device=dev)
+        scales = torch.empty(M, N // 32, dtype=torch.uint8, device=dev)
+        times = {}
+        for mode in ("bf16", "mxfp4"):
+            def call(i):
+                if mode == "bf16":
+                    capi.mxfp4_gemm(x, K, None, None, 0, pks[i % copies], None, out, N, M, N, K, work, wsb, sptr)
+                else:
+                    capi.mxfp4_gemm_mxfp4_out(x, K, None, None, 0, pks[i % copies], None, codes, scales, M, N, K,
+                                              work, wsb, sptr)
+            with torch.cuda.stream(stream):
+                for i in range(3):
+                    call(i)
+            stream.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(stream):
+                with torch.cuda.graph(graph, stream=stream):
+                    for i in range(reps):
+                        call(i)
+            stream.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                graph.replay()
+                a.record(stream)
+                graph.replay()
+                b.record(stream)
+            stream.synchronize()
+            assert capi.mxfp4_get_device_error(sptr) == capi.OK
+            times[mode] = a.elapsed_time(b) / reps
+            del graph
+        out_bytes = M * N // 2 + M * N // 32
+        nbytes = N * K / 2 + N * K / 32 + 2 * M * K + out_bytes
+        res[f"M{M}"] = {"us_bf16_out": round(times["bf16"] * 1e3, 2), "us_mxfp4_out": round(times["mxfp4"] * 1e3, 2),
+                        "gbs_mxfp4_out": round(nbytes / (times["mxfp4"] * 1e-3) / 1e9, 1),
+                        "tflops_mxfp4_out": round(2.0 * M * N * K / (times["mxfp4"] * 1e-3) / 1e12, 1)}
+    return {"metric": "W4A4 GEMM with MXFP4 output epilogue vs bf16 output, N = 14336, K = 5120",
+            "unit": "us per call", "cases": res,
+            "bytes_per_launch": "N*K/2 + N*K/32 (packed W) + 2*M*K (bf16 A) + M*N/2 + M*N/32 (MXFP4 out)",
+            "l2": "4 rotating weight copies; 20 calls replayed from a CUDA graph"}
 
 
 def run_norm_quant(args, torch, np, capi, synth, dev, stream, hbm_peak):

@@ -218,6 +218,30 @@ MXFP4_API mxfp4_status mxfp4_gemm(const void* a_bf16_dev, int lda,
                         void* workspace_dev, size_t workspace_bytes, void* stream);
 
 /*
+ * The same GEMM with an MXFP4 output epilogue: the result, computed and
+ * rounded to bf16 exactly as mxfp4_gemm computes it, is quantized per 1x32
+ * along N by the rule of mxfp4_quant_act, for the next layer to take as its
+ * pre-quantized input.  The pages list a fused MXFP4 output epilogue among
+ * the companion changes of their test stack ("[AMD] Add opt-in AITER ASM
+ * FP4 GEMM for Quark dense linear", Setup & Environment, companion PR
+ * #39912) without printing it; the plainest reading is taken: the bytes
+ * equal mxfp4_gemm's bf16 output passed through mxfp4_quant_act (ROWMAJOR).
+ *
+ *   out_codes_dev   [M][N/2] uint8, row-major (output)
+ *   out_scales_dev  [M][ceil(N/32)] uint8, row-major (output)
+ * The activation, weight, bias and workspace arguments are mxfp4_gemm's
+ * (mxfp4_gemm_workspace_bytes sizes the workspace).  N must be even.  No
+ * alignment is required of the outputs (16-byte aligned rows store faster).
+ * Errors: those of mxfp4_gemm.
+ */
+MXFP4_API mxfp4_status mxfp4_gemm_mxfp4_out(const void* a_bf16_dev, int lda,
+                                            const uint8_t* a_codes_dev, const uint8_t* a_scales_dev,
+                                            mxfp4_layout a_layout, const void* w_packed_dev,
+                                            const void* bias_dev, uint8_t* out_codes_dev,
+                                            uint8_t* out_scales_dev, int M, int N, int K,
+                                            void* workspace_dev, size_t workspace_bytes, void* stream);
+
+/*
  * A16WFP4 batched matmul for the MLA absorbed K-up / V-up projections
  * (PR #34317, Modifications): bf16 activations against FP4 weights with E8M0
  * scales, no activation quantization:

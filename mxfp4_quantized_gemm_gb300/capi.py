@@ -40,6 +40,7 @@ _SIGNATURES = {
     "mxfp4_rmsnorm_quant_act": (_i, [_p, _i, _p, _i, _p, ctypes.c_float, _i, _i, _p, _p, _i, _p, _i, _p]),
     "mxfp4_gemm_workspace_bytes": (_sz, [_i, _i, _i]),
     "mxfp4_gemm": (_i, [_p, _i, _p, _p, _i, _p, _p, _p, _i, _i, _i, _i, _p, _sz, _p]),
+    "mxfp4_gemm_mxfp4_out": (_i, [_p, _i, _p, _p, _i, _p, _p, _p, _p, _i, _i, _i, _p, _sz, _p]),
     "a16wfp4_bmm": (_i, [_p, _p, _p, _i, _i, _i, _i, _i, _p]),
     "mxfp4_get_device_error": (_i, [_p]),
     "mxfp4_gemm_noalloc": (_i, [_p, _i, _p, _p, _p, _i, _i, _i, _i, _p]),
@@ -126,6 +127,14 @@ def mxfp4_gemm(a_bf16, lda: int, a_codes, a_scales, a_layout: int, w_packed, bia
                           _ptr(bias), _ptr(out), ldo, M, N, K, _ptr(workspace), workspace_bytes,
                           _stream(stream)),
            "mxfp4_gemm")
+
+
+def mxfp4_gemm_mxfp4_out(a_bf16, lda: int, a_codes, a_scales, a_layout: int, w_packed, bias, out_codes,
+                         out_scales, M: int, N: int, K: int, workspace, workspace_bytes: int, stream=None) -> None:
+    _check(lib.mxfp4_gemm_mxfp4_out(_ptr(a_bf16), lda, _ptr(a_codes), _ptr(a_scales), a_layout, _ptr(w_packed),
+                                    _ptr(bias), _ptr(out_codes), _ptr(out_scales), M, N, K, _ptr(workspace),
+                                    workspace_bytes, _stream(stream)),
+           "mxfp4_gemm_mxfp4_out")
 
 
 def a16wfp4_bmm(x, w_packed, out, B: int, M: int, N: int, K: int, out_layout: int, stream=None) -> None:

@@ -171,18 +171,25 @@ size_t mxfp4_gemm_workspace_bytes(int M, int N, int K) {
   return gemm_workspace_layout(M, N, K, current_gemm_grid()).total;
 }
 
-mxfp4_status mxfp4_gemm(const void* a_bf16, int lda, const uint8_t* a_codes, const uint8_t* a_scales,
-                        mxfp4_layout a_layout, const void* w_packed, const void* bias, void* out, int ldo, int M,
-                        int N, int K, void* workspace, size_t workspace_bytes, void* stream) {
-  if (w_packed == nullptr || out == nullptr) return MXFP4_ERR_INVALID_ARG;
+// The GEMM behind mxfp4_gemm (bf16 `out`) and mxfp4_gemm_mxfp4_out
+// (qcodes / qscales set, `out` unused).
+static mxfp4_status gemm_any(const void* a_bf16, int lda, const uint8_t* a_codes, const uint8_t* a_scales,
+                             mxfp4_layout a_layout, const void* w_packed, const void* bias, void* out, int ldo,
+                             uint8_t* qcodes, uint8_t* qscales, int M, int N, int K, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+  const bool quant_out = qcodes != nullptr;
+  if (w_packed == nullptr || (!quant_out && out == nullptr) || (quant_out && qscales == nullptr))
+    return MXFP4_ERR_INVALID_ARG;
   if (M <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_INVALID_ARG;
+  if (quant_out && (N & 1)) return MXFP4_ERR_UNSUPPORTED_SHAPE;
   const bool from_bf16 = a_bf16 != nullptr;
   if (from_bf16 && (a_codes != nullptr || a_scales != nullptr)) return MXFP4_ERR_INVALID_ARG;
   if (!from_bf16 && (a_codes == nullptr || a_scales == nullptr)) return MXFP4_ERR_INVALID_ARG;
   if (!from_bf16 && a_layout != MXFP4_LAYOUT_ROWMAJOR && a_layout != MXFP4_LAYOUT_TILED)
     return MXFP4_ERR_INVALID_ARG;
-  if ((K & 1) || ldo < N || (from_bf16 && lda < K)) return MXFP4_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned16(w_packed) || !aligned16(out) || (bias != nullptr && (reinterpret_cast<uintptr_t>(bias) & 1)))
+  if ((K & 1) || (!quant_out && ldo < N) || (from_bf16 && lda < K)) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(w_packed) || (!quant_out && !aligned16(out)) ||
+      (bias != nullptr && (reinterpret_cast<uintptr_t>(bias) & 1)))
     return MXFP4_ERR_MISALIGNED;
   if (from_bf16 && (reinterpret_cast<uintptr_t>(a_bf16) & 1)) return MXFP4_ERR_MISALIGNED;
   if (!from_bf16 && a_layout == MXFP4_LAYOUT_TILED && (!aligned16(a_codes) || !aligned16(a_scales)))
@@ -215,6 +222,8 @@ mxfp4_status mxfp4_gemm(const void* a_bf16, int lda, const uint8_t* a_codes, con
     d.M = M;
     d.N = N;
     d.K = K;
+    d.qcodes = qcodes;
+    d.qscales = qscales;
     if (from_bf16 && M <= kDecodeLocalQuantMaxM) {
       d.x = a_bf16;   // quantized inside the GEMM kernel
       d.ldx = lda;
@@ -263,9 +272,27 @@ mxfp4_status mxfp4_gemm(const void* a_bf16, int lda, const uint8_t* a_codes, con
   p.M = M;
   p.N = N;
   p.K = K;
+  p.qcodes = qcodes;
+  p.qscales = qscales;
   p.workspace = ws + wl.streamk_off;
   p.workspace_bytes = wl.total - wl.streamk_off;
   return from_cuda(launch_gemm(p, dev, s));
+}
+
+mxfp4_status mxfp4_gemm(const void* a_bf16, int lda, const uint8_t* a_codes, const uint8_t* a_scales,
+                        mxfp4_layout a_layout, const void* w_packed, const void* bias, void* out, int ldo, int M,
+                        int N, int K, void* workspace, size_t workspace_bytes, void* stream) {
+  return gemm_any(a_bf16, lda, a_codes, a_scales, a_layout, w_packed, bias, out, ldo, nullptr, nullptr, M, N, K,
+                  workspace, workspace_bytes, stream);
+}
+
+mxfp4_status mxfp4_gemm_mxfp4_out(const void* a_bf16, int lda, const uint8_t* a_codes, const uint8_t* a_scales,
+                                  mxfp4_layout a_layout, const void* w_packed, const void* bias, uint8_t* out_codes,
+                                  uint8_t* out_scales, int M, int N, int K, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  if (out_codes == nullptr || out_scales == nullptr) return MXFP4_ERR_INVALID_ARG;
+  return gemm_any(a_bf16, lda, a_codes, a_scales, a_layout, w_packed, bias, nullptr, 0, out_codes, out_scales, M, N,
+                  K, workspace, workspace_bytes, stream);
 }
 
 mxfp4_status a16wfp4_bmm(const void* x, const void* w_packed, void* out, int B, int M, int N, int K,

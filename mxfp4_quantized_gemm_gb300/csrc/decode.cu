@@ -74,7 +74,65 @@ __device__ __forceinline__ uint32_t partial_off(int r, int q) {
   return static_cast<uint32_t>(r) * 1024u + ((static_cast<uint32_t>(q) ^ (r & 7)) << 4);
 }
 
-template <int kRowsA>
+// MXFP4 output of a split tile (the cluster sum's other form): the CTA of
+// rank `rank` takes 32-column blocks [8 rank / S, 8 (rank + 1) / S); 8
+// consecutive lanes share one (row, block), lane `sub` summing its 4 columns
+// 4 sub.. over the S parts in rank order (the sums of the bf16 path, in the
+// same order), and quantize it together.  Whole warps loop, so every lane
+// takes part in the shuffles.  Called by warps 2..9.
+__device__ __forceinline__ void split_sum_store_q(const OutView o, int M, int S, int rank, uint32_t pbase, int n0) {
+  const int b_lo = rank * 8 / S, nbk = (rank + 1) * 8 / S - b_lo;
+  const int total = M * nbk * 8;
+  const int lane = threadIdx.x & 31;
+  const uint16_t* bias = reinterpret_cast<const uint16_t*>(o.bias);
+  for (int base = (threadIdx.x - 64) & ~31; base < total; base += kEpiThreads) {
+    const int gi = base + lane;
+    const bool act = gi < total;
+    const int unit = gi >> 3, sub = gi & 7;
+    const int r = act ? unit / nbk : 0, bb = b_lo + (act ? unit % nbk : 0);
+    const int n = n0 + 32 * bb + 4 * sub;      // this lane's first column
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (act) {
+      const uint32_t a = pbase + partial_off(r, bb * 8 + sub);
+      float4 p[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (k < S) p[k] = ld_shared_cluster_f4(mapa_shared(a, static_cast<uint32_t>(k)));
+      acc = p[0];
+#pragma unroll
+      for (int k = 1; k < 8; ++k) {
+        if (k < S) {
+          acc.x += p[k].x;
+          acc.y += p[k].y;
+          acc.z += p[k].z;
+          acc.w += p[k].w;
+        }
+      }
+    }
+    // + bias and bf16 as store_quad forms them; columns past N are zeros
+    float x[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = act && n + i < o.N ? with_bias(bias, n + i, x[i]) : 0.f;
+    const uint32_t w0 = pack_bf16x2(x[0], x[1]), w1 = pack_bf16x2(x[2], x[3]);
+    uint32_t sbyte;
+    const uint32_t codes = quantize4_words(w0, w1, sbyte);
+    if (act && n < o.N) {
+      const int row_bytes = o.N >> 1;
+      uint8_t* dst = o.qcodes + static_cast<size_t>(r) * row_bytes + (n >> 1);
+      if (n + 4 <= o.N && (reinterpret_cast<uintptr_t>(dst) & 1) == 0) {
+        *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(codes);
+      } else {
+        dst[0] = static_cast<uint8_t>(codes);
+        if ((n >> 1) + 1 < row_bytes) dst[1] = static_cast<uint8_t>(codes >> 8);
+      }
+      if (sub == 0) o.qscales[static_cast<size_t>(r) * ((o.N + 31) >> 5) + (n >> 5)] = static_cast<uint8_t>(sbyte);
+    }
+  }
+}
+
+// kQ: MXFP4 output (g.o.qcodes set); the bf16 instantiation holds none of
+// its code.
+template <int kRowsA, bool kQ>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs g) {
   using C = Cfg<kRowsA>;
   extern __shared__ uint8_t smem_raw[];
@@ -325,7 +383,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
               float chunk[32];
 #pragma unroll
               for (int c = 0; c < 32; ++c) chunk[c] = __uint_as_float(r[c0 + c]);
-              store_chunk(g.o, rl, n0 + c0, chunk);
+              if (kQ)
+                store_chunk_q(g.o, rl, n0 + c0, chunk);
+              else
+                store_chunk_bf16(g.o, rl, n0 + c0, chunk);
             }
           } else {
             const int qc0 = (h * 128 + pass * 64) >> 2;
@@ -351,7 +412,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       const int q_lo = rank * 64 / S, nq = (rank + 1) * 64 / S - q_lo;
       const uint32_t pbase = smem_u32(smem);
       const int n0 = t0 * kTileN;
-      for (int gi = threadIdx.x - 64; gi < g.M * nq; gi += kEpiThreads) {
+      if (kQ) split_sum_store_q(g.o, g.M, S, rank, pbase, n0);
+      for (int gi = threadIdx.x - 64; !kQ && gi < g.M * nq; gi += kEpiThreads) {
         const int r = gi / nq, qq = q_lo + gi % nq;
         const uint32_t a = pbase + partial_off(r, qq);
         float4 p[8];
@@ -379,16 +441,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 // ===================================================================== host
 // Per-device, per-kernel host caches; several host threads may fill them
 // at once, each writing the same value.
-static std::atomic<bool> g_attr_set[64][3];
-static std::atomic<int> g_max_clusters[64][3][9];   // co-resident clusters of size S (0: not yet queried)
+static std::atomic<bool> g_attr_set[64][6];
+static std::atomic<int> g_max_clusters[64][6][9];   // co-resident clusters of size S (0: not yet queried)
 
-template <int kRowsA>
+template <int kRowsA, bool kQ>
 static cudaError_t prepare(const DeviceInfo& dev, int which) {
   using C = Cfg<kRowsA>;
   if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
   if (!g_attr_set[dev.device][which].load(std::memory_order_acquire)) {
     cudaError_t e =
-        cudaFuncSetAttribute(decode_kernel<kRowsA>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        cudaFuncSetAttribute(decode_kernel<kRowsA, kQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     g_attr_set[dev.device][which].store(true, std::memory_order_release);
   }
@@ -396,7 +458,7 @@ static cudaError_t prepare(const DeviceInfo& dev, int which) {
 }
 
 // How many clusters of S CTAs (one per SM) the device holds at once.
-template <int kRowsA>
+template <int kRowsA, bool kQ>
 static int max_clusters(int S, const DeviceInfo& dev, int which) {
   using C = Cfg<kRowsA>;
   std::atomic<int>& slot = g_max_clusters[dev.device][which][S];
@@ -414,7 +476,7 @@ static int max_clusters(int S, const DeviceInfo& dev, int which) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<kRowsA>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<kRowsA, kQ>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       n = 0;
     }
@@ -424,10 +486,10 @@ static int max_clusters(int S, const DeviceInfo& dev, int which) {
   return cached;
 }
 
-template <int kRowsA>
+template <int kRowsA, bool kQ>
 static cudaError_t launch_rows(DecodeArgs a, const DeviceInfo& dev, cudaStream_t s, int which) {
   using C = Cfg<kRowsA>;
-  cudaError_t e = prepare<kRowsA>(dev, which);
+  cudaError_t e = prepare<kRowsA, kQ>(dev, which);
   if (e != cudaSuccess) return e;
   // Split: with fewer tiles than SMs, S CTAs per tile (a cluster), S as
   // large as the SMs allow (at most 8 and at most one k-step per CTA) with
@@ -437,7 +499,7 @@ static cudaError_t launch_rows(DecodeArgs a, const DeviceInfo& dev, cudaStream_t
     split = dev.sm_count / a.n_tiles;
     if (split > 8) split = 8;
     if (split > a.KT) split = a.KT;
-    while (split > 1 && max_clusters<kRowsA>(split, dev, which) < a.n_tiles) --split;
+    while (split > 1 && max_clusters<kRowsA, kQ>(split, dev, which) < a.n_tiles) --split;
   }
   a.split = split;
   const int grid = split > 1 ? a.n_tiles * split : (a.n_tiles < dev.sm_count ? a.n_tiles : dev.sm_count);
@@ -456,7 +518,7 @@ static cudaError_t launch_rows(DecodeArgs a, const DeviceInfo& dev, cudaStream_t
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = split > 1 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<kRowsA>, a);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<kRowsA, kQ>, a);
 }
 
 cudaError_t launch_decode(const DecodeProblem& p, const DeviceInfo& dev, cudaStream_t s) {
@@ -472,14 +534,23 @@ cudaError_t launch_decode(const DecodeProblem& p, const DeviceInfo& dev, cudaStr
   a.o.bias = static_cast<const __nv_bfloat16*>(p.bias);
   a.o.ldo = p.ldo;
   a.o.N = p.N;
+  a.o.qcodes = p.qcodes;
+  a.o.qscales = p.qscales;
   a.M = p.M;
   a.K = p.K;
   a.KT = static_cast<int>(padded_k(p.K) / kKTile);
   a.n_tiles = static_cast<int>(ceil_div(p.N, kTileN));
+  if (p.qcodes != nullptr) {
+    switch (gemm_rows_a(p.M)) {
+      case 16: return launch_rows<16, true>(a, dev, s, 3);
+      case 32: return launch_rows<32, true>(a, dev, s, 4);
+      default: return launch_rows<64, true>(a, dev, s, 5);
+    }
+  }
   switch (gemm_rows_a(p.M)) {
-    case 16: return launch_rows<16>(a, dev, s, 0);
-    case 32: return launch_rows<32>(a, dev, s, 1);
-    default: return launch_rows<64>(a, dev, s, 2);
+    case 16: return launch_rows<16, false>(a, dev, s, 0);
+    case 32: return launch_rows<32, false>(a, dev, s, 1);
+    default: return launch_rows<64, false>(a, dev, s, 2);
   }
 }
 

@@ -272,6 +272,8 @@ struct FixupArgs {
 
 // At most 64 registers per thread, so a waiting fix-up block fits on an SM
 // next to a resident GEMM CTA (of the next call).
+// kQuant: MXFP4 output (g.o.qcodes set).
+template <bool kQuant>
 __global__ void __launch_bounds__(256, 4) gemm_fixup_kernel(const __grid_constant__ FixupArgs f) {
   griddep_launch_dependents();
   griddep_wait();                                   // the GEMM's parts are complete and visible
@@ -282,6 +284,41 @@ __global__ void __launch_bounds__(256, 4) gemm_fixup_kernel(const __grid_constan
   const int c_lo = sk_owner(t * KT, g.total, g.grid);
   const int c_hi = sk_owner(t * KT + KT - 1, g.total, g.grid);
   const int rows = (g.M - mt * 128) < g.rows_a ? (g.M - mt * 128) : g.rows_a;
+  if (kQuant) {
+    // MXFP4 output: one (row, 32-column block) per thread, the same sums in
+    // the same order (8 float4 groups of the row, contributors in CTA order).
+    const int u = blockIdx.y * 256 + threadIdx.x;
+    if (u >= rows * (kTileN / 32)) return;
+    const int row = u / (kTileN / 32), blk = u % (kTileN / 32);
+    const int gq0 = row * (kTileN / 4) + blk * 8;
+    float4 acc[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int cc = c_lo; cc <= c_hi; ++cc) {
+      const int sl = 2 * cc + (sk_begin(cc, g.total, g.grid) / KT == t ? 0 : 1);
+      const float4* Q = reinterpret_cast<const float4*>(g.partials + static_cast<size_t>(sl) * g.rows_a * kTileN);
+      float4 p[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) p[k] = __ldcg(Q + gq0 + k);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        acc[k].x += p[k].x;
+        acc[k].y += p[k].y;
+        acc[k].z += p[k].z;
+        acc[k].w += p[k].w;
+      }
+    }
+    float v[32];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      v[4 * k] = acc[k].x;
+      v[4 * k + 1] = acc[k].y;
+      v[4 * k + 2] = acc[k].z;
+      v[4 * k + 3] = acc[k].w;
+    }
+    store_chunk(g.o, mt * 128 + row, nt * kTileN + 32 * blk, v);
+    return;
+  }
   const int groups = rows * (kTileN / 4);
   const int g0 = blockIdx.y * kFixupGroups + threadIdx.x;   // this thread: groups g0 and g0 + 256
   if (g0 >= groups) return;
@@ -342,6 +379,8 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
   a.o.out = static_cast<__nv_bfloat16*>(p.out);
   a.o.ldo = p.ldo;
   a.o.N = p.N;
+  a.o.qcodes = p.qcodes;
+  a.o.qscales = p.qscales;
   a.M = p.M;
   a.KT = static_cast<int>(Kp / kKTile);
   a.n_tiles = static_cast<int>(ceil_div(p.N, kTileN));
@@ -384,7 +423,8 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_fixup_kernel, f);
+  return p.qcodes != nullptr ? cudaLaunchKernelEx(&cfg, gemm_fixup_kernel<true>, f)
+                             : cudaLaunchKernelEx(&cfg, gemm_fixup_kernel<false>, f);
 }
 
 uint32_t gemm_read_clear_error() {

@@ -10,6 +10,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant_math.cuh"
 
 namespace mx {
 
@@ -56,6 +57,11 @@ __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
   return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
+// v + bias[n], or v itself without a bias (no + 0: a -0 result stays -0, the
+// same in every store path).
+__device__ __forceinline__ float with_bias(const uint16_t* bias, int n, float v) {
+  return bias != nullptr ? v + bf16_bits_to_float(__ldg(bias + n)) : v;
+}
 
 // Balanced stream-K split: CTA c owns iterations [sk_begin(c), sk_begin(c+1)).
 __device__ __forceinline__ int sk_begin(int c, int total, int grid) {
@@ -69,35 +75,79 @@ __device__ __forceinline__ int sk_owner(int it, int total, int grid) {
   return c;
 }
 
-// Where the bf16 results go.
+// Where the results go: bf16 [M][ldo], or (qcodes != null) the MXFP4
+// quantization of those bf16 values, row-major codes [M][N/2] and scales
+// [M][ceil(N/32)] (N even).
 struct OutView {
   __nv_bfloat16* out;
   const __nv_bfloat16* bias;   // [N] or null
   int ldo, N;
+  uint8_t* qcodes;
+  uint8_t* qscales;
 };
 
+// MXFP4 output: the 32 outputs of row m from column n (a multiple of 32) +
+// bias, rounded to bf16 exactly as the bf16 store rounds them, then
+// quantized as one 1x32 block (columns past N count as zeros) by the
+// thread that holds them.
+__device__ __forceinline__ void store_chunk_q(const OutView& o, int m, int n, const float (&v)[32]) {
+  if (n >= o.N) return;
+  const uint16_t* bias = reinterpret_cast<const uint16_t*>(o.bias);
+  uint32_t w[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int c = n + 2 * j;
+    const float lo = c < o.N ? with_bias(bias, c, v[2 * j]) : 0.f;
+    const float hi = c + 1 < o.N ? with_bias(bias, c + 1, v[2 * j + 1]) : 0.f;
+    w[j] = pack_bf16x2(lo, hi);
+  }
+  const uint4 blk[4] = {make_uint4(w[0], w[1], w[2], w[3]), make_uint4(w[4], w[5], w[6], w[7]),
+                        make_uint4(w[8], w[9], w[10], w[11]), make_uint4(w[12], w[13], w[14], w[15])};
+  uint4 codes;
+  const uint32_t sbyte = quantize32_words(blk, codes);
+  const int row_bytes = o.N >> 1;
+  uint8_t* dst = o.qcodes + static_cast<size_t>(m) * row_bytes + (n >> 1);
+  if (n + 32 <= o.N && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
+    *reinterpret_cast<uint4*>(dst) = codes;
+  } else {
+    const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+#pragma unroll
+    for (int b = 0; b < 16; ++b)
+      if ((n >> 1) + b < row_bytes) dst[b] = static_cast<uint8_t>(cw[b >> 2] >> (8 * (b & 3)));
+  }
+  o.qscales[static_cast<size_t>(m) * ((o.N + 31) >> 5) + (n >> 5)] = static_cast<uint8_t>(sbyte);
+}
+
 // 32 consecutive outputs of row m starting at column n: + bias, bf16, store.
-__device__ __forceinline__ void store_chunk(const OutView& o, int m, int n, const float (&v)[32]) {
+__device__ __forceinline__ void store_chunk_bf16(const OutView& o, int m, int n, const float (&v)[32]) {
   __nv_bfloat16* dst = o.out + static_cast<size_t>(m) * o.ldo + n;
   const uint16_t* bias = reinterpret_cast<const uint16_t*>(o.bias);
   if (n + 32 <= o.N && (reinterpret_cast<uintptr_t>(dst) & 15) == 0) {
 #pragma unroll
     for (int c = 0; c < 32; c += 8) {
-      float b[8];
+      float x[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) b[i] = bias != nullptr ? bf16_bits_to_float(__ldg(bias + n + c + i)) : 0.f;
+      for (int i = 0; i < 8; ++i) x[i] = with_bias(bias, n + c + i, v[c + i]);
       uint4 w;
-      w.x = pack_bf16x2(v[c] + b[0], v[c + 1] + b[1]);
-      w.y = pack_bf16x2(v[c + 2] + b[2], v[c + 3] + b[3]);
-      w.z = pack_bf16x2(v[c + 4] + b[4], v[c + 5] + b[5]);
-      w.w = pack_bf16x2(v[c + 6] + b[6], v[c + 7] + b[7]);
+      w.x = pack_bf16x2(x[0], x[1]);
+      w.y = pack_bf16x2(x[2], x[3]);
+      w.z = pack_bf16x2(x[4], x[5]);
+      w.w = pack_bf16x2(x[6], x[7]);
       *reinterpret_cast<uint4*>(dst + c) = w;
     }
   } else {
     for (int c = 0; c < 32; ++c)
-      if (n + c < o.N)
-        dst[c] = __float2bfloat16_rn(v[c] + (bias != nullptr ? bf16_bits_to_float(__ldg(bias + n + c)) : 0.f));
+      if (n + c < o.N) dst[c] = __float2bfloat16_rn(with_bias(bias, n + c, v[c]));
   }
+}
+
+// The same, or for MXFP4 output (o.qcodes set) its quantization (n is then a
+// multiple of 32).
+__device__ __forceinline__ void store_chunk(const OutView& o, int m, int n, const float (&v)[32]) {
+  if (o.qcodes != nullptr)
+    store_chunk_q(o, m, n, v);
+  else
+    store_chunk_bf16(o, m, n, v);
 }
 
 // 4 consecutive outputs of row m starting at column n: + bias, bf16, store.
@@ -106,11 +156,9 @@ __device__ __forceinline__ void store_quad(const OutView& o, int m, int n, float
   __nv_bfloat16* dst = o.out + static_cast<size_t>(m) * o.ldo + n;
   const uint16_t* bias = reinterpret_cast<const uint16_t*>(o.bias);
   float x[4] = {v.x, v.y, v.z, v.w};
-  if (bias != nullptr) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      if (n + i < o.N) x[i] += bf16_bits_to_float(__ldg(bias + n + i));
-  }
+  for (int i = 0; i < 4; ++i)
+    if (n + i < o.N) x[i] = with_bias(bias, n + i, x[i]);
   if (n + 4 <= o.N && (reinterpret_cast<uintptr_t>(dst) & 7) == 0) {
     *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]));
   } else {

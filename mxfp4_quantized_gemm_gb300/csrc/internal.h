@@ -79,8 +79,10 @@ struct GemmProblem {
   bool a_blocked;           // a_codes holds blocked activations with 128-row blocks
   const uint8_t* w_packed;  // packed weights (codes region then scales region)
   const void* bias;         // bf16 [N] or null
-  void* out;                // bf16 [M][ldo]
+  void* out;                // bf16 [M][ldo]; unused with MXFP4 output
   int ldo, M, N, K;
+  uint8_t* qcodes;          // MXFP4 output (row-major codes [M][N/2], scales [M][ceil(N/32)]) or null
+  uint8_t* qscales;
   void* workspace;          // stream-K partial sums
   size_t workspace_bytes;
 };
@@ -102,6 +104,8 @@ struct DecodeProblem {
   const void* bias;
   void* out;
   int ldo, M, N, K;
+  uint8_t* qcodes;          // MXFP4 output or null (as GemmProblem)
+  uint8_t* qscales;
 };
 cudaError_t launch_decode(const DecodeProblem& p, const DeviceInfo& dev, cudaStream_t s);
 uint32_t decode_read_clear_error();

@@ -16,6 +16,7 @@ including the pages' flattening of 3-D activations to 2-D for the GEMM.
     torch.ops.mxfp4.rmsnorm_quant_act(x, gamma, eps, layout, residual) -> (codes, scales)   # residual updated
     torch.ops.mxfp4.linear(x, w_packed, bias, N) -> out          # x [..., K] bf16
     torch.ops.mxfp4.linear_prequant(codes, scales, layout, w_packed, bias, M, N, K) -> out
+    torch.ops.mxfp4.linear_mxfp4_out(x, w_packed, bias, N) -> (codes, scales)   # next layer's input
     torch.ops.mxfp4.a16wfp4_bmm(x, w_packed, N, batch_major) -> out
 """
 
@@ -224,6 +225,36 @@ def _(codes, scales, layout, w_packed, bias, M, N, K):
                 dtypes=(torch.uint8, torch.uint8, torch.uint8, torch.bfloat16))
     _check_weights("mxfp4::linear_prequant", w_packed, 1, N, K)
     return codes.new_empty(M, N, dtype=torch.bfloat16)
+
+
+@custom_op("mxfp4::linear_mxfp4_out", mutates_args=())
+def linear_mxfp4_out(x: Tensor, w_packed: Tensor, bias: Optional[Tensor], N: int) -> tuple[Tensor, Tensor]:
+    """linear() with the MXFP4 output epilogue: the bf16 result quantized per
+    1x32 along N, row-major codes [M, N/2] and scales [M, ceil(N/32)] (M =
+    the flattened leading dims of x), ready for linear_prequant."""
+    _check_args("mxfp4::linear_mxfp4_out", x, w_packed, bias, dtypes=(torch.bfloat16, torch.uint8, torch.bfloat16))
+    _check_weights("mxfp4::linear_mxfp4_out", w_packed, 1, N, x.shape[-1])
+    torch._check(N % 2 == 0, lambda: f"mxfp4::linear_mxfp4_out: N = {N} must be even")
+    c = _capi()
+    K = x.shape[-1]
+    x2 = x.reshape(-1, K).contiguous()
+    M = x2.shape[0]
+    codes = torch.empty(M, N // 2, dtype=torch.uint8, device=x.device)
+    scales = torch.empty(M, _cdiv(N, 32), dtype=torch.uint8, device=x.device)
+    ws, nbytes = _workspace(M, N, K, x.device)
+    b = bias.contiguous() if bias is not None else None
+    c.mxfp4_gemm_mxfp4_out(x2, K, None, None, LAYOUT_ROWMAJOR, w_packed, b, codes, scales, M, N, K, ws, nbytes,
+                           _stream(x))
+    return codes, scales
+
+
+@linear_mxfp4_out.register_fake
+def _(x, w_packed, bias, N):
+    _check_args("mxfp4::linear_mxfp4_out", x, w_packed, bias, dtypes=(torch.bfloat16, torch.uint8, torch.bfloat16))
+    _check_weights("mxfp4::linear_mxfp4_out", w_packed, 1, N, x.shape[-1])
+    torch._check(N % 2 == 0, lambda: f"mxfp4::linear_mxfp4_out: N = {N} must be even")
+    M = x.numel() // x.shape[-1]
+    return x.new_empty(M, N // 2, dtype=torch.uint8), x.new_empty(M, _cdiv(N, 32), dtype=torch.uint8)
 
 
 @custom_op("mxfp4::a16wfp4_bmm", mutates_args=())

@@ -94,6 +94,23 @@ def test_argument_checks_precede_any_launch(capi):
     assert lib.mxfp4_gemm(A, 64, None, None, 0, A + 2, None, A, 8, 4, 8, 64, A, ws, None) == capi.ERR_MISALIGNED
 
 
+def test_mxfp4_out_gemm_argument_checks(capi):
+    lib, A = capi.lib, 1 << 20
+    ws = capi.mxfp4_gemm_workspace_bytes(4, 8, 64)
+    f = lib.mxfp4_gemm_mxfp4_out
+    assert f(A, 64, None, None, 0, A, None, None, A, 4, 8, 64, A, ws, None) == capi.ERR_INVALID_ARG
+    assert f(A, 64, None, None, 0, A, None, A, None, 4, 8, 64, A, ws, None) == capi.ERR_INVALID_ARG
+    assert f(A, 64, None, None, 0, None, None, A, A, 4, 8, 64, A, ws, None) == capi.ERR_INVALID_ARG
+    assert f(A, 64, None, None, 0, A, None, A, A, 4, 7, 64, A, ws, None) == capi.ERR_UNSUPPORTED_SHAPE   # odd N
+    assert f(A, 64, None, None, 0, A, None, A, A, 4, 8, 63, A, ws, None) == capi.ERR_UNSUPPORTED_SHAPE   # odd K
+    assert f(A, 64, None, None, 0, A, None, A, A, 4, 8, 64, A, ws - 1, None) == capi.ERR_WORKSPACE
+    assert f(A, 64, None, None, 0, A + 8, None, A, A, 4, 8, 64, A, ws, None) == capi.ERR_MISALIGNED
+    if not torch.cuda.is_available():
+        # unaligned outputs are accepted: the call gets as far as the device check
+        assert f(A, 64, None, None, 0, A, None, A + 1, A + 3, 4, 8, 64, A, ws, None) in (capi.ERR_NO_DEVICE,
+                                                                                        capi.ERR_CUDA)
+
+
 def test_rmsnorm_quant_argument_checks(capi):
     lib, A = capi.lib, 1 << 20
     f = lib.mxfp4_rmsnorm_quant_act

@@ -89,6 +89,20 @@ def test_prequant_op_matches_fused(capi, M, layout):
     assert torch.equal(y, torch.ops.mxfp4.linear(xd, packed, bd, N))
 
 
+def test_linear_mxfp4_out_op_feeds_linear_prequant(capi):
+    M, N, K, N2 = 12, 1024, 2048, 512
+    x, wc, ws, b = problem(M, N, K, seed=17)
+    packed = pack_weights(capi, wc, ws, K)
+    packed2 = pack_weights(capi, synth.weight_codes(N2, N, seed=18), synth.weight_scales(N2, N, -6, 0, seed=18), N)
+    xd, bd = dev_bf16(x).view(3, 4, K), dev_bf16(b)
+    codes, scales = torch.ops.mxfp4.linear_mxfp4_out(xd, packed, bd, N)
+    y = torch.ops.mxfp4.linear(xd, packed, bd, N)
+    c2, s2 = torch.ops.mxfp4.quant_act(y, 0)
+    assert torch.equal(codes, c2) and torch.equal(scales, s2)
+    z = torch.ops.mxfp4.linear_prequant(codes, scales, 0, packed2, None, M, N2, N)
+    assert torch.equal(z, torch.ops.mxfp4.linear(y.view(M, N), packed2, None, N2))
+
+
 def test_rmsnorm_quant_op_matches_capi(capi):
     M, K = 6, 5120
     x = dev_bf16(synth.activations(M, K, seed=21)).view(2, 3, K)

@@ -53,6 +53,13 @@ def test_rmsnorm_quant_shapes():
     assert c.shape == (7, 50) and s.shape == (7, 4)
 
 
+def test_linear_mxfp4_out_shapes():
+    c, s = torch.ops.mxfp4.linear_mxfp4_out(meta(2, 5, 1024), packed_meta(1, 1000, 1024), None, 1000)
+    assert c.shape == (10, 500) and s.shape == (10, 32) and c.dtype == U8
+    with pytest.raises(RuntimeError, match="even"):
+        torch.ops.mxfp4.linear_mxfp4_out(meta(2, 1024), packed_meta(1, 999, 1024), None, 999)
+
+
 def test_pack_weights_shape():
     w = torch.ops.mxfp4.pack_weights(meta(3, 300, 256, dtype=U8), meta(3, 300, 16, dtype=U8), 512)
     assert w.numel() == 3 * 2 * 2 * 34816
