@@ -33,7 +33,10 @@
 //    the dependency wait; for larger M (where every CTA re-reading bf16 x
 //    would cost as much L2 traffic as its weights) the standalone quantizer
 //    runs first and the kernel copies the quantized rows in with one bulk
-//    copy per stage.
+//    copy per stage;
+//  * decode_kernel<rows, true> is the MXFP4 output epilogue's form (the
+//    results quantized per 1x32 along N instead of stored as bf16); the bf16
+//    form is a separate instantiation that holds none of that code.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 

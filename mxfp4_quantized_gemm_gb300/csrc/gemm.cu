@@ -25,7 +25,11 @@
 // publish the part).  The tensor pipe bounds the kernel: per 256-wide
 // k-step its four MMAs and the scale copies run back to back, so for
 // K <= 6144 the activation scales of every k-step stay in TMEM across the
-// tiles of one activation row tile (four copies per k-step instead of six).  The kernel is launched as a programmatic dependent:
+// tiles of one activation row tile (four copies per k-step instead of six).
+// With an MXFP4 output (OutView::qcodes set) the epilogue threads quantize
+// their 32-column chunks instead of storing bf16, and the fix-up kernel's
+// <true> form sums one (row, 32-column block) per thread.  The kernel is
+// launched as a programmatic dependent:
 // it sets up and requests its first weight stages while the activation
 // quantizer before it finishes, and lets the next kernel launch early.
 #include <cuda_bf16.h>
