@@ -86,9 +86,14 @@ def load_peaks():
 
 
 def kernel_source_hash():
+    """sha256 (first 16 hex digits) of the decode kernel's sources, with //
+    comments and blank lines dropped: a comment edit does not change the kernel."""
     h = hashlib.sha256()
     for f in ("decode.cu", "gemm_common.cuh", "quant_math.cuh", "ptx.cuh", "internal.h"):
-        h.update(open(os.path.join(ROOT, "mxfp4_quantized_gemm_gb300", "csrc", f), "rb").read())
+        for line in open(os.path.join(ROOT, "mxfp4_quantized_gemm_gb300", "csrc", f), encoding="utf-8"):
+            code = line.split("//", 1)[0].rstrip()
+            if code:
+                h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 
