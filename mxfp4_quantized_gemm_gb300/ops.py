@@ -75,6 +75,11 @@ def _check_weights(where: str, w_packed: Tensor, batch: int, N: int, K: int) -> 
                  lambda: f"{where}: packed weights hold {w_packed.numel()} bytes, {need} needed")
 
 
+def _check_bias(where: str, bias: Optional[Tensor], N: int) -> None:
+    if bias is not None:
+        torch._check(bias.numel() == N, lambda: f"{where}: bias has {bias.numel()} elements, N = {N}")
+
+
 def _act_bytes(M: int, K: int, layout: int) -> tuple[int, int]:
     if layout == LAYOUT_ROWMAJOR:
         return M * (K // 2), M * _cdiv(K, 32)
@@ -83,11 +88,21 @@ def _act_bytes(M: int, K: int, layout: int) -> tuple[int, int]:
 
 
 # ------------------------------------------------------------ weight repack
+def _check_pack(where: str, codes: Tensor, scales: Tensor, K: int) -> None:
+    _check_args(where, codes, scales, dtypes=(torch.uint8, torch.uint8))
+    torch._check(codes.dim() in (2, 3) and scales.dim() == codes.dim(),
+                 lambda: f"{where}: codes and scales must both be [N, *] or [B, N, *]")
+    torch._check(K > 0 and K % 2 == 0, lambda: f"{where}: K = {K} must be positive and even")
+    torch._check(codes.shape[-1] == K // 2 and scales.shape[-1] == _cdiv(K, 32),
+                 lambda: f"{where}: codes [.., {codes.shape[-1]}] / scales [.., {scales.shape[-1]}] do not hold K = {K}")
+    torch._check(codes.shape[:-1] == scales.shape[:-1], lambda: f"{where}: codes and scales differ in leading dims")
+
+
 @custom_op("mxfp4::pack_weights", mutates_args=())
 def pack_weights(codes: Tensor, scales: Tensor, K: int) -> Tensor:
     """codes [N, K/2] or [B, N, K/2] uint8, scales [.., N, ceil(K/32)] uint8
     -> the packed weight buffer (uint8)."""
-    _check_args("mxfp4::pack_weights", codes, scales, dtypes=(torch.uint8, torch.uint8))
+    _check_pack("mxfp4::pack_weights", codes, scales, K)
     c = _capi()
     B = codes.shape[0] if codes.dim() == 3 else 1
     N = codes.shape[-2]
@@ -98,7 +113,7 @@ def pack_weights(codes: Tensor, scales: Tensor, K: int) -> Tensor:
 
 @pack_weights.register_fake
 def _(codes, scales, K):
-    _check_args("mxfp4::pack_weights", codes, scales, dtypes=(torch.uint8, torch.uint8))
+    _check_pack("mxfp4::pack_weights", codes, scales, K)
     B = codes.shape[0] if codes.dim() == 3 else 1
     return codes.new_empty(_packed_weight_bytes(B, codes.shape[-2], K), dtype=torch.uint8)
 
@@ -141,6 +156,7 @@ def rmsnorm_quant_act(x: Tensor, gamma: Tensor, eps: float, layout: int,
     times gamma, quantized per 1x32 like quant_act; returns (codes, scales)."""
     _check_args("mxfp4::rmsnorm_quant_act", x, gamma, residual,
                 dtypes=(torch.bfloat16, torch.bfloat16, torch.bfloat16))
+    torch._check(gamma.numel() == x.shape[-1], lambda: "mxfp4::rmsnorm_quant_act: gamma must have K elements")
     c = _capi()
     K = x.shape[-1]
     x2 = x.reshape(-1, K).contiguous()
@@ -164,6 +180,7 @@ def rmsnorm_quant_act(x: Tensor, gamma: Tensor, eps: float, layout: int,
 def _(x, gamma, eps, layout, residual):
     _check_args("mxfp4::rmsnorm_quant_act", x, gamma, residual,
                 dtypes=(torch.bfloat16, torch.bfloat16, torch.bfloat16))
+    torch._check(gamma.numel() == x.shape[-1], lambda: "mxfp4::rmsnorm_quant_act: gamma must have K elements")
     K = x.shape[-1]
     M = x.numel() // K
     nc, ns = _act_bytes(M, K, layout)
@@ -184,6 +201,7 @@ def linear(x: Tensor, w_packed: Tensor, bias: Optional[Tensor], N: int) -> Tenso
     call, W the packed FP4 weights of N rows; y [..., N] bf16."""
     _check_args("mxfp4::linear", x, w_packed, bias, dtypes=(torch.bfloat16, torch.uint8, torch.bfloat16))
     _check_weights("mxfp4::linear", w_packed, 1, N, x.shape[-1])
+    _check_bias("mxfp4::linear", bias, N)
     c = _capi()
     K = x.shape[-1]
     x2 = x.reshape(-1, K).contiguous()
@@ -199,7 +217,20 @@ def linear(x: Tensor, w_packed: Tensor, bias: Optional[Tensor], N: int) -> Tenso
 def _(x, w_packed, bias, N):
     _check_args("mxfp4::linear", x, w_packed, bias, dtypes=(torch.bfloat16, torch.uint8, torch.bfloat16))
     _check_weights("mxfp4::linear", w_packed, 1, N, x.shape[-1])
+    _check_bias("mxfp4::linear", bias, N)
     return x.new_empty(*x.shape[:-1], N, dtype=torch.bfloat16)
+
+
+def _check_prequant(codes, scales, layout, w_packed, bias, M, N, K) -> None:
+    where = "mxfp4::linear_prequant"
+    _check_args(where, codes, scales, w_packed, bias, dtypes=(torch.uint8, torch.uint8, torch.uint8, torch.bfloat16))
+    _check_weights(where, w_packed, 1, N, K)
+    _check_bias(where, bias, N)
+    torch._check(layout in (LAYOUT_ROWMAJOR, LAYOUT_TILED), lambda: f"{where}: layout {layout}")
+    torch._check(M > 0, lambda: f"{where}: M = {M} must be positive")
+    nc, ns = _act_bytes(M, K, layout)
+    torch._check(codes.numel() >= nc and scales.numel() >= ns,
+                 lambda: f"{where}: codes / scales hold {codes.numel()} / {scales.numel()} bytes, {nc} / {ns} needed")
 
 
 @custom_op("mxfp4::linear_prequant", mutates_args=())
@@ -207,9 +238,7 @@ def linear_prequant(codes: Tensor, scales: Tensor, layout: int, w_packed: Tensor
                     N: int, K: int) -> Tensor:
     """The pages' pre-quantized (x_fp4, x_scales) input: codes and scales in
     `layout` (as from quant_act) against the packed weights; [M, N] bf16."""
-    _check_args("mxfp4::linear_prequant", codes, scales, w_packed, bias,
-                dtypes=(torch.uint8, torch.uint8, torch.uint8, torch.bfloat16))
-    _check_weights("mxfp4::linear_prequant", w_packed, 1, N, K)
+    _check_prequant(codes, scales, layout, w_packed, bias, M, N, K)
     c = _capi()
     out = torch.empty(M, N, dtype=torch.bfloat16, device=codes.device)
     ws, nbytes = _workspace(M, N, K, codes.device)
@@ -221,9 +250,7 @@ def linear_prequant(codes: Tensor, scales: Tensor, layout: int, w_packed: Tensor
 
 @linear_prequant.register_fake
 def _(codes, scales, layout, w_packed, bias, M, N, K):
-    _check_args("mxfp4::linear_prequant", codes, scales, w_packed, bias,
-                dtypes=(torch.uint8, torch.uint8, torch.uint8, torch.bfloat16))
-    _check_weights("mxfp4::linear_prequant", w_packed, 1, N, K)
+    _check_prequant(codes, scales, layout, w_packed, bias, M, N, K)
     return codes.new_empty(M, N, dtype=torch.bfloat16)
 
 
@@ -234,6 +261,7 @@ def linear_mxfp4_out(x: Tensor, w_packed: Tensor, bias: Optional[Tensor], N: int
     the flattened leading dims of x), ready for linear_prequant."""
     _check_args("mxfp4::linear_mxfp4_out", x, w_packed, bias, dtypes=(torch.bfloat16, torch.uint8, torch.bfloat16))
     _check_weights("mxfp4::linear_mxfp4_out", w_packed, 1, N, x.shape[-1])
+    _check_bias("mxfp4::linear_mxfp4_out", bias, N)
     torch._check(N % 2 == 0, lambda: f"mxfp4::linear_mxfp4_out: N = {N} must be even")
     c = _capi()
     K = x.shape[-1]
@@ -252,6 +280,7 @@ def linear_mxfp4_out(x: Tensor, w_packed: Tensor, bias: Optional[Tensor], N: int
 def _(x, w_packed, bias, N):
     _check_args("mxfp4::linear_mxfp4_out", x, w_packed, bias, dtypes=(torch.bfloat16, torch.uint8, torch.bfloat16))
     _check_weights("mxfp4::linear_mxfp4_out", w_packed, 1, N, x.shape[-1])
+    _check_bias("mxfp4::linear_mxfp4_out", bias, N)
     torch._check(N % 2 == 0, lambda: f"mxfp4::linear_mxfp4_out: N = {N} must be even")
     M = x.numel() // x.shape[-1]
     return x.new_empty(M, N // 2, dtype=torch.uint8), x.new_empty(M, _cdiv(N, 32), dtype=torch.uint8)

@@ -86,6 +86,22 @@ def test_argument_checks():
         torch.ops.mxfp4.a16wfp4_bmm(torch.zeros(2, 3, 64, dtype=BF), torch.zeros(2 * 34816, dtype=U8), 128, False)
 
 
+def test_size_checks_keep_kernels_in_bounds():
+    w = packed_meta(1, 300, 1024)
+    with pytest.raises(RuntimeError, match="bias"):
+        torch.ops.mxfp4.linear(meta(4, 1024), w, meta(299), 300)
+    with pytest.raises(RuntimeError, match="needed"):
+        torch.ops.mxfp4.linear_prequant(meta(4, 511, dtype=U8), meta(4, 32, dtype=U8), 0, w, None, 4, 300, 1024)
+    with pytest.raises(RuntimeError, match="do not hold"):
+        torch.ops.mxfp4.pack_weights(meta(300, 256, dtype=U8), meta(300, 32, dtype=U8), 1024)
+    with pytest.raises(RuntimeError, match="leading"):
+        torch.ops.mxfp4.pack_weights(meta(300, 512, dtype=U8), meta(301, 32, dtype=U8), 1024)
+    with pytest.raises(RuntimeError, match="gamma"):
+        torch.ops.mxfp4.rmsnorm_quant_act(meta(4, 1024), meta(1000), 1e-6, 0, None)
+    with pytest.raises(RuntimeError, match="bias"):
+        torch.ops.mxfp4.linear_mxfp4_out(meta(4, 1024), w, meta(301), 300)
+
+
 @pytest.fixture(scope="module")
 def capi():
     from mxfp4_quantized_gemm_gb300 import build
