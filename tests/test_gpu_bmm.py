@@ -48,7 +48,8 @@ def test_mla_absorbed_bmm(capi, kind, N, K, batch_major, M):
 
 
 @pytest.mark.parametrize("B,M,N,K", [(1, 1, 128, 64), (3, 130, 200, 128), (2, 257, 64, 256), (5, 33, 512, 192),
-                                     (3, 200, 256, 512), (2, 300, 200, 384), (4, 17, 512, 448), (1, 129, 40, 320)])
+                                     (3, 200, 256, 512), (2, 300, 200, 384), (4, 17, 512, 448), (1, 129, 40, 320),
+                                     (2, 150, 256, 768), (1, 260, 300, 1024)])   # K > 512: 64-row weight tiles
 @pytest.mark.parametrize("batch_major", [False, True])
 def test_bmm_small_shapes(capi, B, M, N, K, batch_major):
     x = synth.bmm_activations(B, M, K, seed=B * M)
