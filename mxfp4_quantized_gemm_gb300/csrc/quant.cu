@@ -19,46 +19,43 @@ namespace mx {
 
 static __device__ uint32_t g_quant_error;
 
-// One warp per unit of (row, 256 consecutive elements): lane l holds
-// elements 8l..8l+7, four lanes form one 32-element block.
-// At most 64 registers per thread, so a quantizer block fits on an SM next
-// to a resident GEMM CTA.
+// A warp owns one 256-element k-tile column kt and the rows r0, r0 + R,
+// r0 + 2R, ... of it (R row groups per k-tile: warp gw has kt = gw % KT,
+// r0 = gw / KT, the only division); lane l holds elements 8l..8l+7 of the
+// k-tile, four lanes form one 32-element block.  Four rows' loads are in
+// flight together.  At most 64 registers per thread, so a quantizer block
+// fits on an SM next to a resident GEMM CTA.
 // kLayout: ActLayout::kRowMajor, kTiled or kBlocked (block_rows rows per
 // block; the rows written are 0..rows-1).
 template <ActLayout kLayout>
 __global__ void __launch_bounds__(256, 4) quant_kernel(const uint16_t* __restrict__ x, int M, int K, int ldx,
                                                     uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
-                                                    int rows, int KT, bool vec_ok, int block_rows) {
+                                                    int rows, int KT, bool vec_ok, int block_rows, int R) {
   const int lane = threadIdx.x & 31;
-  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  const int64_t units = static_cast<int64_t>(rows) * KT;
+  const int gw = static_cast<int>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
   // Launched as a programmatic dependent: let the GEMM behind this kernel
   // start its set-up and weight prefetch now, but touch memory only after the
   // kernel before this one (which may produce x or still read the outputs'
   // buffers) has completed.
   griddep_launch_dependents();
   griddep_wait();
-
-  // Four units per warp per pass: their loads are all in flight together.
-  for (int64_t u0 = warp; u0 < units; u0 += 4 * nwarps) {
-    uint16_t v[4][8];
+  if (gw >= KT * R) return;   // warp-uniform; the kernel has no block barrier
+  const int kt = gw % KT, r0 = gw / KT;
+  const int e0 = kt * 256 + lane * 8;
+  for (int r = r0; r < rows; r += 4 * R) {
+    uint4 v[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int64_t u = u0 + j * nwarps;
-      const int r = static_cast<int>(u / KT);
-      const int kt = static_cast<int>(u - static_cast<int64_t>(r) * KT);
-      load8_bf16(x, u < units ? r : M, M, K, ldx, kt * 256 + lane * 8, vec_ok, v[j]);
+      const int rr = r + j * R;
+      v[j] = load8_words(x, rr < rows ? rr : M, M, K, ldx, e0, vec_ok);
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int64_t u = u0 + j * nwarps;
-      if (u >= units) break;     // warp-uniform
-      const int r = static_cast<int>(u / KT);
-      const int kt = static_cast<int>(u - static_cast<int64_t>(r) * KT);
+      const int rr = r + j * R;
+      if (rr >= rows) break;     // warp-uniform
       uint32_t sbyte;
-      const uint32_t packed = quantize8(v[j], sbyte);
-      store_act8<kLayout>(codes, scales, r, M, K, KT, block_rows, kt * 32 + lane, (lane & 3) == 0, packed, sbyte);
+      const uint32_t packed = quantize8_words(v[j], sbyte);
+      store_act8<kLayout>(codes, scales, rr, M, K, KT, block_rows, kt * 32 + lane, (lane & 3) == 0, packed, sbyte);
     }
   }
 }
@@ -194,14 +191,17 @@ static cudaError_t launch_dependent(Kern k, int grid, cudaStream_t s, Args... ar
   return cudaLaunchKernelEx(&cfg, k, args...);
 }
 
+// Warps per k-tile column (R) and blocks for `rows` rows of KT k-tiles.
 // Decode-sized inputs (a few rows): at most one 256-thread CTA per SM, which
 // fits next to a resident GEMM CTA, so the whole grid starts (and triggers
 // its dependent GEMM) at once.  Larger inputs: up to eight CTAs per SM.
-static int quant_grid(int64_t units, int M, const DeviceInfo& dev) {
-  int64_t blocks = (units + 7) / 8;
-  const int64_t cap = static_cast<int64_t>(dev.sm_count) * (M <= kDecodeMaxM ? 1 : 8);
-  if (blocks > cap) blocks = cap;
-  return static_cast<int>(blocks < 1 ? 1 : blocks);
+static void quant_grid(int rows, int KT, int M, const DeviceInfo& dev, int* R, int* blocks) {
+  const int64_t target_warps = static_cast<int64_t>(dev.sm_count) * (M <= kDecodeMaxM ? 1 : 8) * 8;
+  int64_t r = target_warps / KT;
+  if (r > rows) r = rows;
+  if (r < 1) r = 1;
+  *R = static_cast<int>(r);
+  *blocks = static_cast<int>((static_cast<int64_t>(KT) * r + 7) / 8);
 }
 
 cudaError_t launch_quant(const void* x, int M, int K, int ldx, uint8_t* codes, uint8_t* scales, ActLayout layout,
@@ -209,23 +209,24 @@ cudaError_t launch_quant(const void* x, int M, int K, int ldx, uint8_t* codes, u
   const bool vec_ok = (reinterpret_cast<uintptr_t>(x) & 15) == 0 && (ldx % 8) == 0;
   const uint16_t* xs = static_cast<const uint16_t*>(x);
   const int KT = static_cast<int>(padded_k(K) / kKTile);
+  int R = 1, grid = 1;
   if (layout == ActLayout::kTiled) {
     const int rows = rows_arg > 0 ? rows_arg : static_cast<int>(padded_rows(M));
-    const int grid = quant_grid(static_cast<int64_t>(rows) * KT, M, dev);
+    quant_grid(rows, KT, M, dev, &R, &grid);
     return launch_dependent(quant_kernel<ActLayout::kTiled>, grid, s, xs, M, K, ldx, codes, scales, rows, KT, vec_ok,
-                            0);
+                            0, R);
   }
   if (layout == ActLayout::kBlocked) {
     if (rows_arg <= 0 || rows_arg > kRowTile || (rows_arg < kRowTile && M > rows_arg)) return cudaErrorInvalidValue;
     const int rows = rows_arg == kRowTile ? static_cast<int>(padded_rows(M)) : rows_arg;
-    const int grid = quant_grid(static_cast<int64_t>(rows) * KT, M, dev);
+    quant_grid(rows, KT, M, dev, &R, &grid);
     return launch_dependent(quant_kernel<ActLayout::kBlocked>, grid, s, xs, M, K, ldx, codes, scales, rows, KT,
-                            vec_ok, rows_arg);
+                            vec_ok, rows_arg, R);
   }
   const int KTr = static_cast<int>(ceil_div(K, kKTile));
-  const int grid = quant_grid(static_cast<int64_t>(M) * KTr, M, dev);
+  quant_grid(M, KTr, M, dev, &R, &grid);
   return launch_dependent(quant_kernel<ActLayout::kRowMajor>, grid, s, xs, M, K, ldx, codes, scales, M, KTr, vec_ok,
-                          0);
+                          0, R);
 }
 
 // Empty kernel launched (normally) after the repack: a programmatic

@@ -148,20 +148,4 @@ __device__ __forceinline__ uint32_t quantize32_words(const uint4 (&v)[4], uint4&
   return sbyte;
 }
 
-// Same for 8 values given one by one.
-__device__ __forceinline__ uint32_t quantize8(const uint16_t (&v)[8], uint32_t& sbyte) {
-  const uint4 w = make_uint4(v[0] | (static_cast<uint32_t>(v[1]) << 16), v[2] | (static_cast<uint32_t>(v[3]) << 16),
-                             v[4] | (static_cast<uint32_t>(v[5]) << 16), v[6] | (static_cast<uint32_t>(v[7]) << 16));
-  return quantize8_words(w, sbyte);
-}
-
-// Loads this lane's 8 bf16 values of row r, elements [e0, e0 + 8) (zeros past
-// K or for r >= M).
-__device__ __forceinline__ void load8_bf16(const uint16_t* __restrict__ x, int r, int M, int K, int ldx, int e0,
-                                           bool vec_ok, uint16_t (&v)[8]) {
-  const uint4 q = load8_words(x, r, M, K, ldx, e0, vec_ok);
-  v[0] = q.x & 0xFFFF; v[1] = q.x >> 16; v[2] = q.y & 0xFFFF; v[3] = q.y >> 16;
-  v[4] = q.z & 0xFFFF; v[5] = q.z >> 16; v[6] = q.w & 0xFFFF; v[7] = q.w >> 16;
-}
-
 }  // namespace mx
