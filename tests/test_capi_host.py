@@ -37,6 +37,12 @@ def test_every_declared_symbol_is_exported(capi):
         assert hasattr(capi.lib, name), name
 
 
+def test_every_declared_symbol_has_a_binding(capi):
+    # the thin binding carries the header's names (size queries and calls alike)
+    for name in declared_functions():
+        assert callable(getattr(capi, name, None)), name
+
+
 def test_abi_version_and_status_strings(capi):
     assert capi.mxfp4_abi_version() == 2
     for s in range(8):

@@ -134,13 +134,34 @@ def test_bmm_op_matches_capi(capi, batch_major):
 
 
 def test_opcheck_schema_and_fake(capi):
+    """Every operator: schema checks, and the fake kernel's outputs match the
+    real kernel's in shape, dtype and strides."""
     M, N, K = 5, 300, 1024
     x, wc, ws, b = problem(M, N, K, seed=9)
     packed = pack_weights(capi, wc, ws, K)
-    torch.library.opcheck(torch.ops.mxfp4.linear.default, (dev_bf16(x), packed, dev_bf16(b), N),
-                          test_utils=("test_schema", "test_faketensor"))
-    torch.library.opcheck(torch.ops.mxfp4.quant_act.default, (dev_bf16(x), 1),
-                          test_utils=("test_schema", "test_faketensor"))
+    xd, bd = dev_bf16(x), dev_bf16(b)
+    utils = ("test_schema", "test_faketensor")
+    torch.library.opcheck(torch.ops.mxfp4.linear.default, (xd, packed, bd, N), test_utils=utils)
+    torch.library.opcheck(torch.ops.mxfp4.linear_mxfp4_out.default, (xd, packed, bd, N), test_utils=utils)
+    for layout in (0, 1):
+        torch.library.opcheck(torch.ops.mxfp4.quant_act.default, (xd, layout), test_utils=utils)
+        codes, scales = torch.ops.mxfp4.quant_act(xd, layout)
+        torch.library.opcheck(torch.ops.mxfp4.linear_prequant.default, (codes, scales, layout, packed, bd, M, N, K),
+                              test_utils=utils)
+        torch.library.opcheck(torch.ops.mxfp4.rmsnorm_quant_act.default,
+                              (xd, dev_bf16(synth.norm_gamma(K, seed=9)), 1e-6, layout, None), test_utils=utils)
+    # the residual form: the schema check also confirms that only the declared
+    # argument is written
+    torch.library.opcheck(torch.ops.mxfp4.rmsnorm_quant_act.default,
+                          (xd, dev_bf16(synth.norm_gamma(K, seed=9)), 1e-6, 0, dev_bf16(synth.residual(M, K, seed=9))),
+                          test_utils=utils)
+    torch.library.opcheck(torch.ops.mxfp4.pack_weights.default, (dev_u8(wc), dev_u8(ws), K), test_utils=utils)
+    B = 2
+    xb = dev_bf16(synth.bmm_activations(B, 7, 192, seed=9))
+    pb = pack_weights(capi, synth.weight_codes(256, 192, seed=9, batch=B),
+                      synth.weight_scales(256, 192, -6, 0, seed=9, batch=B), 192)
+    for bm in (False, True):
+        torch.library.opcheck(torch.ops.mxfp4.a16wfp4_bmm.default, (xb, pb, 256, bm), test_utils=utils)
 
 
 def test_compiled_layer_matches_eager(capi):
