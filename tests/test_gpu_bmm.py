@@ -60,3 +60,19 @@ def test_bmm_small_shapes(capi, B, M, N, K, batch_major):
     acc, mag = ref.a16wfp4_bmm_f64(ref.bf16_bits_to_f64(x), wc, ws, K)
     got_bmn = got.transpose(1, 0, 2) if batch_major else got
     check_close(got_bmn, acc, mag, -(-K // 16) + 2)
+
+
+@pytest.mark.parametrize("B,M,N,K", [(185, 600, 128, 64), (89, 700, 300, 192)])
+@pytest.mark.parametrize("batch_major", [False, True])
+def test_bmm_more_pairs_than_sms(capi, B, M, N, K, batch_major):
+    """More (batch, weight tile) pairs than a GB300 has SMs (178 and 185
+    against 152), several M tiles each, ragged M and N: the grid runs in two
+    waves of one-CTA-per-SM blocks.  Every output is compared."""
+    x = synth.bmm_activations(B, M, K, seed=B + M)
+    wc = synth.weight_codes(N, K, seed=N + 1, batch=B)
+    ws = synth.weight_scales(N, K, -8, 2, seed=N + 1, batch=B)
+    packed = pack_weights(capi, wc, ws, K)
+    got = run_bmm(capi, x, packed, B, M, N, K, batch_major)
+    acc, mag = ref.a16wfp4_bmm_f64(ref.bf16_bits_to_f64(x), wc, ws, K)
+    got_bmn = got.transpose(1, 0, 2) if batch_major else got
+    check_close(got_bmn, acc, mag, -(-K // 16) + 2)
