@@ -789,13 +789,18 @@ def run_single(args):
     pks = [pk] + [pk.clone() for _ in range(args.copies - 1)]
     x = synth.bf16_tensor(synth.activations(M, K, seed=1, outlier_frac=0.01)).cuda()
     out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    codes = torch.empty(M * (N // 2), dtype=torch.uint8, device="cuda")
+    scales = torch.empty(M * ceil_div(N, 32), dtype=torch.uint8, device="cuda")
     wsb = capi.mxfp4_gemm_workspace_bytes(M, N, K)
     work = torch.zeros(wsb, dtype=torch.uint8, device="cuda")
     for i in range(args.calls):
-        capi.mxfp4_gemm(x, K, None, None, 0, pks[i % len(pks)], None, out, N, M, N, K, work, wsb)
+        if args.mxfp4_out:
+            capi.mxfp4_gemm_mxfp4_out(x, K, None, None, 0, pks[i % len(pks)], None, codes, scales, M, N, K, work, wsb)
+        else:
+            capi.mxfp4_gemm(x, K, None, None, 0, pks[i % len(pks)], None, out, N, M, N, K, work, wsb)
     torch.cuda.synchronize()
     assert capi.mxfp4_get_device_error() == capi.OK
-    print(f"single {M},{N},{K}: {args.calls} calls ok")
+    print(f"single {M},{N},{K}{' (MXFP4 out)' if args.mxfp4_out else ''}: {args.calls} calls ok")
 
 
 def main():
@@ -814,6 +819,8 @@ def main():
                     help="profiling mode: kup,M or vup,M of one A16WFP4 BMM call, no JSON line")
     ap.add_argument("--single-norm", type=str, default=None,
                     help="profiling mode: M or M,res of one fused RMSNorm -> MXFP4 call (K = 5120), no JSON line")
+    ap.add_argument("--mxfp4-out", action="store_true",
+                    help="with --single: the MXFP4 output form (mxfp4_gemm_mxfp4_out)")
     ap.add_argument("--calls", type=int, default=6)
     ap.add_argument("--copies", type=int, default=4)
     args = ap.parse_args()
