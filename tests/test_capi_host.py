@@ -151,3 +151,22 @@ def test_valid_call_without_device_reports_no_device(capi):
     A = 1 << 20
     st = capi.lib.mxfp4_quant_act(A, 4, 32, 32, A, A, 0, None)
     assert st in (capi.ERR_NO_DEVICE, capi.ERR_CUDA)
+
+
+def test_noalloc_gemm_argument_checks(capi):
+    lib, A = capi.lib, 1 << 20
+    f = lib.mxfp4_gemm_noalloc
+    cap = capi.mxfp4_gemm_noalloc_max_scratch_bytes()
+    assert cap == 48 << 20
+    assert f(None, 64, A, None, A, 8, 4, 8, 64, None) == capi.ERR_INVALID_ARG
+    assert f(A, 64, None, None, A, 8, 4, 8, 64, None) == capi.ERR_INVALID_ARG
+    assert f(A, 64, A, None, None, 8, 4, 8, 64, None) == capi.ERR_INVALID_ARG
+    assert f(A, 64, A, None, A, 8, 0, 8, 64, None) == capi.ERR_INVALID_ARG
+    # a problem whose scratch exceeds the fixed array is refused before any device use
+    M, N, K = 8192, 34816, 5120
+    assert capi.mxfp4_gemm_workspace_bytes(M, N, K) > cap
+    assert f(A, K, A, None, A, N, M, N, K, None) == capi.ERR_WORKSPACE
+    # a valid small call reaches the device query (only without a GPU: the
+    # fake addresses must never reach a kernel)
+    if not torch.cuda.is_available():
+        assert f(A, 64, A, None, A, 8, 4, 8, 64, None) in (capi.ERR_NO_DEVICE, capi.ERR_CUDA)
