@@ -140,3 +140,33 @@ def test_bmm_matches_exact_brute_force_and_layouts():
                 if acc != 0:
                     assert got[b, m, n] == bf16_bits_exact(acc)
                 assert got_mbn[m, b, n] == got[b, m, n]
+
+
+def _permute_blocks(codes, scales, perm):
+    """Reorder the 32-element K blocks of [R, K/2] codes and [R, K/32] scales."""
+    R, nb = scales.shape
+    c = codes.reshape(R, nb, 16)[:, perm, :].reshape(R, nb * 16)
+    return np.ascontiguousarray(c), np.ascontiguousarray(scales[:, perm])
+
+
+def test_consistent_permutations_commute_with_the_gemm():
+    """At a size past brute force: reordering the K blocks of both operands
+    the same way leaves every sum unchanged (each product is an exact dyadic
+    rational and the sums stay exact in float64 here), and reordering the
+    weight rows reorders the output columns.  A transposed operand, a wrong
+    block index or a scale read from the wrong row breaks one of them."""
+    M, N, K = 7, 40, 2048
+    g = np.random.default_rng(12)
+    a_c = synth.weight_codes(M, K, 12, 1)
+    a_s = synth.weight_scales(M, K, -4, 2, 12, 2)
+    w_c = synth.weight_codes(N, K, 12, 3)
+    w_s = synth.weight_scales(N, K, -8, 0, 12, 4)
+    base = ref.mxfp4_gemm_f64(a_c, a_s, w_c, w_s, K)[0]
+    perm = g.permutation(K // 32)
+    pa = _permute_blocks(a_c, a_s, perm)
+    pw = _permute_blocks(w_c, w_s, perm)
+    assert np.array_equal(ref.mxfp4_gemm_f64(*pa, *pw, K)[0], base)
+    rows = g.permutation(N)
+    assert np.array_equal(ref.mxfp4_gemm_f64(a_c, a_s, w_c[rows], w_s[rows], K)[0], base[:, rows])
+    # permuting only one operand's blocks changes the result (the test can fail)
+    assert not np.array_equal(ref.mxfp4_gemm_f64(*pa, w_c, w_s, K)[0], base)
