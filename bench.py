@@ -803,6 +803,91 @@ def run_single(args):
     print(f"single {M},{N},{K}{' (MXFP4 out)' if args.mxfp4_out else ''}: {args.calls} calls ok")
 
 
+# name, pair (cta_group::2), kind (0 mxf4, 1 bf16), N, MMAs per step, scale copies per step, copy form
+# (0: 32x128b.warpx4, 1: 128x256b).  A step of the 1-CTA GEMM kernels today is
+# "mxf4 1cta 128x256 x4 + 6 cp"; the others bound what a different tile or a CTA pair could issue.
+TC_RATE_VARIANTS = (
+    ("mxf4 1cta 128x256 x4", 0, 0, 256, 4, 0, 0),
+    ("mxf4 1cta 128x256 x4 + 6 cp", 0, 0, 256, 4, 6, 0),
+    ("mxf4 1cta 128x256 x4 + 4 cp", 0, 0, 256, 4, 4, 0),
+    ("mxf4 1cta 128x256 x4 + 2 cp", 0, 0, 256, 4, 2, 0),
+    ("mxf4 1cta 128x256 x4 + 2 cp128x256b", 0, 0, 256, 4, 2, 1),
+    ("mxf4 1cta 128x128 x4", 0, 0, 128, 4, 0, 0),
+    ("mxf4 1cta 128x64 x8", 0, 0, 64, 8, 0, 0),
+    ("mxf4 1cta 128x64 x8 + 6 cp", 0, 0, 64, 8, 6, 0),
+    ("mxf4 2cta 256x256 x4", 1, 0, 256, 4, 0, 0),
+    ("mxf4 2cta 256x256 x4 + 6 cp", 1, 0, 256, 4, 6, 0),
+    ("mxf4 2cta 256x256 x4 + 4 cp", 1, 0, 256, 4, 4, 0),
+    ("mxf4 2cta 256x256 x4 + 2 cp", 1, 0, 256, 4, 2, 0),
+    ("mxf4 2cta 256x128 x4", 1, 0, 128, 4, 0, 0),
+    ("mxf4 2cta 256x64 x4", 1, 0, 64, 4, 0, 0),
+    ("mxf4 2cta 256x64 x4 + 3 cp", 1, 0, 64, 4, 3, 0),
+    ("bf16 1cta 128x256 x4", 0, 1, 256, 4, 0, 0),
+    ("bf16 2cta 256x256 x4", 1, 1, 256, 4, 0, 0),
+)
+
+
+def run_tc_rates(args):
+    """Tensor-pipe issue rates of the instruction mixes above on every SM at once
+    (mxfp4_diag_tensor_rate), and the dense FP4 rate they imply; one JSON line."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from mxfp4_quantized_gemm_gb300 import capi
+    dev = torch.device("cuda", 0)
+    props = torch.cuda.get_device_properties(dev)
+    ns = torch.zeros(capi.mxfp4_diag_max_units(), dtype=torch.int64, device=dev)
+    addr = torch.zeros(2, dtype=torch.int32, device=dev)
+    capi.mxfp4_diag_pair_alloc_probe(addr)
+    torch.cuda.synchronize()
+    a = [int(v) & 0xFFFFFFFF for v in addr.cpu().tolist()]
+    cols = [v & 0x3FFFFFFF for v in a]
+    ranks = sorted(v >> 30 for v in a)
+    pair_ok = cols[0] == cols[1] and ranks == [0, 1]
+    steps = args.tc_steps
+    clocks = ClockSampler(0)
+    clocks.start()
+    rows = []
+    for name, pair, kind, n, mmas, copies, form in TC_RATE_VARIANTS:
+        if pair and not pair_ok:
+            rows.append({"name": name, "skipped": "cta_group::2 allocation is not collective"})
+            continue
+        m = 256 if pair else 128
+        k = 64 if kind == 0 else 16
+        meds = []
+        for _ in range(3):
+            ns.zero_()
+            units = capi.mxfp4_diag_tensor_rate(pair, kind, n, mmas, copies, form, steps, ns)
+            torch.cuda.synchronize()
+            v = [x for x in ns[:units].cpu().tolist() if x > 0]
+            if len(v) != units:
+                raise RuntimeError(f"{name}: {units - len(v)} units timed out")
+            meds.append(statistics.median(v))
+        med = statistics.median(meds)
+        ns_step = med / steps
+        flop = units * mmas * 2.0 * m * n * k * steps
+        rows.append({"name": name, "units": units, "ns_per_step": round(ns_step, 1),
+                     "ns_per_mma": round(ns_step / mmas, 1),
+                     "ns_per_copy_over_mma_only": None,
+                     "tflops": round(flop / (med * 1e-9) / 1e12, 1)})
+    clk = clocks.stop()
+    base = {r["name"]: r["ns_per_step"] for r in rows if "ns_per_step" in r}
+    for r in rows:
+        nm = r["name"]
+        if "+" in nm and "ns_per_step" in r:
+            ref = base.get(nm.split(" +")[0])
+            cp = int(nm.split("+ ")[1].split(" ")[0])
+            if ref is not None and cp:
+                r["ns_per_copy_over_mma_only"] = round((r["ns_per_step"] - ref) / cp, 1)
+    fp4 = [r["tflops"] for r in rows if r["name"].startswith("mxf4") and "+" not in r["name"] and "tflops" in r]
+    bf16 = [r["tflops"] for r in rows if r["name"].startswith("bf16") and "tflops" in r]
+    print(json.dumps({"tc_rates": rows, "pair_alloc": {"cols": cols, "collective": pair_ok},
+                      "mxf4_dense_peak_tflops": max(fp4) if fp4 else None,
+                      "bf16_dense_peak_tflops": max(bf16) if bf16 else None,
+                      "sms": props.multi_processor_count, "steps": steps, "clocks": clk}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -821,9 +906,15 @@ def main():
                     help="profiling mode: M or M,res of one fused RMSNorm -> MXFP4 call (K = 5120), no JSON line")
     ap.add_argument("--mxfp4-out", action="store_true",
                     help="with --single: the MXFP4 output form (mxfp4_gemm_mxfp4_out)")
+    ap.add_argument("--tc-rates", action="store_true",
+                    help="measure tensor-pipe issue rates (scale copies, MMAs, CTA pairs) and print one JSON line")
+    ap.add_argument("--tc-steps", type=int, default=4000)
     ap.add_argument("--calls", type=int, default=6)
     ap.add_argument("--copies", type=int, default=4)
     args = ap.parse_args()
+    if args.tc_rates:
+        run_tc_rates(args)
+        return
     if args.single:
         run_single(args)
         return

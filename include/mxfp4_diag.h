@@ -1,0 +1,61 @@
+/*
+ * mxfp4_diag.h — diagnostic entry points of the GB300 MXFP4 library.
+ *
+ * These calls measure the hardware the GEMM kernels run on; they compute
+ * nothing of the MXFP4 linear and are not part of its path.  The paper pages
+ * have no counterpart: they quote no kernel-level rates (the speed tests of
+ * sglang PR #39598 "[AMD] Add opt-in AITER ASM FP4 GEMM for Quark dense
+ * linear" are left as a TODO), so the dense FP4 tensor-core rate the GEMM's
+ * roofline is quoted against is measured here.
+ *
+ * Conventions as in mxfp4.h: device pointers are the caller's, every call is
+ * asynchronous on `stream` (a cudaStream_t), argument checks return a status
+ * before any launch.
+ */
+#ifndef MXFP4_GB300_DIAG_H
+#define MXFP4_GB300_DIAG_H
+
+#include "mxfp4.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Largest number of measuring units (CTAs, or CTA pairs) one
+ * mxfp4_diag_tensor_rate launch reports: the size of its ns_dev buffer. */
+MXFP4_API int mxfp4_diag_max_units(void);
+
+/* Tensor-pipe issue rate of one instruction mix, on every SM at once.
+ *
+ * Each unit (one CTA per SM, or with pair = 1 one 2-CTA cluster issuing
+ * cta_group::2 instructions) issues `steps` steps back to back after 16
+ * untimed ones; a step is `copies` scale copies (shared memory -> TMEM;
+ * copy_form 0: tcgen05.cp.32x128b.warpx4, 1: tcgen05.cp.128x256b) then
+ * `mmas` MMAs of shape M x mma_n x K into one TMEM accumulator (kind 0:
+ * kind::mxf4.block_scale.scale_vec::2X, E2M1 x E2M1 with UE8M0 scales,
+ * K = 64; kind 1: kind::f16, bf16 x bf16, K = 16; M = 128, or 256 for a
+ * pair), committed to a ring of four mbarriers with a wait on the commit of
+ * the step four back.  Operands are zero bytes.
+ *
+ * ns_dev: device buffer of mxfp4_diag_max_units() uint64; unit u's elapsed
+ * nanoseconds for the timed steps (%globaltimer) land in ns_dev[u], or 0 if a
+ * bounded wait gave up.  *units (host) receives the number of units launched.
+ * Arguments: mma_n a multiple of 16 in [16, 256] ([64, 256] for a pair),
+ * 1 <= mmas <= 16, 0 <= copies <= 8 (form 0) or 4 (form 1), no copies with
+ * kind 1, 1 <= steps <= 10^6; otherwise MXFP4_ERR_INVALID_ARG. */
+MXFP4_API mxfp4_status mxfp4_diag_tensor_rate(int pair, int kind, int mma_n, int mmas, int copies, int copy_form,
+                                              int steps, unsigned long long* ns_dev, int* units, void* stream);
+
+/* One 2-CTA cluster whose CTAs each take 32 TMEM columns with
+ * tcgen05.alloc.cta_group::2 (one warp per CTA, as that form requires) and
+ * free them again.  addr_dev (device, 2 uint32) receives each CTA's column
+ * address with its cluster rank in bits 30..31: equal addresses show that
+ * the pair allocated together, which the pair forms of
+ * mxfp4_diag_tensor_rate rely on. */
+MXFP4_API mxfp4_status mxfp4_diag_pair_alloc_probe(uint32_t* addr_dev, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP4_GB300_DIAG_H */

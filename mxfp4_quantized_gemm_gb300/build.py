@@ -18,7 +18,7 @@ BUILD_DIR = os.path.join(PKG_DIR, "_build")
 INCLUDE_DIR = os.path.join(os.path.dirname(PKG_DIR), "include")
 LIB_NAME = "libmxfp4_gb300.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
-SOURCES = ("quant.cu", "norm_quant.cu", "gemm.cu", "decode.cu", "bmm.cu", "capi.cu", "noalloc.cu")
+SOURCES = ("quant.cu", "norm_quant.cu", "gemm.cu", "decode.cu", "bmm.cu", "capi.cu", "noalloc.cu", "tc_rate.cu")
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
@@ -46,7 +46,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
     nvcc = _nvcc()
     os.makedirs(BUILD_DIR, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
-    headers.append(os.path.join(os.path.dirname(PKG_DIR), "include", "mxfp4.h"))
+    headers += [os.path.join(INCLUDE_DIR, f) for f in os.listdir(INCLUDE_DIR) if f.endswith(".h")]
 
     def compile_one(src: str) -> str:
         s = os.path.join(CSRC, src)

@@ -45,6 +45,9 @@ _SIGNATURES = {
     "mxfp4_get_device_error": (_i, [_p]),
     "mxfp4_gemm_noalloc": (_i, [_p, _i, _p, _p, _p, _i, _i, _i, _i, _p]),
     "mxfp4_gemm_noalloc_max_scratch_bytes": (_sz, []),
+    "mxfp4_diag_max_units": (_i, []),
+    "mxfp4_diag_tensor_rate": (_i, [_i, _i, _i, _i, _i, _i, _i, _p, ctypes.POINTER(_i), _p]),
+    "mxfp4_diag_pair_alloc_probe": (_i, [_p, _p]),
 }
 for _name, (_res, _args) in _SIGNATURES.items():
     _fn = getattr(lib, _name)
@@ -155,3 +158,24 @@ def mxfp4_gemm_noalloc_max_scratch_bytes() -> int:
 
 def mxfp4_get_device_error(stream=None) -> int:
     return lib.mxfp4_get_device_error(_stream(stream))
+
+
+# ---- diagnostics (include/mxfp4_diag.h): measurements of the hardware, not the linear
+
+def mxfp4_diag_max_units() -> int:
+    return lib.mxfp4_diag_max_units()
+
+
+def mxfp4_diag_tensor_rate(pair: int, kind: int, mma_n: int, mmas: int, copies: int, copy_form: int, steps: int,
+                           ns_dev, stream=None) -> int:
+    """Launches the issue-rate measurement; returns the number of units (CTAs or pairs) whose
+    elapsed nanoseconds land in ``ns_dev`` once the stream has finished."""
+    units = _i(0)
+    _check(lib.mxfp4_diag_tensor_rate(pair, kind, mma_n, mmas, copies, copy_form, steps, _ptr(ns_dev),
+                                      ctypes.byref(units), _stream(stream)),
+           "mxfp4_diag_tensor_rate")
+    return units.value
+
+
+def mxfp4_diag_pair_alloc_probe(addr_dev, stream=None) -> None:
+    _check(lib.mxfp4_diag_pair_alloc_probe(_ptr(addr_dev), _stream(stream)), "mxfp4_diag_pair_alloc_probe")
