@@ -804,26 +804,26 @@ def run_single(args):
 
 
 # name, pair (cta_group::2), kind (0 mxf4, 1 bf16), N, MMAs per step, scale copies per step, copy form
-# (0: 32x128b.warpx4, 1: 128x256b).  A step of the 1-CTA GEMM kernels today is
-# "mxf4 1cta 128x256 x4 + 6 cp"; the others bound what a different tile or a CTA pair could issue.
-TC_RATE_VARIANTS = (
-    ("mxf4 1cta 128x256 x4", 0, 0, 256, 4, 0, 0),
-    ("mxf4 1cta 128x256 x4 + 6 cp", 0, 0, 256, 4, 6, 0),
-    ("mxf4 1cta 128x256 x4 + 4 cp", 0, 0, 256, 4, 4, 0),
-    ("mxf4 1cta 128x256 x4 + 2 cp", 0, 0, 256, 4, 2, 0),
-    ("mxf4 1cta 128x256 x4 + 2 cp128x256b", 0, 0, 256, 4, 2, 1),
-    ("mxf4 1cta 128x128 x4", 0, 0, 128, 4, 0, 0),
-    ("mxf4 1cta 128x64 x8", 0, 0, 64, 8, 0, 0),
-    ("mxf4 1cta 128x64 x8 + 6 cp", 0, 0, 64, 8, 6, 0),
-    ("mxf4 2cta 256x256 x4", 1, 0, 256, 4, 0, 0),
-    ("mxf4 2cta 256x256 x4 + 6 cp", 1, 0, 256, 4, 6, 0),
-    ("mxf4 2cta 256x256 x4 + 4 cp", 1, 0, 256, 4, 4, 0),
-    ("mxf4 2cta 256x256 x4 + 2 cp", 1, 0, 256, 4, 2, 0),
-    ("mxf4 2cta 256x128 x4", 1, 0, 128, 4, 0, 0),
-    ("mxf4 2cta 256x64 x4", 1, 0, 64, 4, 0, 0),
-    ("mxf4 2cta 256x64 x4 + 3 cp", 1, 0, 64, 4, 3, 0),
-    ("bf16 1cta 128x256 x4", 0, 1, 256, 4, 0, 0),
-    ("bf16 2cta 256x256 x4", 1, 1, 256, 4, 0, 0),
+# (0: 32x128b.warpx4, 1: 128x256b), depth (steps in flight: the wait is on the commit `depth` steps
+# back).  A k-step of the 1-CTA GEMM kernels is "mxf4 1cta 128x256 x4 + 6 cp"; depth 4 is the round
+# trip of a 4-stage ring, depth 32 leaves only the tensor pipe's throughput.
+TC_RATE_VARIANTS = tuple(
+    [(f"mxf4 1cta 128x256 x4 d{d}", 0, 0, 256, 4, 0, 0, d) for d in (1, 2, 4, 8, 16, 32)]
+    + [(f"mxf4 1cta 128x256 x4 + 6 cp d{d}", 0, 0, 256, 4, 6, 0, d) for d in (4, 8, 16, 32)]
+    + [(f"mxf4 1cta 128x256 x4 + 4 cp d{d}", 0, 0, 256, 4, 4, 0, d) for d in (8, 32)]
+    + [(f"mxf4 1cta 128x256 x4 + 2 cp128x256b d{d}", 0, 0, 256, 4, 2, 1, d) for d in (8, 32)]
+    + [(f"mxf4 1cta 6 cp only d{d}", 0, 0, 256, 0, 6, 0, d) for d in (8, 32)]
+    + [(f"mxf4 1cta 128x128 x4 d{d}", 0, 0, 128, 4, 0, 0, d) for d in (32,)]
+    + [(f"mxf4 1cta 128x64 x8 d{d}", 0, 0, 64, 8, 0, 0, d) for d in (32,)]
+    + [(f"mxf4 1cta 128x64 x8 + 6 cp d{d}", 0, 0, 64, 8, 6, 0, d) for d in (8, 32)]
+    + [(f"mxf4 2cta 256x256 x4 d{d}", 1, 0, 256, 4, 0, 0, d) for d in (4, 8, 16, 32)]
+    + [(f"mxf4 2cta 256x256 x4 + 6 cp d{d}", 1, 0, 256, 4, 6, 0, d) for d in (4, 8, 16, 32)]
+    + [(f"mxf4 2cta 256x256 x4 + 4 cp d{d}", 1, 0, 256, 4, 4, 0, d) for d in (8, 32)]
+    + [(f"mxf4 2cta 256x128 x4 d{d}", 1, 0, 128, 4, 0, 0, d) for d in (32,)]
+    + [(f"mxf4 2cta 256x64 x4 d{d}", 1, 0, 64, 4, 0, 0, d) for d in (32,)]
+    + [(f"mxf4 2cta 256x64 x4 + 3 cp d{d}", 1, 0, 64, 4, 3, 0, d) for d in (8, 32)]
+    + [(f"bf16 1cta 128x256 x4 d{d}", 0, 1, 256, 4, 0, 0, d) for d in (4, 32)]
+    + [(f"bf16 2cta 256x256 x4 d{d}", 1, 1, 256, 4, 0, 0, d) for d in (4, 32)]
 )
 
 
@@ -849,7 +849,7 @@ def run_tc_rates(args):
     clocks = ClockSampler(0)
     clocks.start()
     rows = []
-    for name, pair, kind, n, mmas, copies, form in TC_RATE_VARIANTS:
+    for name, pair, kind, n, mmas, copies, form, depth in TC_RATE_VARIANTS:
         if pair and not pair_ok:
             rows.append({"name": name, "skipped": "cta_group::2 allocation is not collective"})
             continue
@@ -858,7 +858,7 @@ def run_tc_rates(args):
         meds = []
         for _ in range(3):
             ns.zero_()
-            units = capi.mxfp4_diag_tensor_rate(pair, kind, n, mmas, copies, form, steps, ns)
+            units = capi.mxfp4_diag_tensor_rate(pair, kind, n, mmas, copies, form, steps, depth, ns)
             torch.cuda.synchronize()
             v = [x for x in ns[:units].cpu().tolist() if x > 0]
             if len(v) != units:
@@ -867,19 +867,10 @@ def run_tc_rates(args):
         med = statistics.median(meds)
         ns_step = med / steps
         flop = units * mmas * 2.0 * m * n * k * steps
-        rows.append({"name": name, "units": units, "ns_per_step": round(ns_step, 1),
-                     "ns_per_mma": round(ns_step / mmas, 1),
-                     "ns_per_copy_over_mma_only": None,
+        rows.append({"name": name, "units": units, "depth": depth, "ns_per_step": round(ns_step, 1),
+                     "ns_per_mma": round(ns_step / mmas, 1) if mmas else None,
                      "tflops": round(flop / (med * 1e-9) / 1e12, 1)})
     clk = clocks.stop()
-    base = {r["name"]: r["ns_per_step"] for r in rows if "ns_per_step" in r}
-    for r in rows:
-        nm = r["name"]
-        if "+" in nm and "ns_per_step" in r:
-            ref = base.get(nm.split(" +")[0])
-            cp = int(nm.split("+ ")[1].split(" ")[0])
-            if ref is not None and cp:
-                r["ns_per_copy_over_mma_only"] = round((r["ns_per_step"] - ref) / cp, 1)
     fp4 = [r["tflops"] for r in rows if r["name"].startswith("mxf4") and "+" not in r["name"] and "tflops" in r]
     bf16 = [r["tflops"] for r in rows if r["name"].startswith("bf16") and "tflops" in r]
     print(json.dumps({"tc_rates": rows, "pair_alloc": {"cols": cols, "collective": pair_ok},

@@ -114,6 +114,19 @@ MXFP4_API size_t mxfp4_packed_weight_bytes(int batch, int N, int K);
 MXFP4_API mxfp4_status mxfp4_pack_weights(const uint8_t* w_codes_dev, const uint8_t* w_scales_dev,
                                 int batch, int N, int K, void* packed_dev, void* stream);
 
+/*
+ * Orders the GEMM and BMM calls issued next on `stream` after every write to
+ * packed weights already issued on it: one empty, ordinary kernel launch.
+ * Needed only when a packed weight buffer was written by something other
+ * than mxfp4_pack_weights (for example a device-to-device copy refreshing
+ * it) and the next kernel on the stream is a GEMM or BMM of this library,
+ * which would otherwise start reading the weights before that write has
+ * finished (see the weight-update contract of mxfp4_gemm).  No counterpart
+ * on the pages, whose weights are written once at load time.
+ * Errors: NO_DEVICE, CUDA.
+ */
+MXFP4_API mxfp4_status mxfp4_weights_updated(void* stream);
+
 /* Bytes of the activation codes / scales buffers for M rows x K elements. */
 MXFP4_API size_t mxfp4_act_code_bytes(int M, int K, mxfp4_layout layout);
 MXFP4_API size_t mxfp4_act_scale_bytes(int M, int K, mxfp4_layout layout);
@@ -203,11 +216,15 @@ MXFP4_API size_t mxfp4_gemm_workspace_bytes(int M, int N, int K);
  *                  any shape; calls sharing one must be ordered on the GPU.
  * For M <= 8 with a bf16 input the whole call is one kernel launch (each
  * thread block quantizes the activations of its own k-range); for
- * 8 < M <= 64 the activation quantizer runs first.  The GEMM kernel is a
- * programmatic dependent launch that reads the packed weights before the
- * previous kernel in the stream has finished: the weights must not be
- * written by the kernel immediately before the call (mxfp4_pack_weights
- * ends with a launch that keeps this true).
+ * 8 < M <= 64 the activation quantizer runs first.
+ * Weight-update contract: the GEMM kernel is a programmatic dependent launch
+ * that starts streaming the packed weights before the previous kernel in
+ * the stream has finished (only its activation, bias and output accesses
+ * wait for it).  So the packed weights must not be written by the kernel
+ * launched immediately before the call.  mxfp4_pack_weights keeps this true
+ * by itself; after writing a packed buffer any other way (a device copy, a
+ * foreign kernel), call mxfp4_weights_updated on the stream before the first
+ * GEMM or BMM that reads it.
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, WORKSPACE, CUDA.
  */
 MXFP4_API mxfp4_status mxfp4_gemm(const void* a_bf16_dev, int lda,
@@ -252,6 +269,8 @@ MXFP4_API mxfp4_status mxfp4_gemm_mxfp4_out(const void* a_bf16_dev, int lda,
  *   x_dev         bf16 [B][M][K], contiguous
  *   w_packed_dev  output of mxfp4_pack_weights(B, N, K)
  *   out_dev       bf16, B*M*N elements in out_layout order
+ * Weight-update contract: as for mxfp4_gemm (the weight tile is read and
+ * dequantized before the previous kernel in the stream has finished).
  * Errors: INVALID_ARG, UNSUPPORTED_SHAPE, MISALIGNED, CUDA.
  */
 MXFP4_API mxfp4_status a16wfp4_bmm(const void* x_dev, const void* w_packed_dev, void* out_dev,
@@ -267,12 +286,16 @@ MXFP4_API mxfp4_status a16wfp4_bmm(const void* x_dev, const void* w_packed_dev, 
  *
  * Same operation and arguments as mxfp4_gemm with a bf16 activation input;
  * the scratch comes from one fixed device array inside the library, of
- * mxfp4_gemm_noalloc_max_scratch_bytes() bytes (48 MiB), which every GPU that
- * uses it holds until the process exits.  A problem whose
+ * mxfp4_gemm_noalloc_max_scratch_bytes() bytes (48 MiB).  The array is
+ * reserved on every device where the library's module is loaded (with eager
+ * module loading, every device the process initialises, whether or not this
+ * entry point is ever called) and held until the process exits.  A problem whose
  * mxfp4_gemm_workspace_bytes(M, N, K) exceeds that size is rejected with
  * MXFP4_ERR_WORKSPACE.  Nothing is allocated or freed.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *     The address is kept for the process: resetting the device
+ *     (cudaDeviceReset) while the library is in use is not supported.
  *   - All calls share the one array and it keeps the last call's contents
  *     (no call needs it cleared); calls that overlap on the GPU — on
  *     different streams, or from several host threads without ordering —

@@ -34,17 +34,21 @@ MXFP4_API int mxfp4_diag_max_units(void);
  * `mmas` MMAs of shape M x mma_n x K into one TMEM accumulator (kind 0:
  * kind::mxf4.block_scale.scale_vec::2X, E2M1 x E2M1 with UE8M0 scales,
  * K = 64; kind 1: kind::f16, bf16 x bf16, K = 16; M = 128, or 256 for a
- * pair), committed to a ring of four mbarriers with a wait on the commit of
- * the step four back.  Operands are zero bytes.
+ * pair), each step committed to an mbarrier, with a wait on the commit of
+ * the step `depth` back before the next step is issued (depth 4: the round
+ * trip of a 4-stage pipeline ring; depth 32: nearly free issue, the tensor
+ * pipe's own rate).  Operands are zero bytes.
  *
  * ns_dev: device buffer of mxfp4_diag_max_units() uint64; unit u's elapsed
  * nanoseconds for the timed steps (%globaltimer) land in ns_dev[u], or 0 if a
  * bounded wait gave up.  *units (host) receives the number of units launched.
  * Arguments: mma_n a multiple of 16 in [16, 256] ([64, 256] for a pair),
- * 1 <= mmas <= 16, 0 <= copies <= 8 (form 0) or 4 (form 1), no copies with
- * kind 1, 1 <= steps <= 10^6; otherwise MXFP4_ERR_INVALID_ARG. */
+ * 0 <= mmas <= 16, 0 <= copies <= 8 (form 0) or 4 (form 1), at least one
+ * instruction per step, no copies with kind 1, 1 <= steps <= 10^6,
+ * 1 <= depth <= 32; otherwise MXFP4_ERR_INVALID_ARG. */
 MXFP4_API mxfp4_status mxfp4_diag_tensor_rate(int pair, int kind, int mma_n, int mmas, int copies, int copy_form,
-                                              int steps, unsigned long long* ns_dev, int* units, void* stream);
+                                              int steps, int depth, unsigned long long* ns_dev, int* units,
+                                              void* stream);
 
 /* One 2-CTA cluster whose CTAs each take 32 TMEM columns with
  * tcgen05.alloc.cta_group::2 (one warp per CTA, as that form requires) and

@@ -34,6 +34,7 @@ _SIGNATURES = {
     "mxfp4_status_string": (ctypes.c_char_p, [_i]),
     "mxfp4_packed_weight_bytes": (_sz, [_i, _i, _i]),
     "mxfp4_pack_weights": (_i, [_p, _p, _i, _i, _i, _p, _p]),
+    "mxfp4_weights_updated": (_i, [_p]),
     "mxfp4_act_code_bytes": (_sz, [_i, _i, _i]),
     "mxfp4_act_scale_bytes": (_sz, [_i, _i, _i]),
     "mxfp4_quant_act": (_i, [_p, _i, _i, _i, _p, _p, _i, _p]),
@@ -46,7 +47,7 @@ _SIGNATURES = {
     "mxfp4_gemm_noalloc": (_i, [_p, _i, _p, _p, _p, _i, _i, _i, _i, _p]),
     "mxfp4_gemm_noalloc_max_scratch_bytes": (_sz, []),
     "mxfp4_diag_max_units": (_i, []),
-    "mxfp4_diag_tensor_rate": (_i, [_i, _i, _i, _i, _i, _i, _i, _p, ctypes.POINTER(_i), _p]),
+    "mxfp4_diag_tensor_rate": (_i, [_i, _i, _i, _i, _i, _i, _i, _i, _p, ctypes.POINTER(_i), _p]),
     "mxfp4_diag_pair_alloc_probe": (_i, [_p, _p]),
 }
 for _name, (_res, _args) in _SIGNATURES.items():
@@ -119,6 +120,10 @@ def mxfp4_pack_weights(w_codes, w_scales, batch: int, N: int, K: int, packed, st
            "mxfp4_pack_weights")
 
 
+def mxfp4_weights_updated(stream=None) -> None:
+    _check(lib.mxfp4_weights_updated(_stream(stream)), "mxfp4_weights_updated")
+
+
 def mxfp4_quant_act(x, M: int, K: int, ldx: int, codes, scales, layout: int, stream=None) -> None:
     _check(lib.mxfp4_quant_act(_ptr(x), M, K, ldx, _ptr(codes), _ptr(scales), layout, _stream(stream)),
            "mxfp4_quant_act")
@@ -167,11 +172,11 @@ def mxfp4_diag_max_units() -> int:
 
 
 def mxfp4_diag_tensor_rate(pair: int, kind: int, mma_n: int, mmas: int, copies: int, copy_form: int, steps: int,
-                           ns_dev, stream=None) -> int:
+                           depth: int, ns_dev, stream=None) -> int:
     """Launches the issue-rate measurement; returns the number of units (CTAs or pairs) whose
     elapsed nanoseconds land in ``ns_dev`` once the stream has finished."""
     units = _i(0)
-    _check(lib.mxfp4_diag_tensor_rate(pair, kind, mma_n, mmas, copies, copy_form, steps, _ptr(ns_dev),
+    _check(lib.mxfp4_diag_tensor_rate(pair, kind, mma_n, mmas, copies, copy_form, steps, depth, _ptr(ns_dev),
                                       ctypes.byref(units), _stream(stream)),
            "mxfp4_diag_tensor_rate")
     return units.value

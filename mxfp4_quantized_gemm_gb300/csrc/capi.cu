@@ -105,6 +105,13 @@ size_t mxfp4_packed_weight_bytes(int batch, int N, int K) {
   return static_cast<size_t>(batch) * static_cast<size_t>(weight_packed_bytes(N, K));
 }
 
+mxfp4_status mxfp4_weights_updated(void* stream) {
+  DeviceInfo dev;
+  mxfp4_status st = device_ready(&dev);
+  if (st != MXFP4_OK) return st;
+  return from_cuda(launch_ordering(dev, static_cast<cudaStream_t>(stream)));
+}
+
 size_t mxfp4_act_code_bytes(int M, int K, mxfp4_layout layout) {
   if (M <= 0 || K <= 0 || (K & 1)) return 0;
   if (layout == MXFP4_LAYOUT_ROWMAJOR) return static_cast<size_t>(M) * (K / 2);

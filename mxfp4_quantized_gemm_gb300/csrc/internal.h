@@ -70,6 +70,9 @@ cudaError_t launch_pack(const uint8_t* codes, const uint8_t* scales, int batch, 
 // Row-major codes/scales -> packed weight blocks.
 cudaError_t launch_pack_weights(const uint8_t* codes, const uint8_t* scales, int batch, int N, int K,
                                 uint8_t* packed, const DeviceInfo& dev, cudaStream_t s);
+// An empty ordinary launch: programmatic dependents launched after it start
+// only once every earlier kernel on the stream has completed.
+cudaError_t launch_ordering(const DeviceInfo& dev, cudaStream_t s);
 uint32_t quant_read_clear_error();
 
 // gemm.cu

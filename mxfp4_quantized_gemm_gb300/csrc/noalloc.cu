@@ -9,12 +9,17 @@
 // (quantized activation codes and scales, stream-K partial sums) lives in one
 // file-scope device array of fixed size instead.
 //
-// The array exists on every GPU where this library's module is loaded, from
-// the first use on that device until the process exits.  Its address is
-// looked up once per device (on that device's first call) and handed to the
-// existing GEMM path; nothing here allocates or frees memory.
+// The array is reserved on every GPU where this library's module is loaded
+// (with eager module loading that is every device the process initialises,
+// even if this entry point is never called) and stays until the process
+// exits.  Its address is looked up once per device (on that device's first
+// call) and handed to the existing GEMM path; nothing here allocates or
+// frees memory.  The cached address belongs to the device's primary
+// context: resetting the device (cudaDeviceReset) while the library is in
+// use is not supported.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -28,19 +33,22 @@ constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(48) << 20;   // 48 M
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
 
-static void* g_noalloc_ptr[64];     // device address of the array, per device
+static std::atomic<void*> g_noalloc_ptr[64];   // device address of the array, per device
 static std::mutex g_noalloc_mutex;
 
 // Device address of the scratch array on the current device (looked up once
-// per device), or nullptr on failure.
+// per device, under a lock; later calls take the published address without
+// it), or nullptr on failure.
 static void* noalloc_scratch(int device) {
+  void* p = g_noalloc_ptr[device].load(std::memory_order_acquire);
+  if (p != nullptr) return p;
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (g_noalloc_ptr[device] == nullptr) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return nullptr;
-    g_noalloc_ptr[device] = ptr;
+  p = g_noalloc_ptr[device].load(std::memory_order_relaxed);
+  if (p == nullptr) {
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    g_noalloc_ptr[device].store(p, std::memory_order_release);
   }
-  return g_noalloc_ptr[device];
+  return p;
 }
 
 }  // namespace mx

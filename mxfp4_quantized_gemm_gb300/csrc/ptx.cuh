@@ -232,34 +232,4 @@ __device__ __forceinline__ void st_shared_f4(uint32_t addr, uint32_t a, uint32_t
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-// ------------------------------------------------- flags between CTAs (gpu scope)
-// Orders this thread's generic-proxy global accesses with its async-proxy
-// (bulk copy) accesses of global memory.
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-// Bounded wait until *p == want (acquire).  Returns false and sets `abort`
-// if that did not happen within kWaitCycles, or if `abort` was already set.
-__device__ __forceinline__ bool flag_wait(const uint32_t* p, uint32_t want, bool& abort) {
-  if (abort) return false;
-  if (ld_acquire_gpu(p) == want) return true;
-  const long long t0 = clock64();
-  while (ld_acquire_gpu(p) != want) {
-    if (clock64() - t0 > kWaitCycles) {
-      abort = true;
-      return false;
-    }
-    __nanosleep(64);
-  }
-  return true;
-}
-
 }  // namespace mx

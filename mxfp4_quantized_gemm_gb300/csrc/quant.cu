@@ -234,6 +234,12 @@ cudaError_t launch_quant(const void* x, int M, int K, int ldx, uint8_t* codes, u
 // its dependency wait, and this guarantees the repack has fully completed.
 __global__ void ordering_kernel() {}
 
+cudaError_t launch_ordering(const DeviceInfo& dev, cudaStream_t s) {
+  (void)dev;
+  ordering_kernel<<<1, 32, 0, s>>>();
+  return cudaGetLastError();
+}
+
 cudaError_t launch_pack(const uint8_t* codes, const uint8_t* scales, int batch, int R, int K, uint8_t* packed,
                         const DeviceInfo& dev, cudaStream_t s) {
   const int64_t cb = tiled_code_bytes(R, K), sb = tiled_scale_bytes(R, K);

@@ -3,8 +3,9 @@
 // One thread per CTA (or per CTA pair) issues the same tcgen05 sequence per
 // "step" back to back -- a number of scale copies (shared memory -> TMEM)
 // followed by a number of MMAs into one accumulator -- and commits each step
-// to a ring of four mbarriers, waiting for the commit of the step four back
-// before it issues the next, as the GEMM kernels' MMA threads do.  Operands
+// to a ring of mbarriers, waiting for the commit of the step `depth` back
+// before it issues the next: depth 4 is the round trip a 4-stage pipeline
+// ring allows, a large depth leaves only the tensor pipe's own throughput.  Operands
 // are zero bytes in shared memory: the rates of the tensor pipe do not
 // depend on the values.  %globaltimer brackets the timed steps, so each CTA
 // reports nanoseconds per step of its own issue stream; launching one CTA
@@ -32,6 +33,7 @@ constexpr int kRateWarm = 16;                  // untimed steps before the timed
 constexpr int kRateSmem = 200 * 1024;          // keeps one CTA per SM
 constexpr int kRateOperandBytes = 80 * 1024;   // A 16 KiB, B 32 KiB, scale sources 32 KiB
 constexpr uint32_t kRateTmemCols = 512;
+constexpr int kRateRing = 32;                  // commit barriers; the deepest wait is 32 steps back
 
 struct RateArgs {
   int pair;        // 1: cta_group::2 over a 2-CTA cluster
@@ -41,6 +43,7 @@ struct RateArgs {
   int copies;      // scale copies per step
   int copy_form;   // 0: 32x128b.warpx4, 1: 128x256b
   int steps;       // timed steps
+  int depth;       // wait for the commit of the step `depth` back (1..32)
   unsigned long long* ns;   // per unit (CTA or pair): ns of the timed steps, 0 after a timeout
 };
 
@@ -119,7 +122,7 @@ template <bool kPair>
 __global__ void __launch_bounds__(128, 1) tc_rate_kernel(const RateArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
-  __shared__ uint64_t ring[4];
+  __shared__ uint64_t ring[kRateRing];
   __shared__ uint64_t done;
   __shared__ uint32_t tmem_slot;
 
@@ -129,7 +132,7 @@ __global__ void __launch_bounds__(128, 1) tc_rate_kernel(const RateArgs a) {
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 4; ++s) mbar_init(&ring[s], 1);
+    for (int s = 0; s < kRateRing; ++s) mbar_init(&ring[s], 1);
     mbar_init(&done, 1);
     fence_mbar_init();
   }
@@ -157,8 +160,11 @@ __global__ void __launch_bounds__(128, 1) tc_rate_kernel(const RateArgs a) {
     const int M = kPair ? 256 : 128;
     const int total = kRateWarm + a.steps;
     for (int s = 0; s < total; ++s) {
-      const int slot = s & 3;
-      if (s >= 4 && !mbar_wait(&ring[slot], static_cast<uint32_t>((s >> 2) - 1) & 1u, abort)) break;
+      const int slot = s & 3;   // scale columns rotate over four slots (their values do not matter)
+      if (s >= a.depth) {
+        const int w = s - a.depth;
+        if (!mbar_wait(&ring[w % kRateRing], static_cast<uint32_t>(w / kRateRing) & 1u, abort)) break;
+      }
       tc_fence_after();
       if (s == kRateWarm) t0 = globaltimer();
       const uint32_t scol = tmem + 256u + static_cast<uint32_t>(slot) * 32u;
@@ -175,7 +181,7 @@ __global__ void __launch_bounds__(128, 1) tc_rate_kernel(const RateArgs a) {
         rate_mma<kPair>(a.kind, tmem, sdesc_sw128(a_s + 32u * q), sdesc_sw128(b_s + 32u * q), id,
                         scol + 4u * (q >> 1), scol + 16u + 8u * (q >> 1));
       }
-      rate_commit<kPair>(&ring[slot]);
+      rate_commit<kPair>(&ring[s % kRateRing]);
     }
     // Arrives (in both CTAs of a pair) once every MMA issued above is done.
     rate_commit<kPair>(&done);
@@ -256,19 +262,21 @@ extern "C" mxfp4_status mxfp4_diag_pair_alloc_probe(uint32_t* addr_dev, void* st
 }
 
 extern "C" mxfp4_status mxfp4_diag_tensor_rate(int pair, int kind, int mma_n, int mmas, int copies, int copy_form,
-                                               int steps, unsigned long long* ns_dev, int* units, void* stream) {
+                                               int steps, int depth, unsigned long long* ns_dev, int* units,
+                                               void* stream) {
   if (ns_dev == nullptr || units == nullptr) return MXFP4_ERR_INVALID_ARG;
   if ((pair != 0 && pair != 1) || (kind != 0 && kind != 1) || (copy_form != 0 && copy_form != 1))
     return MXFP4_ERR_INVALID_ARG;
   // N: a multiple of 16 in [16, 256] (one CTA), [64, 256] (a pair)
   if (mma_n % 16 != 0 || mma_n > 256 || mma_n < (pair ? 64 : 16)) return MXFP4_ERR_INVALID_ARG;
-  if (mmas < 1 || mmas > 16 || copies < 0 || copies > (copy_form == 0 ? 8 : 4) || steps < 1 || steps > 1000000)
+  if (depth < 1 || depth > kRateRing) return MXFP4_ERR_INVALID_ARG;
+  if (mmas < 0 || mmas > 16 || mmas + copies < 1 || copies < 0 || copies > (copy_form == 0 ? 8 : 4) || steps < 1 || steps > 1000000)
     return MXFP4_ERR_INVALID_ARG;
   if (kind == 1 && copies != 0) return MXFP4_ERR_INVALID_ARG;   // bf16 MMAs take no scales
   DeviceInfo dev;
   if (current_device_info(&dev) != cudaSuccess || !dev.ok) return MXFP4_ERR_NO_DEVICE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  RateArgs a{pair, kind, mma_n, mmas, copies, copy_form, steps, ns_dev};
+  RateArgs a{pair, kind, mma_n, mmas, copies, copy_form, steps, depth, ns_dev};
   cudaError_t e;
   if (pair == 0) {
     e = cudaFuncSetAttribute(tc_rate_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRateSmem);

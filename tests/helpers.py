@@ -60,19 +60,34 @@ def ulp_bf16(r: np.ndarray) -> np.ndarray:
     return np.where(a >= 2.0 ** -126, u, 2.0 ** -133)
 
 
-def allowance_budget(n: int) -> int:
-    """Outputs that may need the summation allowance: near-cancelling sums are rare."""
+def allowance_budget(n: int, K: int | None = None) -> int:
+    """Outputs that may need the summation allowance: near-cancelling sums are
+    rare, and with K <= 512 the fp32 sums are short enough that none may."""
+    if K is not None and K <= 512:
+        return 0
     return 2 + n // 10000
 
 
+# Every comparison's statistics, in order, for the end-of-session report
+# (conftest.py prints how many outputs passed only under the allowance).
+ALLOWANCE_LOG: list[dict] = []
+
+
 def check_close(out_bits: np.ndarray, acc: np.ndarray, absdot: np.ndarray, n_acc: int,
-                max_allowance: int | None = -1, what: str = "") -> dict:
-    """Compare bf16 outputs against the float64 oracle; return statistics."""
+                max_allowance: int | None = -1, what: str = "", K: int | None = None) -> dict:
+    """Compare bf16 outputs against the float64 oracle; return statistics
+    (also appended to ALLOWANCE_LOG).  K, when given, sets the allowance
+    budget (none for K <= 512)."""
     out = ref.bf16_bits_to_f64(out_bits)
     refb = ref.bf16_bits_to_f64(ref.f64_to_bf16_bits(acc))
     ref_nonfinite = ~np.isfinite(refb)
     bad_nonfinite = (~np.isfinite(out)) & ~ref_nonfinite
     assert not bad_nonfinite.any(), f"{what}: {int(bad_nonfinite.sum())} unexpected NaN/Inf outputs"
+    nan_ref = np.isnan(refb)
+    assert np.isnan(out[nan_ref]).all(), f"{what}: {int((~np.isnan(out[nan_ref])).sum())} outputs are not NaN " \
+        "where the oracle's are (a 0xFF scale in a contributing block)"
+    inf_ref = np.isinf(refb)
+    assert np.array_equal(out[inf_ref], refb[inf_ref]), f"{what}: an overflowing output is not the oracle's Inf"
     fin = ~ref_nonfinite
     err = np.abs(out - refb)
     tol = 2.0 * ulp_bf16(refb)
@@ -86,12 +101,15 @@ def check_close(out_bits: np.ndarray, acc: np.ndarray, absdot: np.ndarray, n_acc
         details = [(tuple(int(v) for v in i), float(out[tuple(i)]), float(refb[tuple(i)]), float(acc[tuple(i)]))
                    for i in idx]
         raise AssertionError(f"{what}: {n_fail} outputs beyond tolerance, e.g. (index, out, ref, exact) {details}")
+    ratio = np.where(fin, err / np.maximum(ulp_bf16(refb), 1e-300), 0.0)
+    stats = {"what": what, "K": K, "max_ulp": float(ratio.max(initial=0.0)), "n_allowance": n_allow,
+             "n": int(out.size)}
+    ALLOWANCE_LOG.append(stats)
     if max_allowance == -1:
-        max_allowance = allowance_budget(int(out.size))
+        max_allowance = allowance_budget(int(out.size), K)
     if max_allowance is not None:
         assert n_allow <= max_allowance, f"{what}: {n_allow} outputs needed the fp32 summation allowance"
-    ratio = np.where(fin, err / np.maximum(ulp_bf16(refb), 1e-300), 0.0)
-    return {"max_ulp": float(ratio.max(initial=0.0)), "n_allowance": n_allow, "n": int(out.size)}
+    return stats
 
 
 def sample_rows(M: int, seed: int = 0, n_random: int = 48, boundary_stride: int = 4) -> np.ndarray:

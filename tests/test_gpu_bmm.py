@@ -44,7 +44,7 @@ def test_mla_absorbed_bmm(capi, kind, N, K, batch_major, M):
     rows = np.arange(M) if M <= 64 else sample_rows(M, seed=4, n_random=16, boundary_stride=4)
     acc, mag = oracle_rows(x, rows, wc, ws, K)
     got_bmn = got.transpose(1, 0, 2) if batch_major else got
-    check_close(got_bmn[:, rows, :], acc, mag, -(-K // 16) + 2, what=kind)
+    check_close(got_bmn[:, rows, :], acc, mag, -(-K // 16) + 2, what=kind, K=K)
 
 
 @pytest.mark.parametrize("B,M,N,K", [(1, 1, 128, 64), (3, 130, 200, 128), (2, 257, 64, 256), (5, 33, 512, 192),
@@ -59,7 +59,7 @@ def test_bmm_small_shapes(capi, B, M, N, K, batch_major):
     got = run_bmm(capi, x, packed, B, M, N, K, batch_major)
     acc, mag = ref.a16wfp4_bmm_f64(ref.bf16_bits_to_f64(x), wc, ws, K)
     got_bmn = got.transpose(1, 0, 2) if batch_major else got
-    check_close(got_bmn, acc, mag, -(-K // 16) + 2)
+    check_close(got_bmn, acc, mag, -(-K // 16) + 2, what=f"bmm B={B} M={M} N={N} K={K}", K=K)
 
 
 @pytest.mark.parametrize("B,M,N,K", [(185, 600, 128, 64), (89, 700, 300, 192)])
@@ -75,4 +75,52 @@ def test_bmm_more_pairs_than_sms(capi, B, M, N, K, batch_major):
     got = run_bmm(capi, x, packed, B, M, N, K, batch_major)
     acc, mag = ref.a16wfp4_bmm_f64(ref.bf16_bits_to_f64(x), wc, ws, K)
     got_bmn = got.transpose(1, 0, 2) if batch_major else got
-    check_close(got_bmn, acc, mag, -(-K // 16) + 2)
+    check_close(got_bmn, acc, mag, -(-K // 16) + 2, what=f"bmm B={B} M={M} N={N} K={K}", K=K)
+
+
+@pytest.mark.parametrize("band", ["low", "high"])
+@pytest.mark.parametrize("batch_major", [False, True])
+def test_bmm_weight_scales_at_the_e8m0_extremes(capi, band, batch_major):
+    """Live weight blocks at the ends of E8M0: bytes 0x00..0x06 against
+    activations near 2^100, and 0xF0..0xFC against activations near 2^-118,
+    every product and sum inside the fp32 range.  The kernel forms
+    e2m1 * 2^(s-127) in bf16 before the MMA: exact for every code at these
+    scales (the 0x00 values are bf16 subnormals); at 0xFD and 0xFE the larger
+    codes exceed the bf16 range, outside what this kernel represents."""
+    B, M, N, K = 3, 130, 256, 512
+    x = synth.bmm_activations(B, M, K, seed=11)
+    g = np.random.default_rng(5)
+    wc = synth.weight_codes(N, K, seed=12, batch=B)
+    nb = K // 32
+    if band == "low":
+        ws = g.integers(0x00, 0x07, size=(B, N, nb)).astype(np.uint8)
+        ws[:, :, 0] = 0x00
+        e = 100
+    else:
+        ws = g.integers(0xF0, 0xFD, size=(B, N, nb)).astype(np.uint8)
+        ws[:, :, 0] = 0xFC
+        e = -118
+    x = ref.f64_to_bf16_bits(ref.bf16_bits_to_f64(x) * 2.0 ** e)
+    packed = pack_weights(capi, wc, ws, K)
+    got = run_bmm(capi, x, packed, B, M, N, K, batch_major)
+    acc, mag = ref.a16wfp4_bmm_f64(ref.bf16_bits_to_f64(x), wc, ws, K)
+    assert np.isfinite(acc).all()
+    got_bmn = got.transpose(1, 0, 2) if batch_major else got
+    check_close(got_bmn, acc, mag, -(-K // 16) + 2, what=f"bmm {band} scales", K=K)
+
+
+@pytest.mark.parametrize("batch_major", [False, True])
+def test_bmm_nan_weight_scale_poisons_its_output_column(capi, batch_major):
+    """A live 0xFF (NaN) weight scale makes that batch's weight row's outputs
+    NaN for every activation row, and nothing else."""
+    B, M, N, K = 2, 70, 200, 192
+    x = synth.bmm_activations(B, M, K, seed=13)
+    wc = synth.weight_codes(N, K, seed=14, batch=B)
+    ws = synth.weight_scales(N, K, -6, 0, seed=14, batch=B).copy()
+    ws[1, 77, 3] = 0xFF
+    packed = pack_weights(capi, wc, ws, K)
+    got = run_bmm(capi, x, packed, B, M, N, K, batch_major)
+    acc, mag = ref.a16wfp4_bmm_f64(ref.bf16_bits_to_f64(x), wc, ws, K)
+    assert np.isnan(acc[1, :, 77]).all() and np.isfinite(acc[0]).all()
+    got_bmn = got.transpose(1, 0, 2) if batch_major else got
+    check_close(got_bmn, acc, mag, -(-K // 16) + 2, what="bmm NaN scale", K=K)

@@ -108,8 +108,11 @@ def test_prefill_with_bias(capi, M, NK):
     check_close(got[rows], acc, mag, n_acc(K), what=f"prefill M={M} N={N} K={K}")
 
 
-@pytest.mark.parametrize("M", [16, 300])
+@pytest.mark.parametrize("M", [1, 2, 5, 8, 16, 300])
 def test_prequantized_inputs_match_fused(capi, M):
+    """bf16 input (quantized inside the GEMM kernel for M <= 8, by the
+    quantizer kernel above) and the two pre-quantized forms give the same
+    bits."""
     N, K = 640, 5152
     x, wc, ws, b = make_problem(M, N, K, seed=11, edge=True, with_bias=True)
     packed = pack_weights(capi, wc, ws, K)
@@ -156,7 +159,7 @@ def test_leading_dimension_of_output(capi):
     packed = pack_weights(capi, wc, ws, K)
     got = run_gemm(capi, x, packed, b, M, N, K, ldo=N + 40)
     acc, mag = oracle_gemm_rows(x, np.arange(M), wc, ws, K, b)
-    check_close(got, acc, mag, n_acc(K))
+    check_close(got, acc, mag, n_acc(K), K=K)
 
 
 TINY = [(m, n, k) for m in (1, 2, 7, 16, 33, 64, 65, 129)
@@ -171,7 +174,7 @@ def test_tiny_shape_sweep(capi):
         got = run_gemm(capi, x, packed, b, M, N, K)
         acc, mag = oracle_gemm_rows(x, np.arange(M), wc, ws, K, b)
         try:
-            check_close(got, acc, mag, n_acc(K), what=f"{(M, N, K)}")
+            check_close(got, acc, mag, n_acc(K), what=f"{(M, N, K)}", K=K)
         except AssertionError as e:
             bad.append(str(e)[:200])
     assert not bad, f"{len(bad)} of {len(TINY)} shapes failed: {bad[:4]}"
@@ -301,3 +304,86 @@ def test_concurrent_host_threads(capi):
     assert capi.mxfp4_get_device_error() == capi.OK
     for j in jobs:
         assert np.array_equal(host_bits(j["out"]), j["want"]), (j["M"], j["N"], j["K"])
+
+
+def scaled_bf16(bits: np.ndarray, e: int) -> np.ndarray:
+    """bf16 values times 2^e, rounded to bf16 (values pushed below the normal
+    range lose bits; kernel and oracle see the same rounded inputs)."""
+    return ref.f64_to_bf16_bits(ref.bf16_bits_to_f64(bits) * 2.0 ** e)
+
+
+@pytest.mark.parametrize("M", [4, 16, 200])
+@pytest.mark.parametrize("band", ["low", "high"])
+def test_weight_scales_at_the_e8m0_extremes(capi, M, band):
+    """Live weight blocks whose E8M0 scales sit at the ends of the format:
+    bytes 0x00..0x06 (2^-127..2^-121) against activations near 2^100, and
+    0xF0..0xFE (2^113..2^127) against activations near 2^-118, so that every
+    product and sum stays inside the fp32 normal range while the scale
+    exponents reach both limits.  Covers the in-kernel quantizer (M = 4),
+    the decode kernel after the quantizer (M = 16) and the prefill kernel."""
+    N, K = 520, 1024
+    x, wc, _, b = make_problem(M, N, K, seed=M + (0 if band == "low" else 1))
+    g = np.random.default_rng(M)
+    nb = -(-K // 32)
+    if band == "low":
+        ws = g.integers(0x00, 0x07, size=(N, nb)).astype(np.uint8)
+        ws[:, 0] = 0x00
+        x = scaled_bf16(x, 100)
+    else:
+        ws = g.integers(0xF0, 0xFF, size=(N, nb)).astype(np.uint8)
+        ws[:, 0] = 0xFE
+        x = scaled_bf16(x, -118)
+    packed = pack_weights(capi, wc, ws, K)
+    got = run_gemm(capi, x, packed, None, M, N, K)
+    acc, mag = oracle_gemm_rows(x, np.arange(M), wc, ws, K, None)
+    assert np.isfinite(acc).all()
+    check_close(got, acc, mag, n_acc(K), what=f"{band} scales M={M}", K=K)
+
+
+@pytest.mark.parametrize("M", [4, 16, 200])
+def test_nan_weight_scale_poisons_its_output_column(capi, M):
+    """A live weight block with scale 0xFF (E8M0 NaN) makes that weight row's
+    output NaN for every activation row, and nothing else."""
+    N, K = 300, 512
+    x, wc, ws, b = make_problem(M, N, K, seed=7 + M, with_bias=True)
+    ws = ws.copy()
+    ws[37, 5] = 0xFF
+    ws[299, 15] = 0xFF
+    packed = pack_weights(capi, wc, ws, K)
+    got = run_gemm(capi, x, packed, b, M, N, K)
+    acc, mag = oracle_gemm_rows(x, np.arange(M), wc, ws, K, b)
+    assert np.isnan(acc[:, [37, 299]]).all() and np.isfinite(np.delete(acc, [37, 299], axis=1)).all()
+    check_close(got, acc, mag, n_acc(K), what=f"NaN scale M={M}", K=K)
+
+
+@pytest.mark.parametrize("M", [1, 16, 300])
+def test_weights_refreshed_by_a_device_copy(capi, M):
+    """The weight-update contract: a packed buffer rewritten by an ordinary
+    device copy (not mxfp4_pack_weights), then mxfp4_weights_updated, then the
+    GEMM: every call sees the weights of the copy just made, alternating
+    between two weight sets."""
+    N, K = 1024, 5120
+    x, _, _, b = make_problem(M, N, K, seed=91 + M, with_bias=True)
+    sets = []
+    for k in range(2):
+        wc = synth.weight_codes(N, K, seed=500 + k)
+        ws = synth.weight_scales(N, K, -6, 0, seed=500 + k)
+        sets.append((wc, ws, pack_weights(capi, wc, ws, K)))
+    live = torch.empty_like(sets[0][2])
+    out = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    wsb = capi.mxfp4_gemm_workspace_bytes(M, N, K)
+    work = gemm_workspace(capi, wsb)
+    xd, bd = dev_bf16(x), dev_bf16(b)
+    want = []
+    for wc, ws, _ in sets:
+        acc, mag = oracle_gemm_rows(x, np.arange(M), wc, ws, K, b)
+        want.append((acc, mag))
+    torch.cuda.synchronize()
+    for it in range(6):
+        k = it % 2
+        live.copy_(sets[k][2])            # an ordinary kernel writes the weights
+        capi.mxfp4_weights_updated()
+        capi.mxfp4_gemm(xd, K, None, None, 0, live, bd, out, N, M, N, K, work, wsb)
+        torch.cuda.synchronize()
+        assert capi.mxfp4_get_device_error() == capi.OK
+        check_close(host_bits(out), *want[k], n_acc(K), what=f"refresh {it}")
