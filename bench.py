@@ -803,33 +803,15 @@ def run_single(args):
     print(f"single {M},{N},{K}{' (MXFP4 out)' if args.mxfp4_out else ''}: {args.calls} calls ok")
 
 
-# name, pair (cta_group::2), kind (0 mxf4, 1 bf16), N, MMAs per step, scale copies per step, copy form
-# (0: 32x128b.warpx4, 1: 128x256b), depth (steps in flight: the wait is on the commit `depth` steps
-# back).  A k-step of the 1-CTA GEMM kernels is "mxf4 1cta 128x256 x4 + 6 cp"; depth 4 is the round
-# trip of a 4-stage ring, depth 32 leaves only the tensor pipe's throughput.
-TC_RATE_VARIANTS = tuple(
-    [(f"mxf4 1cta 128x256 x4 d{d}", 0, 0, 256, 4, 0, 0, d) for d in (1, 2, 4, 8, 16, 32)]
-    + [(f"mxf4 1cta 128x256 x4 + 6 cp d{d}", 0, 0, 256, 4, 6, 0, d) for d in (4, 8, 16, 32)]
-    + [(f"mxf4 1cta 128x256 x4 + 4 cp d{d}", 0, 0, 256, 4, 4, 0, d) for d in (8, 32)]
-    + [(f"mxf4 1cta 128x256 x4 + 2 cp128x256b d{d}", 0, 0, 256, 4, 2, 1, d) for d in (8, 32)]
-    + [(f"mxf4 1cta 6 cp only d{d}", 0, 0, 256, 0, 6, 0, d) for d in (8, 32)]
-    + [(f"mxf4 1cta 128x128 x4 d{d}", 0, 0, 128, 4, 0, 0, d) for d in (32,)]
-    + [(f"mxf4 1cta 128x64 x8 d{d}", 0, 0, 64, 8, 0, 0, d) for d in (32,)]
-    + [(f"mxf4 1cta 128x64 x8 + 6 cp d{d}", 0, 0, 64, 8, 6, 0, d) for d in (8, 32)]
-    + [(f"mxf4 2cta 256x256 x4 d{d}", 1, 0, 256, 4, 0, 0, d) for d in (4, 8, 16, 32)]
-    + [(f"mxf4 2cta 256x256 x4 + 6 cp d{d}", 1, 0, 256, 4, 6, 0, d) for d in (4, 8, 16, 32)]
-    + [(f"mxf4 2cta 256x256 x4 + 4 cp d{d}", 1, 0, 256, 4, 4, 0, d) for d in (8, 32)]
-    + [(f"mxf4 2cta 256x128 x4 d{d}", 1, 0, 128, 4, 0, 0, d) for d in (32,)]
-    + [(f"mxf4 2cta 256x64 x4 d{d}", 1, 0, 64, 4, 0, 0, d) for d in (32,)]
-    + [(f"mxf4 2cta 256x64 x4 + 3 cp d{d}", 1, 0, 64, 4, 3, 0, d) for d in (8, 32)]
-    + [(f"bf16 1cta 128x256 x4 d{d}", 0, 1, 256, 4, 0, 0, d) for d in (4, 32)]
-    + [(f"bf16 2cta 256x256 x4 d{d}", 1, 1, 256, 4, 0, 0, d) for d in (4, 32)]
-)
+# (N of each MMA, depth) pairs measured for every instruction mix of mxfp4_diag_tensor_rate: a
+# k-step of the 1-CTA GEMM kernels is "mxf4 1cta 4 mma + 6 cp" at N = 256; depth 4 is the round trip
+# of a 4-stage ring, depth 32 leaves the tensor pipe's throughput.
+TC_RATE_POINTS = ((256, 4), (256, 32), (128, 32), (64, 32))
 
 
 def run_tc_rates(args):
-    """Tensor-pipe issue rates of the instruction mixes above on every SM at once
-    (mxfp4_diag_tensor_rate), and the dense FP4 rate they imply; one JSON line."""
+    """Tensor-pipe issue rates of the library's instruction mixes on every SM at once
+    (mxfp4_diag_tensor_rate), and the dense FP4 / bf16 rates they imply; one JSON line."""
     import torch
 
     import __graft_entry__
@@ -849,29 +831,38 @@ def run_tc_rates(args):
     clocks = ClockSampler(0)
     clocks.start()
     rows = []
-    for name, pair, kind, n, mmas, copies, form, depth in TC_RATE_VARIANTS:
-        if pair and not pair_ok:
-            rows.append({"name": name, "skipped": "cta_group::2 allocation is not collective"})
-            continue
-        m = 256 if pair else 128
-        k = 64 if kind == 0 else 16
-        meds = []
-        for _ in range(3):
-            ns.zero_()
-            units = capi.mxfp4_diag_tensor_rate(pair, kind, n, mmas, copies, form, steps, depth, ns)
-            torch.cuda.synchronize()
-            v = [x for x in ns[:units].cpu().tolist() if x > 0]
-            if len(v) != units:
-                raise RuntimeError(f"{name}: {units - len(v)} units timed out")
-            meds.append(statistics.median(v))
-        med = statistics.median(meds)
-        ns_step = med / steps
-        flop = units * mmas * 2.0 * m * n * k * steps
-        rows.append({"name": name, "units": units, "depth": depth, "ns_per_step": round(ns_step, 1),
-                     "ns_per_mma": round(ns_step / mmas, 1) if mmas else None,
-                     "tflops": round(flop / (med * 1e-9) / 1e12, 1)})
+    for var in range(capi.mxfp4_diag_tensor_rate_variants()):
+        info = capi.mxfp4_diag_tensor_rate_info(var)
+        pair, kind, mmas, copies, form, issuers = (info[k] for k in ("pair", "kind", "mmas", "copies", "form",
+                                                                    "issuers"))
+        name = (f"{'mxf4' if kind == 0 else 'bf16'} {'2cta' if pair else '1cta'} {mmas} mma"
+                + (f" + {copies} cp{'128x256b' if form else ''}" if copies else "")
+                + (f" x{issuers} issuers" if issuers > 1 else ""))
+        for n, depth in TC_RATE_POINTS:
+            if (pair and n < 64) or (issuers > 1 and n > 128) or (mmas == 0 and n != 256):
+                continue
+            if pair and not pair_ok:
+                rows.append({"name": name, "skipped": "cta_group::2 allocation is not collective"})
+                break
+            m = 256 if pair else 128
+            k = 64 if kind == 0 else 16
+            meds = []
+            for _ in range(3):
+                ns.zero_()
+                units = capi.mxfp4_diag_tensor_rate(var, n, steps, depth, ns)
+                torch.cuda.synchronize()
+                v = [x for x in ns[:units].cpu().tolist() if x > 0]
+                if len(v) != units:
+                    raise RuntimeError(f"{name}: {units - len(v)} units timed out")
+                meds.append(statistics.median(v))
+            med = statistics.median(meds)
+            ns_step = med / steps
+            flop = units * issuers * mmas * 2.0 * m * n * k * steps
+            rows.append({"name": name, "n": n, "depth": depth, "units": units, "ns_per_step": round(ns_step, 1),
+                         "ns_per_mma": round(ns_step / mmas, 1) if mmas else None,
+                         "tflops": round(flop / (med * 1e-9) / 1e12, 1)})
     clk = clocks.stop()
-    fp4 = [r["tflops"] for r in rows if r["name"].startswith("mxf4") and "+" not in r["name"] and "tflops" in r]
+    fp4 = [r["tflops"] for r in rows if r["name"].startswith("mxf4") and "cp" not in r["name"] and "tflops" in r]
     bf16 = [r["tflops"] for r in rows if r["name"].startswith("bf16") and "tflops" in r]
     print(json.dumps({"tc_rates": rows, "pair_alloc": {"cols": cols, "collective": pair_ok},
                       "mxf4_dense_peak_tflops": max(fp4) if fp4 else None,

@@ -25,30 +25,34 @@ extern "C" {
  * mxfp4_diag_tensor_rate launch reports: the size of its ns_dev buffer. */
 MXFP4_API int mxfp4_diag_max_units(void);
 
-/* Tensor-pipe issue rate of one instruction mix, on every SM at once.
+/* Tensor-pipe issue rate of one of mxfp4_diag_tensor_rate_variants()
+ * instruction mixes, on every SM at once.
  *
- * Each unit (one CTA per SM, or with pair = 1 one 2-CTA cluster issuing
- * cta_group::2 instructions) issues `steps` steps back to back after 16
- * untimed ones; a step is `copies` scale copies (shared memory -> TMEM;
- * copy_form 0: tcgen05.cp.32x128b.warpx4, 1: tcgen05.cp.128x256b) then
- * `mmas` MMAs of shape M x mma_n x K into one TMEM accumulator (kind 0:
- * kind::mxf4.block_scale.scale_vec::2X, E2M1 x E2M1 with UE8M0 scales,
- * K = 64; kind 1: kind::f16, bf16 x bf16, K = 16; M = 128, or 256 for a
- * pair), each step committed to an mbarrier, with a wait on the commit of
- * the step `depth` back before the next step is issued (depth 4: the round
- * trip of a 4-stage pipeline ring; depth 32: nearly free issue, the tensor
- * pipe's own rate).  Operands are zero bytes.
+ * mxfp4_diag_tensor_rate_info(variant, info) fills info[0..5] with the mix:
+ * pair (1: cta_group::2 over a 2-CTA cluster, M = 256; 0: one CTA, M = 128),
+ * kind (0: kind::mxf4.block_scale.scale_vec::2X, E2M1 x E2M1 with UE8M0
+ * scales, K = 64; 1: kind::f16, bf16 x bf16, K = 16), MMAs per step, scale
+ * copies per step, copy form (0: tcgen05.cp.32x128b.warpx4, 1:
+ * tcgen05.cp.128x256b), issuing threads per CTA (1, or 2 with separate
+ * accumulators of N <= 128 columns each).
+ *
+ * Each unit (one CTA per SM, or one 2-CTA cluster) issues `steps` steps back
+ * to back after 16 untimed ones: the copies, then the MMAs of shape
+ * M x mma_n x K into the issuer's accumulator, each step committed to an
+ * mbarrier, with a wait on the commit of the step `depth` back before the
+ * next step is issued (depth 4: the round trip of a 4-stage pipeline ring;
+ * depth 32: nearly free issue).  Operands are zero bytes.
  *
  * ns_dev: device buffer of mxfp4_diag_max_units() uint64; unit u's elapsed
- * nanoseconds for the timed steps (%globaltimer) land in ns_dev[u], or 0 if a
- * bounded wait gave up.  *units (host) receives the number of units launched.
- * Arguments: mma_n a multiple of 16 in [16, 256] ([64, 256] for a pair),
- * 0 <= mmas <= 16, 0 <= copies <= 8 (form 0) or 4 (form 1), at least one
- * instruction per step, no copies with kind 1, 1 <= steps <= 10^6,
- * 1 <= depth <= 32; otherwise MXFP4_ERR_INVALID_ARG. */
-MXFP4_API mxfp4_status mxfp4_diag_tensor_rate(int pair, int kind, int mma_n, int mmas, int copies, int copy_form,
-                                              int steps, int depth, unsigned long long* ns_dev, int* units,
-                                              void* stream);
+ * nanoseconds for the timed steps (%globaltimer; the slower issuer of a
+ * two-issuer CTA) land in ns_dev[u], or 0 if a bounded wait gave up.  *units
+ * (host) receives the number of units launched.  Arguments: mma_n a multiple
+ * of 16 in [16, 256] ([64, 256] for a pair, at most 128 with two issuers),
+ * 1 <= steps <= 10^6, 1 <= depth <= 32; otherwise MXFP4_ERR_INVALID_ARG. */
+MXFP4_API int mxfp4_diag_tensor_rate_variants(void);
+MXFP4_API mxfp4_status mxfp4_diag_tensor_rate_info(int variant, int* info);
+MXFP4_API mxfp4_status mxfp4_diag_tensor_rate(int variant, int mma_n, int steps, int depth,
+                                              unsigned long long* ns_dev, int* units, void* stream);
 
 /* One 2-CTA cluster whose CTAs each take 32 TMEM columns with
  * tcgen05.alloc.cta_group::2 (one warp per CTA, as that form requires) and
@@ -57,6 +61,17 @@ MXFP4_API mxfp4_status mxfp4_diag_tensor_rate(int pair, int kind, int mma_n, int
  * the pair allocated together, which the pair forms of
  * mxfp4_diag_tensor_rate rely on. */
 MXFP4_API mxfp4_status mxfp4_diag_pair_alloc_probe(uint32_t* addr_dev, void* stream);
+
+/* Failure-path test hook: sets, for the mxfp4_rmsnorm_quant_act calls that
+ * follow in this process, the bound (in SM clock cycles) of its bulk-copy
+ * kernel's waits on the row copies; 0 restores the default of about one
+ * second.  With a bound far below a copy's latency the wait runs out: the
+ * kernel records the timeout (reported by mxfp4_get_device_error as
+ * MXFP4_ERR_TIMEOUT), lets every copy it issued land under the full bound,
+ * and exits without writing the rows it did not finish.  A test uses this
+ * to exercise the bounded-wait path without a fault.  Returns
+ * MXFP4_ERR_INVALID_ARG for a negative bound. */
+MXFP4_API mxfp4_status mxfp4_diag_set_wait_cycles(long long cycles);
 
 #ifdef __cplusplus
 }

@@ -47,8 +47,11 @@ _SIGNATURES = {
     "mxfp4_gemm_noalloc": (_i, [_p, _i, _p, _p, _p, _i, _i, _i, _i, _p]),
     "mxfp4_gemm_noalloc_max_scratch_bytes": (_sz, []),
     "mxfp4_diag_max_units": (_i, []),
-    "mxfp4_diag_tensor_rate": (_i, [_i, _i, _i, _i, _i, _i, _i, _i, _p, ctypes.POINTER(_i), _p]),
+    "mxfp4_diag_tensor_rate_variants": (_i, []),
+    "mxfp4_diag_tensor_rate_info": (_i, [_i, ctypes.POINTER(_i)]),
+    "mxfp4_diag_tensor_rate": (_i, [_i, _i, _i, _i, _p, ctypes.POINTER(_i), _p]),
     "mxfp4_diag_pair_alloc_probe": (_i, [_p, _p]),
+    "mxfp4_diag_set_wait_cycles": (_i, [ctypes.c_longlong]),
 }
 for _name, (_res, _args) in _SIGNATURES.items():
     _fn = getattr(lib, _name)
@@ -171,16 +174,30 @@ def mxfp4_diag_max_units() -> int:
     return lib.mxfp4_diag_max_units()
 
 
-def mxfp4_diag_tensor_rate(pair: int, kind: int, mma_n: int, mmas: int, copies: int, copy_form: int, steps: int,
-                           depth: int, ns_dev, stream=None) -> int:
+def mxfp4_diag_tensor_rate_variants() -> int:
+    return lib.mxfp4_diag_tensor_rate_variants()
+
+
+def mxfp4_diag_tensor_rate_info(variant: int) -> dict:
+    """The instruction mix of one measurement variant."""
+    info = (_i * 6)()
+    _check(lib.mxfp4_diag_tensor_rate_info(variant, info), "mxfp4_diag_tensor_rate_info")
+    return dict(zip(("pair", "kind", "mmas", "copies", "form", "issuers"), list(info)))
+
+
+def mxfp4_diag_tensor_rate(variant: int, mma_n: int, steps: int, depth: int, ns_dev, stream=None) -> int:
     """Launches the issue-rate measurement; returns the number of units (CTAs or pairs) whose
     elapsed nanoseconds land in ``ns_dev`` once the stream has finished."""
     units = _i(0)
-    _check(lib.mxfp4_diag_tensor_rate(pair, kind, mma_n, mmas, copies, copy_form, steps, depth, _ptr(ns_dev),
-                                      ctypes.byref(units), _stream(stream)),
+    _check(lib.mxfp4_diag_tensor_rate(variant, mma_n, steps, depth, _ptr(ns_dev), ctypes.byref(units),
+                                      _stream(stream)),
            "mxfp4_diag_tensor_rate")
     return units.value
 
 
 def mxfp4_diag_pair_alloc_probe(addr_dev, stream=None) -> None:
     _check(lib.mxfp4_diag_pair_alloc_probe(_ptr(addr_dev), _stream(stream)), "mxfp4_diag_pair_alloc_probe")
+
+
+def mxfp4_diag_set_wait_cycles(cycles: int) -> None:
+    _check(lib.mxfp4_diag_set_wait_cycles(cycles), "mxfp4_diag_set_wait_cycles")

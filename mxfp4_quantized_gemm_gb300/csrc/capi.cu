@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "mxfp4.h"
+#include "mxfp4_diag.h"
 #include "internal.h"
 #include "norm_quant.h"
 
@@ -314,6 +315,12 @@ mxfp4_status a16wfp4_bmm(const void* x, const void* w_packed, void* out, int B, 
   if (st != MXFP4_OK) return st;
   return from_cuda(launch_bmm(x, static_cast<const uint8_t*>(w_packed), out, B, M, N, K,
                               out_layout == MXFP4_OUT_MBN, dev, static_cast<cudaStream_t>(stream)));
+}
+
+mxfp4_status mxfp4_diag_set_wait_cycles(long long cycles) {
+  if (cycles < 0) return MXFP4_ERR_INVALID_ARG;
+  set_norm_wait_cycles(cycles);
+  return MXFP4_OK;
 }
 
 mxfp4_status mxfp4_get_device_error(void* stream) {

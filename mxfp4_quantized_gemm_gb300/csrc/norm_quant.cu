@@ -57,6 +57,7 @@ struct NormArgs {
   float eps;
   int M, K, rows, chunks, KT;
   bool vec_x, vec_r, vec_y, vec_g;
+  long long wait_cycles;   // bound of the waits on the row copies (kWaitCycles unless a test lowers it)
 };
 
 // bf16(a + b) for 8 values: the packed bf16 add rounds the exact sum once.
@@ -347,7 +348,9 @@ __global__ void __launch_bounds__(1024 / kTmaChunks, kTmaChunks) rmsnorm_quant_t
     uint4 h[kTmaChunks];
 #pragma unroll
     for (int i = 0; i < kTmaChunks; ++i) h[i] = make_uint4(0, 0, 0, 0);
-    if (real && mbar_wait(&full[s], static_cast<uint32_t>(it / kNormStages) & 1u, abort)) {
+    const uint32_t par = static_cast<uint32_t>(it / kNormStages) & 1u;
+    if (real && (a.wait_cycles < kWaitCycles ? mbar_wait_polling(&full[s], par, abort, a.wait_cycles)
+                                             : mbar_wait(&full[s], par, abort))) {
       const uint8_t* xs = ring + static_cast<size_t>(s) * stage_bytes;
 #pragma unroll
       for (int i = 0; i < kTmaChunks; ++i) {
@@ -392,7 +395,8 @@ __global__ void __launch_bounds__(1024 / kTmaChunks, kTmaChunks) rmsnorm_quant_t
   if (abort && tid == 0) {
     atomicOr(&g_norm_error, kErrTimeout);
     // let the copies still in flight (iterations it .. it + kNormStages - 1,
-    // all issued) land before the CTA's memory is reused
+    // all issued) land before the CTA's memory is reused; these waits take
+    // the full bound whatever a.wait_cycles is
     for (int j = it; j < it + kNormStages; ++j) {
       bool again = false;
       if (blockIdx.x + j * gridDim.x < static_cast<unsigned>(a.M))
@@ -466,8 +470,16 @@ uint32_t norm_read_clear_error() {
   return v;
 }
 
+// Bound of the producer's waits on its row copies, in SM clock cycles (0:
+// the default kWaitCycles); lowered only by a test to make a wait run out.
+static std::atomic<long long> g_norm_wait_cycles{0};
+
+void set_norm_wait_cycles(long long cycles) { g_norm_wait_cycles.store(cycles, std::memory_order_relaxed); }
+
 cudaError_t launch_rmsnorm_quant(const NormQuantProblem& p, const DeviceInfo& dev, cudaStream_t s) {
   NormArgs a{};
+  const long long wc = g_norm_wait_cycles.load(std::memory_order_relaxed);
+  a.wait_cycles = wc > 0 ? wc : kWaitCycles;
   a.x = static_cast<const uint16_t*>(p.x);
   a.res = static_cast<uint16_t*>(p.residual);
   a.gamma = static_cast<const uint16_t*>(p.gamma);

@@ -26,5 +26,8 @@ struct NormQuantProblem {
 
 cudaError_t launch_rmsnorm_quant(const NormQuantProblem& p, const DeviceInfo& dev, cudaStream_t s);
 uint32_t norm_read_clear_error();
+// Bound of the bulk-copy producer kernel's waits on its row copies, in SM
+// clock cycles, for launches that follow (0 restores the default).
+void set_norm_wait_cycles(long long cycles);
 
 }  // namespace mx

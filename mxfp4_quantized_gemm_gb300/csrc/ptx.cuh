@@ -55,6 +55,33 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, bool& 
   }
   return true;
 }
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// The same wait with a caller-chosen bound, polled with the non-blocking test
+// (try_wait may suspend the thread for longer than a short bound): how a test
+// makes a wait run out.
+__device__ __forceinline__ bool mbar_wait_polling(uint64_t* bar, uint32_t parity, bool& abort, long long limit) {
+  if (abort) return false;
+  const uint32_t a = smem_u32(bar);
+  const long long t0 = clock64();
+  while (!mbar_test_wait(a, parity)) {
+    if (clock64() - t0 > limit) {
+      abort = true;
+      return false;
+    }
+  }
+  return true;
+}
 
 // ------------------------------------------------------------ bulk copies
 // 1-D bulk copy global -> shared (this CTA), completion counted on `bar`.

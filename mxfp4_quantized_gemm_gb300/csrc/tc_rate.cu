@@ -1,7 +1,7 @@
 // Tensor-pipe issue-rate measurement (diagnostic; not on the GEMM path).
 //
-// One thread per CTA (or per CTA pair) issues the same tcgen05 sequence per
-// "step" back to back -- a number of scale copies (shared memory -> TMEM)
+// One thread per CTA (or per CTA pair; or two threads per CTA, each with its
+// own accumulator) issues the same tcgen05 sequence per "step" back to back -- a number of scale copies (shared memory -> TMEM)
 // followed by a number of MMAs into one accumulator -- and commits each step
 // to a ring of mbarriers, waiting for the commit of the step `depth` back
 // before it issues the next: depth 4 is the round trip a 4-stage pipeline
@@ -36,12 +36,7 @@ constexpr uint32_t kRateTmemCols = 512;
 constexpr int kRateRing = 32;                  // commit barriers; the deepest wait is 32 steps back
 
 struct RateArgs {
-  int pair;        // 1: cta_group::2 over a 2-CTA cluster
-  int kind;        // 0: kind::mxf4 block-scaled, 1: kind::f16 (bf16)
   int mma_n;       // N of each MMA (M is 128, or 256 for a pair)
-  int mmas;        // MMAs per step
-  int copies;      // scale copies per step
-  int copy_form;   // 0: 32x128b.warpx4, 1: 128x256b
   int steps;       // timed steps
   int depth;       // wait for the commit of the step `depth` back (1..32)
   unsigned long long* ns;   // per unit (CTA or pair): ns of the timed steps, 0 after a timeout
@@ -66,9 +61,9 @@ __device__ __forceinline__ uint64_t sdesc_scales_128x256b(uint32_t saddr) {
          (static_cast<uint64_t>(256 >> 4) << 32) | (static_cast<uint64_t>(1) << 46);
 }
 
-template <bool kPair>
-__device__ __forceinline__ void rate_copy(int form, uint32_t taddr, uint64_t desc) {
-  if (form == 0) {
+template <bool kPair, int kForm>
+__device__ __forceinline__ void rate_copy(uint32_t taddr, uint64_t desc) {
+  if (kForm == 0) {
     if (kPair)
       asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
     else
@@ -81,10 +76,10 @@ __device__ __forceinline__ void rate_copy(int form, uint32_t taddr, uint64_t des
   }
 }
 
-template <bool kPair>
-__device__ __forceinline__ void rate_mma(int kind, uint32_t d, uint64_t ad, uint64_t bd, uint32_t id, uint32_t sfa,
+template <bool kPair, int kKind>
+__device__ __forceinline__ void rate_mma(uint32_t d, uint64_t ad, uint64_t bd, uint32_t id, uint32_t sfa,
                                          uint32_t sfb) {
-  if (kind == 0) {
+  if (kKind == 0) {
     if (kPair)
       asm volatile(
           "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, 1, 0;\n\t"
@@ -118,12 +113,17 @@ __device__ __forceinline__ void rate_commit(uint64_t* bar) {
     mma_commit(bar);
 }
 
-template <bool kPair>
+// One instruction mix, fully unrolled: kMmas MMAs of kind kKind (0: mxf4,
+// 1: bf16) after kCopies scale copies of form kForm per step, issued by
+// kIssuers threads of the CTA (lane 0 of warps 0 and 1), each into its own
+// accumulator (columns 0.. and 128.. ; N <= 128 with two issuers) and its
+// own scale columns (256.. and 384..).
+template <bool kPair, int kKind, int kMmas, int kCopies, int kForm, int kIssuers>
 __global__ void __launch_bounds__(128, 1) tc_rate_kernel(const RateArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
-  __shared__ uint64_t ring[kRateRing];
-  __shared__ uint64_t done;
+  __shared__ uint64_t ring[kIssuers][kRateRing];
+  __shared__ uint64_t done[kIssuers];
   __shared__ uint32_t tmem_slot;
 
   for (int i = threadIdx.x; i < kRateOperandBytes / 16; i += blockDim.x)
@@ -132,11 +132,13 @@ __global__ void __launch_bounds__(128, 1) tc_rate_kernel(const RateArgs a) {
   const uint32_t rank = kPair ? cluster_ctarank() : 0u;
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kRateRing; ++s) mbar_init(&ring[s], 1);
-    mbar_init(&done, 1);
+    for (int w = 0; w < kIssuers; ++w) {
+      for (int s = 0; s < kRateRing; ++s) mbar_init(&ring[w][s], 1);
+      mbar_init(&done[w], 1);
+    }
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == 2) {
     if (kPair) {
       asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
                    "r"(kRateTmemCols)
@@ -155,54 +157,68 @@ __global__ void __launch_bounds__(128, 1) tc_rate_kernel(const RateArgs a) {
   bool abort = false;
   unsigned long long t0 = 0, t1 = 0;
 
-  if (threadIdx.x == 0 && rank == 0) {
+  const int issuer = warp;   // lane 0 of warps 0 .. kIssuers-1
+  if ((threadIdx.x & 31) == 0 && issuer < kIssuers && rank == 0) {
     const uint32_t a_s = smem_u32(smem), b_s = a_s + 16 * 1024, sc_s = a_s + 48 * 1024;
-    const int M = kPair ? 256 : 128;
+    constexpr int M = kPair ? 256 : 128;
+    const uint32_t dcol = tmem + 128u * static_cast<uint32_t>(issuer);
+    const uint32_t scbase = tmem + 256u + 128u * static_cast<uint32_t>(issuer);
     const int total = kRateWarm + a.steps;
+    uint32_t id[2];
+    for (int h = 0; h < 2; ++h) id[h] = kKind == 0 ? idesc_mxf4(M, a.mma_n, h * 2, h * 2) : idesc_bf16(M, a.mma_n);
     for (int s = 0; s < total; ++s) {
-      const int slot = s & 3;   // scale columns rotate over four slots (their values do not matter)
       if (s >= a.depth) {
         const int w = s - a.depth;
-        if (!mbar_wait(&ring[w % kRateRing], static_cast<uint32_t>(w / kRateRing) & 1u, abort)) break;
+        if (!mbar_wait(&ring[issuer][w % kRateRing], static_cast<uint32_t>(w / kRateRing) & 1u, abort)) break;
       }
       tc_fence_after();
       if (s == kRateWarm) t0 = globaltimer();
-      const uint32_t scol = tmem + 256u + static_cast<uint32_t>(slot) * 32u;
-      for (int c = 0; c < a.copies; ++c) {
-        if (a.copy_form == 0)
-          rate_copy<kPair>(0, scol + 4u * static_cast<uint32_t>(c & 7), sdesc_scales(sc_s + 512u * (c & 7)));
+      const uint32_t scol = scbase + static_cast<uint32_t>(s & 3) * 32u;   // four rotating slots (values unused)
+#pragma unroll
+      for (int c = 0; c < kCopies; ++c) {
+        if (kForm == 0)
+          rate_copy<kPair, 0>(scol + 4u * (c & 7), sdesc_scales(sc_s + 512u * (c & 7)));
         else
-          rate_copy<kPair>(1, scol + 8u * static_cast<uint32_t>(c & 3),
-                           sdesc_scales_128x256b(sc_s + 4096u * (c & 3)));
+          rate_copy<kPair, 1>(scol + 8u * (c & 3), sdesc_scales_128x256b(sc_s + 4096u * (c & 3)));
       }
-      for (int j = 0; j < a.mmas; ++j) {
+#pragma unroll
+      for (int j = 0; j < kMmas; ++j) {
         const uint32_t q = static_cast<uint32_t>(j & 3);
-        const uint32_t id = a.kind == 0 ? idesc_mxf4(M, a.mma_n, (q & 1) * 2, (q & 1) * 2) : idesc_bf16(M, a.mma_n);
-        rate_mma<kPair>(a.kind, tmem, sdesc_sw128(a_s + 32u * q), sdesc_sw128(b_s + 32u * q), id,
-                        scol + 4u * (q >> 1), scol + 16u + 8u * (q >> 1));
+        rate_mma<kPair, kKind>(dcol, sdesc_sw128(a_s + 32u * q), sdesc_sw128(b_s + 32u * q), id[q & 1],
+                               scol + 4u * (q >> 1), scol + 16u + 8u * (q >> 1));
       }
-      rate_commit<kPair>(&ring[s % kRateRing]);
+      rate_commit<kPair>(&ring[issuer][s % kRateRing]);
     }
-    // Arrives (in both CTAs of a pair) once every MMA issued above is done.
-    rate_commit<kPair>(&done);
+    // Arrives (in both CTAs of a pair) once every instruction issued above is done.
+    rate_commit<kPair>(&done[issuer]);
   }
-  if (threadIdx.x == 0) {
+  if ((threadIdx.x & 31) == 0 && issuer < kIssuers) {
     bool late = false;
-    mbar_wait(&done, 0, late);   // bounded; the work above ends in microseconds
+    mbar_wait(&done[issuer], 0, late);   // bounded; the work above ends in microseconds
     t1 = globaltimer();
     abort = abort || late;
   }
+  __shared__ unsigned long long span[kIssuers];
+  if ((threadIdx.x & 31) == 0 && issuer < kIssuers) span[issuer] = abort ? 0ull : t1 - t0;
   tc_fence_before();
   __syncthreads();
   if (kPair) cluster_sync_all();   // the pair frees its TMEM together, after its last MMA
   tc_fence_after();
-  if (warp == 1) {
+  if (warp == 2) {
     if (kPair)
       asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kRateTmemCols) : "memory");
     else
       tmem_dealloc(tmem, kRateTmemCols);
   }
-  if (threadIdx.x == 0 && rank == 0) a.ns[kPair ? blockIdx.x / 2 : blockIdx.x] = abort ? 0ull : t1 - t0;
+  if (threadIdx.x == 0 && rank == 0) {
+    unsigned long long worst = 0;
+    bool any_zero = false;
+    for (int w = 0; w < kIssuers; ++w) {
+      worst = span[w] > worst ? span[w] : worst;
+      any_zero = any_zero || span[w] == 0;
+    }
+    a.ns[kPair ? blockIdx.x / 2 : blockIdx.x] = any_zero ? 0ull : worst;
+  }
 }
 
 // Each CTA of a 2-CTA cluster allocates 32 TMEM columns with cta_group::2
@@ -261,33 +277,64 @@ extern "C" mxfp4_status mxfp4_diag_pair_alloc_probe(uint32_t* addr_dev, void* st
              : MXFP4_ERR_CUDA;
 }
 
-extern "C" mxfp4_status mxfp4_diag_tensor_rate(int pair, int kind, int mma_n, int mmas, int copies, int copy_form,
-                                               int steps, int depth, unsigned long long* ns_dev, int* units,
-                                               void* stream) {
-  if (ns_dev == nullptr || units == nullptr) return MXFP4_ERR_INVALID_ARG;
-  if ((pair != 0 && pair != 1) || (kind != 0 && kind != 1) || (copy_form != 0 && copy_form != 1))
+namespace mx {
+
+// The measured instruction mixes: pair, kind, MMAs and scale copies per
+// step, copy form, issuing threads.
+struct RateVariant {
+  int pair, kind, mmas, copies, form, issuers;
+  void* kernel;
+};
+#define MX_RATE(P, K, MM, C, F, I) \
+  { P, K, MM, C, F, I, reinterpret_cast<void*>(tc_rate_kernel<P != 0, K, MM, C, F, I>) }
+static const RateVariant kRateVariants[] = {
+    MX_RATE(0, 0, 4, 0, 0, 1),  MX_RATE(0, 0, 4, 6, 0, 1),  MX_RATE(0, 0, 4, 4, 0, 1),
+    MX_RATE(0, 0, 4, 2, 1, 1),  MX_RATE(0, 0, 8, 0, 0, 1),  MX_RATE(0, 0, 16, 0, 0, 1),
+    MX_RATE(0, 0, 0, 6, 0, 1),  MX_RATE(0, 0, 4, 0, 0, 2),  MX_RATE(0, 0, 4, 4, 0, 2),
+    MX_RATE(0, 0, 16, 0, 0, 2), MX_RATE(1, 0, 4, 0, 0, 1),  MX_RATE(1, 0, 4, 6, 0, 1),
+    MX_RATE(1, 0, 4, 4, 0, 1),  MX_RATE(1, 0, 16, 0, 0, 1), MX_RATE(0, 1, 4, 0, 0, 1),
+    MX_RATE(1, 1, 4, 0, 0, 1),  MX_RATE(0, 1, 16, 0, 0, 1), MX_RATE(0, 1, 16, 0, 0, 2),
+};
+#undef MX_RATE
+constexpr int kNumRateVariants = static_cast<int>(sizeof(kRateVariants) / sizeof(kRateVariants[0]));
+
+}  // namespace mx
+
+extern "C" int mxfp4_diag_tensor_rate_variants(void) { return mx::kNumRateVariants; }
+
+extern "C" mxfp4_status mxfp4_diag_tensor_rate_info(int variant, int* info) {
+  if (variant < 0 || variant >= mx::kNumRateVariants || info == nullptr) return MXFP4_ERR_INVALID_ARG;
+  const mx::RateVariant& v = mx::kRateVariants[variant];
+  info[0] = v.pair;
+  info[1] = v.kind;
+  info[2] = v.mmas;
+  info[3] = v.copies;
+  info[4] = v.form;
+  info[5] = v.issuers;
+  return MXFP4_OK;
+}
+
+extern "C" mxfp4_status mxfp4_diag_tensor_rate(int variant, int mma_n, int steps, int depth,
+                                               unsigned long long* ns_dev, int* units, void* stream) {
+  if (ns_dev == nullptr || units == nullptr || variant < 0 || variant >= kNumRateVariants)
     return MXFP4_ERR_INVALID_ARG;
-  // N: a multiple of 16 in [16, 256] (one CTA), [64, 256] (a pair)
-  if (mma_n % 16 != 0 || mma_n > 256 || mma_n < (pair ? 64 : 16)) return MXFP4_ERR_INVALID_ARG;
-  if (depth < 1 || depth > kRateRing) return MXFP4_ERR_INVALID_ARG;
-  if (mmas < 0 || mmas > 16 || mmas + copies < 1 || copies < 0 || copies > (copy_form == 0 ? 8 : 4) || steps < 1 || steps > 1000000)
+  const RateVariant& v = kRateVariants[variant];
+  // N: a multiple of 16 in [16, 256] (one CTA), [64, 256] (a pair), at most 128 with two issuers
+  if (mma_n % 16 != 0 || mma_n > (v.issuers == 2 ? 128 : 256) || mma_n < (v.pair ? 64 : 16))
     return MXFP4_ERR_INVALID_ARG;
-  if (kind == 1 && copies != 0) return MXFP4_ERR_INVALID_ARG;   // bf16 MMAs take no scales
+  if (steps < 1 || steps > 1000000 || depth < 1 || depth > kRateRing) return MXFP4_ERR_INVALID_ARG;
   DeviceInfo dev;
   if (current_device_info(&dev) != cudaSuccess || !dev.ok) return MXFP4_ERR_NO_DEVICE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  RateArgs a{pair, kind, mma_n, mmas, copies, copy_form, steps, depth, ns_dev};
-  cudaError_t e;
-  if (pair == 0) {
-    e = cudaFuncSetAttribute(tc_rate_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRateSmem);
-    if (e != cudaSuccess) return MXFP4_ERR_CUDA;
+  RateArgs a{mma_n, steps, depth, ns_dev};
+  void* args[] = {&a};
+  cudaError_t e = cudaFuncSetAttribute(v.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRateSmem);
+  if (e != cudaSuccess) return MXFP4_ERR_CUDA;
+  if (v.pair == 0) {
     const int grid = dev.sm_count < mxfp4_diag_max_units() ? dev.sm_count : mxfp4_diag_max_units();
     *units = grid;
-    tc_rate_kernel<false><<<grid, 128, kRateSmem, s>>>(a);
-    e = cudaGetLastError();
+    e = cudaLaunchKernel(v.kernel, dim3(grid), dim3(128), args, kRateSmem, s);
   } else {
-    e = cudaFuncSetAttribute(tc_rate_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kRateSmem);
-    if (e != cudaSuccess) return MXFP4_ERR_CUDA;
     // as many pairs as the device holds at once, so every pair runs in one wave
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2, 1, 1);
@@ -301,15 +348,14 @@ extern "C" mxfp4_status mxfp4_diag_tensor_rate(int pair, int kind, int mma_n, in
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_rate_kernel<true>, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, v.kernel, &cfg) != cudaSuccess || n <= 0) {
       cudaGetLastError();
       n = dev.sm_count / 2;
     }
     if (n > dev.sm_count / 2) n = dev.sm_count / 2;
     if (n > mxfp4_diag_max_units()) n = mxfp4_diag_max_units();
     *units = n;
-    void* args[] = {&a};
-    e = launch_cluster2(reinterpret_cast<const void*>(tc_rate_kernel<true>), 2 * n, 128, kRateSmem, s, args);
+    e = launch_cluster2(v.kernel, 2 * n, 128, kRateSmem, s, args);
   }
   return e == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
 }
