@@ -870,6 +870,83 @@ def run_tc_rates(args):
                       "sms": props.multi_processor_count, "steps": steps, "clocks": clk}), flush=True)
 
 
+TIMELINE_POINTS = ("start", "w_req", "wait", "first_mma", "last_mma", "acc_done", "cluster", "done")
+
+
+def run_timeline(args):
+    """Per-call timeline of the decode sweep from the library's timeline build: the 15 calls of one
+    step replayed from a CUDA graph (steps back to back, as in the timed region), each decode
+    launch's CTAs stamping %globaltimer at fixed points.  Prints one table row per call: the
+    median over CTAs of each point, in microseconds from the call's earliest CTA start, and the
+    call's span from its dependency wait opening to its last CTA finishing."""
+    import numpy as np
+    import torch
+
+    from mxfp4_quantized_gemm_gb300 import build
+    build.build()
+    os.environ["MXFP4_GB300_LIB"] = build.build(variant="timeline")
+    from mxfp4_quantized_gemm_gb300 import capi, synth
+    dev = torch.device("cuda", 0)
+    cases = [(M, N, K) for M in DECODE_MS for (N, K) in DECODE_NK]
+    st = []
+    for i, (M, N, K) in enumerate(cases):
+        wc = synth.weight_codes(N, K, seed=0, tensor_id=2)
+        ws = synth.weight_scales(N, K, *W_SCALE_DECODE, seed=0, tensor_id=3)
+        pk = torch.empty(capi.mxfp4_packed_weight_bytes(1, N, K), dtype=torch.uint8, device=dev)
+        capi.mxfp4_pack_weights(torch.from_numpy(wc).to(dev), torch.from_numpy(ws).to(dev), 1, N, K, pk)
+        x = synth.bf16_tensor(synth.activations(M, K, seed=1 + i, tensor_id=1, outlier_frac=0.01)).to(dev)
+        wsb = capi.mxfp4_gemm_workspace_bytes(M, N, K)
+        st.append((M, N, K, pk, x, torch.empty(M, N, dtype=torch.bfloat16, device=dev),
+                   torch.zeros(wsb, dtype=torch.uint8, device=dev), wsb))
+    stream = torch.cuda.Stream(device=dev)
+    sptr = stream.cuda_stream
+
+    def step():
+        for (M, N, K, pk, x, out, work, wsb) in st:
+            capi.mxfp4_gemm(x, K, None, None, 0, pk, None, out, N, M, N, K, work, wsb, sptr)
+
+    with torch.cuda.stream(stream):
+        step()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(4):
+                step()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert capi.mxfp4_get_device_error(sptr) == capi.OK
+    stamps, nxt = capi.mxfp4_diag_decode_timeline()
+    n = len(cases)
+    rows = []
+    prev_end = None
+    for j in range(n):
+        slot = (nxt - n + j) % 64
+        a = stamps[slot].astype(np.int64)
+        live = a[:, 0] > 0
+        a = a[live]
+        t0 = a[:, 0].min()
+        rel = (a - t0) / 1e3
+        med = {TIMELINE_POINTS[p]: round(float(np.median(rel[:, p][a[:, p] > 0])), 2) if (a[:, p] > 0).any()
+               else None for p in range(8)}
+        wait_open = a[:, 2].min()
+        end = a[:, 7].max()
+        M, N, K = cases[j][:3]
+        rows.append({"case": f"M{M}_N{N}_K{K}", "ctas": int(live.sum()), "median_us": med,
+                     "last_done_us": round((end - t0) / 1e3, 2),
+                     "wait_open_us": round((wait_open - t0) / 1e3, 2),
+                     "span_wait_to_done_us": round((end - wait_open) / 1e3, 2),
+                     "gap_prev_done_to_wait_us": None if prev_end is None else round((wait_open - prev_end) / 1e3, 2)})
+        prev_end = end
+    print(json.dumps({"timeline": rows, "points": TIMELINE_POINTS}), flush=True)
+    hdr = "case".ljust(20) + "".join(p.rjust(10) for p in TIMELINE_POINTS) + "   gap  span(wait->done)"
+    print(hdr, file=sys.stderr)
+    for r in rows:
+        print(r["case"].ljust(20) + "".join(str(r["median_us"][p]).rjust(10) for p in TIMELINE_POINTS)
+              + f"  {r['gap_prev_done_to_wait_us']}  {r['span_wait_to_done_us']}", file=sys.stderr)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -891,11 +968,16 @@ def main():
     ap.add_argument("--tc-rates", action="store_true",
                     help="measure tensor-pipe issue rates (scale copies, MMAs, CTA pairs) and print one JSON line")
     ap.add_argument("--tc-steps", type=int, default=4000)
+    ap.add_argument("--timeline", action="store_true",
+                    help="per-call timeline of the decode sweep from the library's timeline build (one JSON line)")
     ap.add_argument("--calls", type=int, default=6)
     ap.add_argument("--copies", type=int, default=4)
     args = ap.parse_args()
     if args.tc_rates:
         run_tc_rates(args)
+        return
+    if args.timeline:
+        run_timeline(args)
         return
     if args.single:
         run_single(args)

@@ -73,6 +73,19 @@ MXFP4_API mxfp4_status mxfp4_diag_pair_alloc_probe(uint32_t* addr_dev, void* str
  * MXFP4_ERR_INVALID_ARG for a negative bound. */
 MXFP4_API mxfp4_status mxfp4_diag_set_wait_cycles(long long cycles);
 
+/* Per-call timeline of the decode GEMM kernel (the M <= 64 path of
+ * mxfp4_gemm), available only in the library's timeline build (compiled with
+ * -DMXFP4_STAMPS; build(variant="timeline")); the default build returns
+ * MXFP4_ERR_INVALID_ARG.  Copies to `host` (at least 64*256*8 uint64) the
+ * %globaltimer stamps, in ns, of the last 64 decode launches: element
+ * [call % 64][cta][point] with points 0 CTA start (after set-up), 1 first
+ * weight stages requested, 2 dependency wait passed, 3 first stage's operands
+ * complete (MMA thread), 4 last MMAs issued, 5 accumulator complete (drain),
+ * 6 split tile: parts visible across the cluster, 7 CTA done.  *next_call
+ * receives the number of decode launches so far (the slot of the next one,
+ * modulo 64).  Synchronous; stamps of launches still running are partial. */
+MXFP4_API mxfp4_status mxfp4_diag_decode_timeline(unsigned long long* host, size_t host_bytes, int* next_call);
+
 #ifdef __cplusplus
 }
 #endif

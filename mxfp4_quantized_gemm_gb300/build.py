@@ -2,6 +2,9 @@
 
 Each CUDA translation unit compiles in parallel; the objects link into one
 shared library next to this file.  Run ``python -m mxfp4_quantized_gemm_gb300.build``.
+``build(variant="timeline")`` builds the same sources with the decode
+kernel's timeline stamps compiled in (``libmxfp4_gb300_timeline.so``), for
+``bench.py --timeline``; the product library never carries them.
 """
 
 from __future__ import annotations
@@ -42,17 +45,22 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
+def build(verbose: bool = False, force: bool = False, variant: str = "default") -> str:
+    if variant not in ("default", "timeline"):
+        raise ValueError(f"unknown build variant {variant!r}")
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    build_dir = BUILD_DIR if variant == "default" else BUILD_DIR + "_" + variant
+    lib_path = LIB_PATH if variant == "default" else LIB_PATH.replace(".so", f"_{variant}.so")
+    extra = [] if variant == "default" else ["-DMXFP4_STAMPS"]
+    os.makedirs(build_dir, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     headers += [os.path.join(INCLUDE_DIR, f) for f in os.listdir(INCLUDE_DIR) if f.endswith(".h")]
 
     def compile_one(src: str) -> str:
         s = os.path.join(CSRC, src)
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
         if force or _stale(obj, [s] + headers):
-            cmd = [nvcc, *NVCC_FLAGS, "-I", INCLUDE_DIR, "-c", s, "-o", obj]
+            cmd = [nvcc, *NVCC_FLAGS, *extra, "-I", INCLUDE_DIR, "-c", s, "-o", obj]
             if verbose:
                 print(" ".join(cmd), flush=True)
             res = subprocess.run(cmd, capture_output=True, text=True)
@@ -64,14 +72,14 @@ def build(verbose: bool = False, force: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    if force or _stale(LIB_PATH, objs):
-        cmd = [nvcc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", *objs, "-o", LIB_PATH]
+    if force or _stale(lib_path, objs):
+        cmd = [nvcc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", *objs, "-o", lib_path]
         if verbose:
             print(" ".join(cmd), flush=True)
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"link failed:\n{res.stderr}")
-    return LIB_PATH
+    return lib_path
 
 
 if __name__ == "__main__":

@@ -6,7 +6,9 @@ kernels.  Arguments that are device buffers accept a torch tensor (its
 ``torch.cuda.Stream``, a raw ``cudaStream_t`` integer, or ``None`` for torch's
 current stream on the current device.  A non-OK status raises
 ``Mxfp4Error``.  Importing this module fails loudly when the library has not
-been built (``python -m mxfp4_quantized_gemm_gb300.build``).
+been built (``python -m mxfp4_quantized_gemm_gb300.build``).  The environment
+variable ``MXFP4_GB300_LIB`` selects another build of the same library (the
+timeline build of ``bench.py --timeline``).
 """
 
 from __future__ import annotations
@@ -14,7 +16,8 @@ from __future__ import annotations
 import ctypes
 import os
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmxfp4_gb300.so")
+_LIB_PATH = os.environ.get("MXFP4_GB300_LIB") or os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                                                               "libmxfp4_gb300.so")
 if not os.path.exists(_LIB_PATH):
     raise ImportError(
         f"{_LIB_PATH} is missing: build it with `python -m mxfp4_quantized_gemm_gb300.build` "
@@ -52,6 +55,7 @@ _SIGNATURES = {
     "mxfp4_diag_tensor_rate": (_i, [_i, _i, _i, _i, _p, ctypes.POINTER(_i), _p]),
     "mxfp4_diag_pair_alloc_probe": (_i, [_p, _p]),
     "mxfp4_diag_set_wait_cycles": (_i, [ctypes.c_longlong]),
+    "mxfp4_diag_decode_timeline": (_i, [_p, _sz, ctypes.POINTER(_i)]),
 }
 for _name, (_res, _args) in _SIGNATURES.items():
     _fn = getattr(lib, _name)
@@ -201,3 +205,14 @@ def mxfp4_diag_pair_alloc_probe(addr_dev, stream=None) -> None:
 
 def mxfp4_diag_set_wait_cycles(cycles: int) -> None:
     _check(lib.mxfp4_diag_set_wait_cycles(cycles), "mxfp4_diag_set_wait_cycles")
+
+
+def mxfp4_diag_decode_timeline():
+    """(stamps [64 calls][256 CTAs][8 points] uint64 ns as a numpy array, next call slot) from the
+    timeline build; raises Mxfp4Error on the default build."""
+    import numpy as np
+    buf = np.zeros((64, 256, 8), dtype=np.uint64)
+    nxt = _i(0)
+    _check(lib.mxfp4_diag_decode_timeline(buf.ctypes.data, buf.nbytes, ctypes.byref(nxt)),
+           "mxfp4_diag_decode_timeline")
+    return buf, nxt.value

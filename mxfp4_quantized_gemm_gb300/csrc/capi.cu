@@ -323,6 +323,14 @@ mxfp4_status mxfp4_diag_set_wait_cycles(long long cycles) {
   return MXFP4_OK;
 }
 
+mxfp4_status mxfp4_diag_decode_timeline(unsigned long long* host, size_t host_bytes, int* next_call) {
+  if (host == nullptr || next_call == nullptr || host_bytes < 64u * 256u * 8u * sizeof(unsigned long long))
+    return MXFP4_ERR_INVALID_ARG;
+  const int n = decode_stamps(host, next_call);
+  if (n == 0) return MXFP4_ERR_INVALID_ARG;   // the default build carries no stamps
+  return n > 0 ? MXFP4_OK : MXFP4_ERR_CUDA;
+}
+
 mxfp4_status mxfp4_get_device_error(void* stream) {
   DeviceInfo dev;
   mxfp4_status st = device_ready(&dev);

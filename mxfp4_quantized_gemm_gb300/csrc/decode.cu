@@ -53,6 +53,22 @@ namespace mx {
 
 static __device__ uint32_t g_decode_error;
 
+// Timeline stamps (built only with -DMXFP4_STAMPS, the library's timeline
+// variant): %globaltimer at fixed points of every CTA of the last
+// kStampCalls launches, for the per-call timeline the benchmark prints.
+#ifdef MXFP4_STAMPS
+constexpr int kStampCalls = 64, kStampCtas = 256, kStampPoints = 8;
+static __device__ unsigned long long g_stamps[kStampCalls][kStampCtas][kStampPoints];
+__device__ __forceinline__ void stamp_at(int call, int point) {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  if (blockIdx.x < kStampCtas) g_stamps[call][blockIdx.x][point] = t;
+}
+#define MX_STAMP(p) stamp_at(g.stamp_call, p)
+#else
+#define MX_STAMP(p) ((void)0)
+#endif
+
 struct DecodeArgs {
   const uint16_t* x;       // bf16 activations [M][ldx], quantized in the kernel; null: a_codes/a_scales
   int ldx;
@@ -65,6 +81,9 @@ struct DecodeArgs {
   int M, K, KT;
   int n_tiles;             // ceil(N / 256)
   int split;               // CTAs per tile = cluster size; 1: CTAs take whole tiles
+#ifdef MXFP4_STAMPS
+  int stamp_call;          // slot of this launch in the stamp buffer
+#endif
 };
 
 constexpr int kLoadAhead = 8;        // x loads in flight per quantizing warp
@@ -196,7 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
   // The next kernel in the stream waits for this one to complete before it
   // touches memory, so it may be launched now; its CTAs take SMs as this
   // kernel's CTAs leave.
-  if (threadIdx.x == 0) griddep_launch_dependents();
+  if (threadIdx.x == 0) {
+    griddep_launch_dependents();
+    MX_STAMP(0);
+  }
 
   if (warp == 0) {
     // ---- producer: the weight block of each stage (one bulk copy), and in
@@ -226,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       mbar_arrive_expect_tx(&full[lane], static_cast<uint32_t>(C::kW));
       w_load(lane, smem + lane * C::kStageBytes, &full[lane]);
     }
+    if (lane == 0) MX_STAMP(1);
     if (prequant) {
       griddep_wait();   // the activations may come from the kernel before this one
       if (lane < npre) a_load(lane, smem + lane * C::kStageBytes, &full[lane]);
@@ -253,11 +276,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
           const int s = i % C::kStages;
           if (!mbar_wait(&full[s], (i / C::kStages) & 1, abort)) break;
           tc_fence_after();
+          if (i == 0) MX_STAMP(3);
           issue_stage_mma<C>(tmem, smem_u32(smem + s * C::kStageBytes), s, j != 0 ? 1u : 0u);
           mma_commit(&empty[s]);
         }
         mma_commit(acc_full);
       }
+      MX_STAMP(4);
       // TMEM is freed only after the last drain has read the accumulator.
       mbar_wait(acc_empty, (n_my & 1) ^ 1, abort);
     }
@@ -280,6 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       }
     }
     griddep_wait();
+    if (threadIdx.x == 64) MX_STAMP(2);
     const int w = multi_tile ? (warp & 1) + ((warp >> 1) & 2) : warp - 2;
     if (!prequant && (!multi_tile || (warp & 3) >= 2)) {
       // Items (stage i, row r) for rows r = w, w + n_qwarps, ... < M, in stage
@@ -360,6 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
         const int t = t0 + tl * t_step;
         const bool ok = mbar_wait(acc_full, tl & 1, abort);
         tc_fence_after();
+        if (threadIdx.x == 128 && tl == n_my - 1) MX_STAMP(5);
 #pragma unroll
         for (int pass = 0; pass < 2; ++pass) {
           uint32_t r[64];
@@ -409,6 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     // second barrier keeps every CTA's shared memory alive until all reads
     // of it are done.
     cluster_sync_all();
+    if (threadIdx.x == 0) MX_STAMP(6);
     if (warp >= 2) {
       const int S = g.split;
       const int rank = blockIdx.x % S;
@@ -438,6 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     }
     cluster_sync_all();
   }
+  if (threadIdx.x == 0) MX_STAMP(7);
   if (abort) atomicOr(&g_decode_error, kErrTimeout);
 }
 
@@ -445,6 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 // Per-device, per-kernel host caches; several host threads may fill them
 // at once, each writing the same value.
 static std::atomic<bool> g_attr_set[64][6];
+#ifdef MXFP4_STAMPS
+static std::atomic<int> g_stamp_next{0};   // stamp slot of the next launch (in launch order)
+#endif
 static std::atomic<int> g_max_clusters[64][6][9];   // co-resident clusters of size S (0: not yet queried)
 
 template <int kRowsA, bool kQ>
@@ -543,6 +575,9 @@ cudaError_t launch_decode(const DecodeProblem& p, const DeviceInfo& dev, cudaStr
   a.K = p.K;
   a.KT = static_cast<int>(padded_k(p.K) / kKTile);
   a.n_tiles = static_cast<int>(ceil_div(p.N, kTileN));
+#ifdef MXFP4_STAMPS
+  a.stamp_call = g_stamp_next.fetch_add(1) % kStampCalls;
+#endif
   if (p.qcodes != nullptr) {
     switch (gemm_rows_a(p.M)) {
       case 16: return launch_rows<16, true>(a, dev, s, 3);
@@ -556,6 +591,16 @@ cudaError_t launch_decode(const DecodeProblem& p, const DeviceInfo& dev, cudaStr
     default: return launch_rows<64, false>(a, dev, s, 2);
   }
 }
+
+#ifdef MXFP4_STAMPS
+int decode_stamps(unsigned long long* host, int* next_call) {
+  *next_call = g_stamp_next.load();
+  if (cudaMemcpyFromSymbol(host, g_stamps, sizeof(g_stamps)) != cudaSuccess) return -1;
+  return kStampCalls * kStampCtas * kStampPoints;
+}
+#else
+int decode_stamps(unsigned long long*, int*) { return 0; }
+#endif
 
 uint32_t decode_read_clear_error() {
   uint32_t v = 0, zero = 0;

@@ -112,6 +112,10 @@ struct DecodeProblem {
 };
 cudaError_t launch_decode(const DecodeProblem& p, const DeviceInfo& dev, cudaStream_t s);
 uint32_t decode_read_clear_error();
+// Timeline stamps of the last decode launches (timeline build only): copies
+// the stamp buffer to `host` and returns its element count, 0 in the default
+// build, -1 on a CUDA error; *next_call = slot of the next launch.
+int decode_stamps(unsigned long long* host, int* next_call);
 
 // bmm.cu
 cudaError_t launch_bmm(const void* x, const uint8_t* w_packed, void* out, int B, int M, int N, int K,
