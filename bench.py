@@ -831,11 +831,14 @@ def run_tc_rates(args):
     clocks = ClockSampler(0)
     clocks.start()
     rows = []
+    only = None if args.tc_only is None else {int(v) for v in args.tc_only.split(",")}
     for var in range(capi.mxfp4_diag_tensor_rate_variants()):
+        if only is not None and var not in only:
+            continue
         info = capi.mxfp4_diag_tensor_rate_info(var)
         pair, kind, mmas, copies, form, issuers = (info[k] for k in ("pair", "kind", "mmas", "copies", "form",
                                                                     "issuers"))
-        name = (f"{'mxf4' if kind == 0 else 'bf16'} {'2cta' if pair else '1cta'} {mmas} mma"
+        name = (f"{('mxf4', 'bf16', 'mxf4nvf4')[kind]} {'2cta' if pair else '1cta'} {mmas} mma"
                 + (f" + {copies} cp{'128x256b' if form else ''}" if copies else "")
                 + (f" x{issuers} issuers" if issuers > 1 else ""))
         for n, depth in TC_RATE_POINTS:
@@ -845,7 +848,7 @@ def run_tc_rates(args):
                 rows.append({"name": name, "skipped": "cta_group::2 allocation is not collective"})
                 break
             m = 256 if pair else 128
-            k = 64 if kind == 0 else 16
+            k = 16 if kind == 1 else 64
             meds = []
             for _ in range(3):
                 ns.zero_()
@@ -862,10 +865,12 @@ def run_tc_rates(args):
                          "ns_per_mma": round(ns_step / mmas, 1) if mmas else None,
                          "tflops": round(flop / (med * 1e-9) / 1e12, 1)})
     clk = clocks.stop()
-    fp4 = [r["tflops"] for r in rows if r["name"].startswith("mxf4") and "cp" not in r["name"] and "tflops" in r]
+    fp4 = [r["tflops"] for r in rows if r["name"].startswith("mxf4 ") and "cp" not in r["name"] and "tflops" in r]
+    nvf4 = [r["tflops"] for r in rows if r["name"].startswith("mxf4nvf4") and "cp" not in r["name"] and "tflops" in r]
     bf16 = [r["tflops"] for r in rows if r["name"].startswith("bf16") and "tflops" in r]
     print(json.dumps({"tc_rates": rows, "pair_alloc": {"cols": cols, "collective": pair_ok},
                       "mxf4_dense_peak_tflops": max(fp4) if fp4 else None,
+                      "mxf4nvf4_2x_dense_peak_tflops": max(nvf4) if nvf4 else None,
                       "bf16_dense_peak_tflops": max(bf16) if bf16 else None,
                       "sms": props.multi_processor_count, "steps": steps, "clocks": clk}), flush=True)
 
@@ -968,6 +973,8 @@ def main():
     ap.add_argument("--tc-rates", action="store_true",
                     help="measure tensor-pipe issue rates (scale copies, MMAs, CTA pairs) and print one JSON line")
     ap.add_argument("--tc-steps", type=int, default=4000)
+    ap.add_argument("--tc-only", type=str, default=None,
+                    help="with --tc-rates: comma-separated variant indexes to measure (default all)")
     ap.add_argument("--timeline", action="store_true",
                     help="per-call timeline of the decode sweep from the library's timeline build (one JSON line)")
     ap.add_argument("--calls", type=int, default=6)

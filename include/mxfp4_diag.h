@@ -31,7 +31,8 @@ MXFP4_API int mxfp4_diag_max_units(void);
  * mxfp4_diag_tensor_rate_info(variant, info) fills info[0..5] with the mix:
  * pair (1: cta_group::2 over a 2-CTA cluster, M = 256; 0: one CTA, M = 128),
  * kind (0: kind::mxf4.block_scale.scale_vec::2X, E2M1 x E2M1 with UE8M0
- * scales, K = 64; 1: kind::f16, bf16 x bf16, K = 16), MMAs per step, scale
+ * scales, K = 64; 1: kind::f16, bf16 x bf16, K = 16; 2: the kind 0 product
+ * issued as kind::mxf4nvf4.block_scale.scale_vec::2X), MMAs per step, scale
  * copies per step, copy form (0: tcgen05.cp.32x128b.warpx4, 1:
  * tcgen05.cp.128x256b), issuing threads per CTA (1, or 2 with separate
  * accumulators of N <= 128 columns each).

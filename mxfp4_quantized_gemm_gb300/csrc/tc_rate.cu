@@ -79,7 +79,24 @@ __device__ __forceinline__ void rate_copy(uint32_t taddr, uint64_t desc) {
 template <bool kPair, int kKind>
 __device__ __forceinline__ void rate_mma(uint32_t d, uint64_t ad, uint64_t bd, uint32_t id, uint32_t sfa,
                                          uint32_t sfb) {
-  if (kKind == 0) {
+  if (kKind == 2) {
+    // the same block-scaled E2M1 product (UE8M0 scales, one per 32 elements)
+    // issued as kind::mxf4nvf4
+    if (kPair)
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, 1, 0;\n\t"
+          "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::
+              "r"(d),
+          "l"(ad), "l"(bd), "r"(id), "r"(sfa), "r"(sfb)
+          : "memory");
+    else
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, 1, 0;\n\t"
+          "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::
+              "r"(d),
+          "l"(ad), "l"(bd), "r"(id), "r"(sfa), "r"(sfb)
+          : "memory");
+  } else if (kKind == 0) {
     if (kPair)
       asm volatile(
           "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, 1, 0;\n\t"
@@ -114,7 +131,7 @@ __device__ __forceinline__ void rate_commit(uint64_t* bar) {
 }
 
 // One instruction mix, fully unrolled: kMmas MMAs of kind kKind (0: mxf4,
-// 1: bf16) after kCopies scale copies of form kForm per step, issued by
+// 1: bf16, 2: the mxf4 product issued as kind::mxf4nvf4) after kCopies scale copies of form kForm per step, issued by
 // kIssuers threads of the CTA (lane 0 of warps 0 and 1), each into its own
 // accumulator (columns 0.. and 128.. ; N <= 128 with two issuers) and its
 // own scale columns (256.. and 384..).
@@ -165,7 +182,7 @@ __global__ void __launch_bounds__(128, 1) tc_rate_kernel(const RateArgs a) {
     const uint32_t scbase = tmem + 256u + 128u * static_cast<uint32_t>(issuer);
     const int total = kRateWarm + a.steps;
     uint32_t id[2];
-    for (int h = 0; h < 2; ++h) id[h] = kKind == 0 ? idesc_mxf4(M, a.mma_n, h * 2, h * 2) : idesc_bf16(M, a.mma_n);
+    for (int h = 0; h < 2; ++h) id[h] = kKind != 1 ? idesc_mxf4(M, a.mma_n, h * 2, h * 2) : idesc_bf16(M, a.mma_n);
     for (int s = 0; s < total; ++s) {
       if (s >= a.depth) {
         const int w = s - a.depth;
@@ -294,6 +311,7 @@ static const RateVariant kRateVariants[] = {
     MX_RATE(0, 0, 16, 0, 0, 2), MX_RATE(1, 0, 4, 0, 0, 1),  MX_RATE(1, 0, 4, 6, 0, 1),
     MX_RATE(1, 0, 4, 4, 0, 1),  MX_RATE(1, 0, 16, 0, 0, 1), MX_RATE(0, 1, 4, 0, 0, 1),
     MX_RATE(1, 1, 4, 0, 0, 1),  MX_RATE(0, 1, 16, 0, 0, 1), MX_RATE(0, 1, 16, 0, 0, 2),
+    MX_RATE(0, 2, 16, 0, 0, 1), MX_RATE(0, 2, 4, 4, 0, 1),  MX_RATE(1, 2, 16, 0, 0, 1),
 };
 #undef MX_RATE
 constexpr int kNumRateVariants = static_cast<int>(sizeof(kRateVariants) / sizeof(kRateVariants[0]));
