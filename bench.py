@@ -925,12 +925,16 @@ def run_timeline(args):
     stamps, nxt = capi.mxfp4_diag_decode_timeline()
     n = len(cases)
     rows = []
+    raw = {}
     prev_end = None
     for j in range(n):
-        slot = (nxt - n + j) % 64
-        a = stamps[slot].astype(np.int64)
-        live = a[:, 0] > 0
-        a = a[live]
+        seq = nxt - n + j
+        a = stamps[seq % 64].astype(np.uint64)
+        live = (a[:, 0] >> np.uint64(48)) == np.uint64(seq & 0xFFFF)
+        a = a[live].copy()
+        a[:, 0] &= np.uint64(0xFFFFFFFFFFFF)
+        a = a.astype(np.int64)
+        raw[cases[j]] = a
         t0 = a[:, 0].min()
         rel = (a - t0) / 1e3
         med = {TIMELINE_POINTS[p]: round(float(np.median(rel[:, p][a[:, p] > 0])), 2) if (a[:, p] > 0).any()
@@ -944,6 +948,8 @@ def run_timeline(args):
                      "span_wait_to_done_us": round((end - wait_open) / 1e3, 2),
                      "gap_prev_done_to_wait_us": None if prev_end is None else round((wait_open - prev_end) / 1e3, 2)})
         prev_end = end
+    if args.timeline_raw:
+        np.savez(args.timeline_raw, **{f"M{M}_N{N}_K{K}": a for (M, N, K), a in raw.items()})
     print(json.dumps({"timeline": rows, "points": TIMELINE_POINTS}), flush=True)
     hdr = "case".ljust(20) + "".join(p.rjust(10) for p in TIMELINE_POINTS) + "   gap  span(wait->done)"
     print(hdr, file=sys.stderr)
@@ -975,6 +981,8 @@ def main():
     ap.add_argument("--tc-steps", type=int, default=4000)
     ap.add_argument("--tc-only", type=str, default=None,
                     help="with --tc-rates: comma-separated variant indexes to measure (default all)")
+    ap.add_argument("--timeline-raw", type=str, default=None,
+                    help="with --timeline: also save every CTA's stamps (ns) to this .npz file")
     ap.add_argument("--timeline", action="store_true",
                     help="per-call timeline of the decode sweep from the library's timeline build (one JSON line)")
     ap.add_argument("--calls", type=int, default=6)

@@ -82,9 +82,12 @@ MXFP4_API mxfp4_status mxfp4_diag_set_wait_cycles(long long cycles);
  * [call % 64][cta][point] with points 0 CTA start (after set-up), 1 first
  * weight stages requested, 2 dependency wait passed, 3 first stage's operands
  * complete (MMA thread), 4 last MMAs issued, 5 accumulator complete (drain),
- * 6 split tile: parts visible across the cluster, 7 CTA done.  *next_call
- * receives the number of decode launches so far (the slot of the next one,
- * modulo 64).  Synchronous; stamps of launches still running are partial. */
+ * 6 split tile: parts visible across the cluster, 7 CTA done.  Point 0
+ * carries the launch's sequence number (modulo 2^16) in its top 16 bits and
+ * the time in the low 48, so rows left by an older launch in the same slot
+ * can be discarded.  *next_call receives the number of decode launches so
+ * far (the sequence number of the next one).  Synchronous; stamps of
+ * launches still running are partial. */
 MXFP4_API mxfp4_status mxfp4_diag_decode_timeline(unsigned long long* host, size_t host_bytes, int* next_call);
 
 #ifdef __cplusplus
