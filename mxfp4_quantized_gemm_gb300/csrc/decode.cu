@@ -20,8 +20,7 @@
 //    leaves its fp32 partial tile in its own shared memory and, after one
 //    cluster barrier, sums a 1/S column share of all S partials through
 //    distributed shared memory (in rank order, so the result is the same
-//    for every call; all of a thread's remote loads in flight at once),
-//    adds the bias and stores bf16.  No CTA ever waits for
+//    for every call), adds the bias and stores bf16.  No CTA ever waits for
 //    a CTA outside its cluster, and the kernel needs no global scratch;
 //  * with at least as many tiles as SMs (S = 1) each CTA takes whole tiles;
 //  * the kernel is a programmatic dependent launch and lets its own
@@ -87,7 +86,7 @@ struct DecodeArgs {
   int n_tiles;             // ceil(N / 256)
   int split;               // CTAs per tile = cluster size; 1: CTAs take whole tiles
 #ifdef MXFP4_STAMPS
-  int stamp_call;          // sequence number of this launch (slot = seq % kStampCalls)
+  int stamp_call;          // slot of this launch in the stamp buffer
 #endif
 };
 
@@ -153,49 +152,6 @@ __device__ __forceinline__ void split_sum_store_q(const OutView o, int M, int S,
         if ((n >> 1) + 1 < row_bytes) dst[1] = static_cast<uint8_t>(codes >> 8);
       }
       if (sub == 0) o.qscales[static_cast<size_t>(r) * ((o.N + 31) >> 5) + (n >> 5)] = static_cast<uint8_t>(sbyte);
-    }
-  }
-}
-
-// bf16 output of a split tile: the CTA of rank `rank` takes column chunks
-// [64 rank / S, 64 (rank + 1) / S) of every live row and sums them over the
-// S parts in rank order (the same order for every call), then adds the bias
-// and stores.  Every remote load a thread needs (at most 21 float4 for
-// M <= 64) is issued before the first is used, so the sum waits one
-// distributed-shared-memory round trip, not one per item; the thread then
-// arrives on the cluster barrier that lets the other CTAs free their shared
-// memory, before its stores.  Called by warps 2..9.
-template <int S>
-__device__ __forceinline__ void split_sum_store(const OutView& o, int M, int rank, uint32_t pbase, int n0) {
-  constexpr int kMaxNq = (64 + S - 1) / S;
-  constexpr int kItems = (kDecodeMaxM * kMaxNq + kEpiThreads - 1) / kEpiThreads;
-  const int q_lo = rank * 64 / S, nq = (rank + 1) * 64 / S - q_lo;
-  const int total = M * nq;
-  const int t = static_cast<int>(threadIdx.x) - 64;
-  float4 p[kItems][S];
-#pragma unroll
-  for (int it = 0; it < kItems; ++it) {
-    const int gi = t + it * kEpiThreads;
-    if (gi < total) {
-      const uint32_t a = pbase + partial_off(gi / nq, q_lo + gi % nq);
-#pragma unroll
-      for (int k = 0; k < S; ++k) p[it][k] = ld_shared_cluster_f4(mapa_shared(a, static_cast<uint32_t>(k)));
-    }
-  }
-  cluster_arrive_release();
-#pragma unroll
-  for (int it = 0; it < kItems; ++it) {
-    const int gi = t + it * kEpiThreads;
-    if (gi < total) {
-      float4 acc = p[it][0];
-#pragma unroll
-      for (int k = 1; k < S; ++k) {
-        acc.x += p[it][k].x;
-        acc.y += p[it][k].y;
-        acc.z += p[it][k].z;
-        acc.w += p[it][k].w;
-      }
-      store_quad(o, gi / nq, n0 + 4 * (q_lo + gi % nq), acc);
     }
   }
 }
@@ -488,27 +444,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     if (warp >= 2) {
       const int S = g.split;
       const int rank = blockIdx.x % S;
+      const int q_lo = rank * 64 / S, nq = (rank + 1) * 64 / S - q_lo;
       const uint32_t pbase = smem_u32(smem);
       const int n0 = t0 * kTileN;
-      if (kQ) {
-        split_sum_store_q(g.o, g.M, S, rank, pbase, n0);
-        cluster_arrive_release();
-      } else {
-        switch (S) {
-          case 2: split_sum_store<2>(g.o, g.M, rank, pbase, n0); break;
-          case 3: split_sum_store<3>(g.o, g.M, rank, pbase, n0); break;
-          case 4: split_sum_store<4>(g.o, g.M, rank, pbase, n0); break;
-          case 5: split_sum_store<5>(g.o, g.M, rank, pbase, n0); break;
-          case 6: split_sum_store<6>(g.o, g.M, rank, pbase, n0); break;
-          case 7: split_sum_store<7>(g.o, g.M, rank, pbase, n0); break;
-          default: split_sum_store<8>(g.o, g.M, rank, pbase, n0); break;
+      if (kQ) split_sum_store_q(g.o, g.M, S, rank, pbase, n0);
+      for (int gi = threadIdx.x - 64; !kQ && gi < g.M * nq; gi += kEpiThreads) {
+        const int r = gi / nq, qq = q_lo + gi % nq;
+        const uint32_t a = pbase + partial_off(r, qq);
+        float4 p[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (k < S) p[k] = ld_shared_cluster_f4(mapa_shared(a, static_cast<uint32_t>(k)));
+        float4 acc = p[0];
+#pragma unroll
+        for (int k = 1; k < 8; ++k) {
+          if (k < S) {
+            acc.x += p[k].x;
+            acc.y += p[k].y;
+            acc.z += p[k].z;
+            acc.w += p[k].w;
+          }
         }
+        store_quad(g.o, r, n0 + 4 * qq, acc);
       }
-    } else {
-      cluster_arrive_release();
     }
-    // every CTA's shared memory stays until all reads of it are done
-    cluster_wait_acquire();
+    cluster_sync_all();
   }
   if (threadIdx.x == 0) MX_STAMP(7);
   if (abort) atomicOr(&g_decode_error, kErrTimeout);

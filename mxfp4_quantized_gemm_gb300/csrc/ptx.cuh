@@ -241,15 +241,6 @@ __device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31) == 0; 
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// The two halves of that barrier: a thread's arrival (its earlier shared-
-// memory accesses, local or remote, ordered before it) and the wait for
-// every thread of the cluster to have arrived.
-__device__ __forceinline__ void cluster_arrive_release() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait_acquire() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 // Address of the same shared-memory location in the CTA of cluster rank `rank`.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
