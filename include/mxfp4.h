@@ -259,6 +259,39 @@ MXFP4_API mxfp4_status mxfp4_gemm_mxfp4_out(const void* a_bf16_dev, int lda,
                                             void* workspace_dev, size_t workspace_bytes, void* stream);
 
 /*
+ * The same GEMM with the split + cat fused epilogue.  The pages name it only:
+ * a 5-tuple activation input requests the Triton-only fused "split + cat"
+ * epilogue (fused_gemm_afp4wfp4_split_cat), which their ASM path rejects
+ * (sglang PR #39598 blog analysis, section 2: _asm_fp4_prequantized_input,
+ * the fused_gemm_afp4wfp4_split_cat import; PR #39598 Motivation,
+ * "Limitation").  The plainest reading of the name is taken: the GEMM's
+ * bf16 result (+ bias), computed and rounded exactly as mxfp4_gemm computes
+ * it, is viewed as H = N / (s1 + s2) groups of s1 + s2 columns; the first s1
+ * columns of group h are concatenated with the caller's z[m][h] (s3 values)
+ * into out_cat, the other s2 go to out_split:
+ *   out_cat[m][h][j]        = y[m][h (s1 + s2) + j]          j < s1
+ *   out_cat[m][h][s1 + j]   = z[m][h][j]                     j < s3
+ *   out_split[m][h][j]      = y[m][h (s1 + s2) + s1 + j]     j < s2
+ * (the multi-head key/value projection pattern: per head, a part joined with
+ * a separately computed part and a part kept apart).
+ *
+ *   z_dev          bf16 [M][H][s3], contiguous (ignored when s3 == 0)
+ *   out_cat_dev    bf16 [M][H][s1 + s3], contiguous (ignored when s1 + s3 == 0)
+ *   out_split_dev  bf16 [M][H][s2], contiguous (ignored when s2 == 0)
+ * The activation, weight, bias and workspace arguments are mxfp4_gemm's
+ * (mxfp4_gemm_workspace_bytes sizes the workspace).  s1, s2, s3 >= 0,
+ * s1 + s2 > 0 (INVALID_ARG); s1, s2, s3 multiples of 8 and N a multiple of
+ * s1 + s2 (UNSUPPORTED_SHAPE); the three tensors 16-byte aligned
+ * (MISALIGNED).  Other errors: those of mxfp4_gemm.
+ */
+MXFP4_API mxfp4_status mxfp4_gemm_split_cat(const void* a_bf16_dev, int lda,
+                                            const uint8_t* a_codes_dev, const uint8_t* a_scales_dev,
+                                            mxfp4_layout a_layout, const void* w_packed_dev,
+                                            const void* bias_dev, int M, int N, int K, int s1, int s2,
+                                            const void* z_dev, int s3, void* out_cat_dev, void* out_split_dev,
+                                            void* workspace_dev, size_t workspace_bytes, void* stream);
+
+/*
  * A16WFP4 batched matmul for the MLA absorbed K-up / V-up projections
  * (PR #34317, Modifications): bf16 activations against FP4 weights with E8M0
  * scales, no activation quantization:

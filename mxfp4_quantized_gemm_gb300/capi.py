@@ -45,6 +45,7 @@ _SIGNATURES = {
     "mxfp4_gemm_workspace_bytes": (_sz, [_i, _i, _i]),
     "mxfp4_gemm": (_i, [_p, _i, _p, _p, _i, _p, _p, _p, _i, _i, _i, _i, _p, _sz, _p]),
     "mxfp4_gemm_mxfp4_out": (_i, [_p, _i, _p, _p, _i, _p, _p, _p, _p, _i, _i, _i, _p, _sz, _p]),
+    "mxfp4_gemm_split_cat": (_i, [_p, _i, _p, _p, _i, _p, _p, _i, _i, _i, _i, _i, _p, _i, _p, _p, _p, _sz, _p]),
     "a16wfp4_bmm": (_i, [_p, _p, _p, _i, _i, _i, _i, _i, _p]),
     "mxfp4_get_device_error": (_i, [_p]),
     "mxfp4_gemm_noalloc": (_i, [_p, _i, _p, _p, _p, _i, _i, _i, _i, _p]),
@@ -150,6 +151,15 @@ def mxfp4_gemm_mxfp4_out(a_bf16, lda: int, a_codes, a_scales, a_layout: int, w_p
                                     _ptr(bias), _ptr(out_codes), _ptr(out_scales), M, N, K, _ptr(workspace),
                                     workspace_bytes, _stream(stream)),
            "mxfp4_gemm_mxfp4_out")
+
+
+def mxfp4_gemm_split_cat(a_bf16, lda: int, a_codes, a_scales, a_layout: int, w_packed, bias, M: int, N: int,
+                         K: int, s1: int, s2: int, z, s3: int, out_cat, out_split, workspace, workspace_bytes: int,
+                         stream=None) -> None:
+    _check(lib.mxfp4_gemm_split_cat(_ptr(a_bf16), lda, _ptr(a_codes), _ptr(a_scales), a_layout, _ptr(w_packed),
+                                    _ptr(bias), M, N, K, s1, s2, _ptr(z), s3, _ptr(out_cat), _ptr(out_split),
+                                    _ptr(workspace), workspace_bytes, _stream(stream)),
+           "mxfp4_gemm_split_cat")
 
 
 def a16wfp4_bmm(x, w_packed, out, B: int, M: int, N: int, K: int, out_layout: int, stream=None) -> None:

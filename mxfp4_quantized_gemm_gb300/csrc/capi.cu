@@ -1,6 +1,7 @@
 // C ABI of the library (declared in include/mxfp4.h): argument checks on
 // the host, workspace carving, dispatch to the kernels of quant.cu, gemm.cu
 // and bmm.cu.  No entry point allocates device memory.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <atomic>
 #include <cstdint>
@@ -179,17 +180,26 @@ size_t mxfp4_gemm_workspace_bytes(int M, int N, int K) {
   return gemm_workspace_layout(M, N, K, current_gemm_grid()).total;
 }
 
-// The GEMM behind mxfp4_gemm (bf16 `out`) and mxfp4_gemm_mxfp4_out
-// (qcodes / qscales set, `out` unused).
+// The split + cat output form of mxfp4_gemm_split_cat (on: selected).
+struct SplitCat {
+  bool on;
+  void* cat;
+  void* split;
+  const void* z;
+  int s1, s2, s3;
+};
+
+// The GEMM behind mxfp4_gemm (bf16 `out`), mxfp4_gemm_mxfp4_out (qcodes /
+// qscales set, `out` unused) and mxfp4_gemm_split_cat (sc.on).
 static mxfp4_status gemm_any(const void* a_bf16, int lda, const uint8_t* a_codes, const uint8_t* a_scales,
                              mxfp4_layout a_layout, const void* w_packed, const void* bias, void* out, int ldo,
                              uint8_t* qcodes, uint8_t* qscales, int M, int N, int K, void* workspace,
-                             size_t workspace_bytes, void* stream) {
-  const bool quant_out = qcodes != nullptr;
-  if (w_packed == nullptr || (!quant_out && out == nullptr) || (quant_out && qscales == nullptr))
+                             size_t workspace_bytes, void* stream, const SplitCat& sc = SplitCat{}) {
+  const bool quant_out = qcodes != nullptr || sc.on;   // no bf16 [M][ldo] output
+  if (w_packed == nullptr || (!quant_out && out == nullptr) || (qcodes != nullptr && qscales == nullptr))
     return MXFP4_ERR_INVALID_ARG;
   if (M <= 0 || N <= 0 || K <= 0) return MXFP4_ERR_INVALID_ARG;
-  if (quant_out && (N & 1)) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  if (qcodes != nullptr && (N & 1)) return MXFP4_ERR_UNSUPPORTED_SHAPE;
   const bool from_bf16 = a_bf16 != nullptr;
   if (from_bf16 && (a_codes != nullptr || a_scales != nullptr)) return MXFP4_ERR_INVALID_ARG;
   if (!from_bf16 && (a_codes == nullptr || a_scales == nullptr)) return MXFP4_ERR_INVALID_ARG;
@@ -232,6 +242,13 @@ static mxfp4_status gemm_any(const void* a_bf16, int lda, const uint8_t* a_codes
     d.K = K;
     d.qcodes = qcodes;
     d.qscales = qscales;
+    d.splitcat = sc.on;
+    d.cat = sc.cat;
+    d.split = sc.split;
+    d.z = sc.z;
+    d.s1 = sc.s1;
+    d.s2 = sc.s2;
+    d.s3 = sc.s3;
     if (from_bf16 && M <= kDecodeLocalQuantMaxM) {
       d.x = a_bf16;   // quantized inside the GEMM kernel
       d.ldx = lda;
@@ -282,6 +299,13 @@ static mxfp4_status gemm_any(const void* a_bf16, int lda, const uint8_t* a_codes
   p.K = K;
   p.qcodes = qcodes;
   p.qscales = qscales;
+  p.splitcat = sc.on;
+  p.cat = sc.cat;
+  p.split = sc.split;
+  p.z = sc.z;
+  p.s1 = sc.s1;
+  p.s2 = sc.s2;
+  p.s3 = sc.s3;
   p.workspace = ws + wl.streamk_off;
   p.workspace_bytes = wl.total - wl.streamk_off;
   return from_cuda(launch_gemm(p, dev, s));
@@ -301,6 +325,22 @@ mxfp4_status mxfp4_gemm_mxfp4_out(const void* a_bf16, int lda, const uint8_t* a_
   if (out_codes == nullptr || out_scales == nullptr) return MXFP4_ERR_INVALID_ARG;
   return gemm_any(a_bf16, lda, a_codes, a_scales, a_layout, w_packed, bias, nullptr, 0, out_codes, out_scales, M, N,
                   K, workspace, workspace_bytes, stream);
+}
+
+mxfp4_status mxfp4_gemm_split_cat(const void* a_bf16, int lda, const uint8_t* a_codes, const uint8_t* a_scales,
+                                  mxfp4_layout a_layout, const void* w_packed, const void* bias, int M, int N, int K,
+                                  int s1, int s2, const void* z, int s3, void* out_cat, void* out_split,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+  if (s1 < 0 || s2 < 0 || s3 < 0 || s1 + s2 == 0) return MXFP4_ERR_INVALID_ARG;
+  if ((s1 + s3 > 0 && out_cat == nullptr) || (s2 > 0 && out_split == nullptr) || (s3 > 0 && z == nullptr))
+    return MXFP4_ERR_INVALID_ARG;
+  if (M <= 0 || N <= 0) return MXFP4_ERR_INVALID_ARG;
+  if ((s1 % 8) || (s2 % 8) || (s3 % 8) || N % (s1 + s2) != 0) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  if ((s1 + s3 > 0 && !aligned16(out_cat)) || (s2 > 0 && !aligned16(out_split)) || (s3 > 0 && !aligned16(z)))
+    return MXFP4_ERR_MISALIGNED;
+  SplitCat sc{true, out_cat, out_split, z, s1, s2, s3};
+  return gemm_any(a_bf16, lda, a_codes, a_scales, a_layout, w_packed, bias, nullptr, 0, nullptr, nullptr, M, N, K,
+                  workspace, workspace_bytes, stream, sc);
 }
 
 mxfp4_status a16wfp4_bmm(const void* x, const void* w_packed, void* out, int B, int M, int N, int K,

@@ -156,9 +156,10 @@ __device__ __forceinline__ void split_sum_store_q(const OutView o, int M, int S,
   }
 }
 
-// kQ: MXFP4 output (g.o.qcodes set); the bf16 instantiation holds none of
-// its code.
-template <int kRowsA, bool kQ>
+// kOut: 0 bf16 output, 1 MXFP4 output (g.o.qcodes set), 2 the split + cat
+// form (g.o.splitcat set); the bf16 instantiation holds none of the other forms'
+// code.
+template <int kRowsA, int kOut>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_constant__ DecodeArgs g) {
   using C = Cfg<kRowsA>;
   extern __shared__ uint8_t smem_raw[];
@@ -417,8 +418,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
               float chunk[32];
 #pragma unroll
               for (int c = 0; c < 32; ++c) chunk[c] = __uint_as_float(r[c0 + c]);
-              if (kQ)
+              if (kOut == 1)
                 store_chunk_q(g.o, rl, n0 + c0, chunk);
+              else if (kOut == 2)
+                store_chunk_sc(g.o, rl, n0 + c0, chunk);
               else
                 store_chunk_bf16(g.o, rl, n0 + c0, chunk);
             }
@@ -447,8 +450,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
       const int q_lo = rank * 64 / S, nq = (rank + 1) * 64 / S - q_lo;
       const uint32_t pbase = smem_u32(smem);
       const int n0 = t0 * kTileN;
-      if (kQ) split_sum_store_q(g.o, g.M, S, rank, pbase, n0);
-      for (int gi = threadIdx.x - 64; !kQ && gi < g.M * nq; gi += kEpiThreads) {
+      if (kOut == 1) split_sum_store_q(g.o, g.M, S, rank, pbase, n0);
+      for (int gi = threadIdx.x - 64; kOut != 1 && gi < g.M * nq; gi += kEpiThreads) {
         const int r = gi / nq, qq = q_lo + gi % nq;
         const uint32_t a = pbase + partial_off(r, qq);
         float4 p[8];
@@ -465,7 +468,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
             acc.w += p[k].w;
           }
         }
-        store_quad(g.o, r, n0 + 4 * qq, acc);
+        if (kOut == 2)
+          store_quad_sc(g.o, r, n0 + 4 * qq, acc);
+        else
+          store_quad(g.o, r, n0 + 4 * qq, acc);
       }
     }
     cluster_sync_all();
@@ -477,19 +483,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
 // ===================================================================== host
 // Per-device, per-kernel host caches; several host threads may fill them
 // at once, each writing the same value.
-static std::atomic<bool> g_attr_set[64][6];
+static std::atomic<bool> g_attr_set[64][9];
 #ifdef MXFP4_STAMPS
 static std::atomic<int> g_stamp_next{0};   // stamp slot of the next launch (in launch order)
 #endif
-static std::atomic<int> g_max_clusters[64][6][9];   // co-resident clusters of size S (0: not yet queried)
+static std::atomic<int> g_max_clusters[64][9][9];   // co-resident clusters of size S (0: not yet queried)
 
-template <int kRowsA, bool kQ>
+template <int kRowsA, int kOut>
 static cudaError_t prepare(const DeviceInfo& dev, int which) {
   using C = Cfg<kRowsA>;
   if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
   if (!g_attr_set[dev.device][which].load(std::memory_order_acquire)) {
     cudaError_t e =
-        cudaFuncSetAttribute(decode_kernel<kRowsA, kQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        cudaFuncSetAttribute(decode_kernel<kRowsA, kOut>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     g_attr_set[dev.device][which].store(true, std::memory_order_release);
   }
@@ -497,7 +503,7 @@ static cudaError_t prepare(const DeviceInfo& dev, int which) {
 }
 
 // How many clusters of S CTAs (one per SM) the device holds at once.
-template <int kRowsA, bool kQ>
+template <int kRowsA, int kOut>
 static int max_clusters(int S, const DeviceInfo& dev, int which) {
   using C = Cfg<kRowsA>;
   std::atomic<int>& slot = g_max_clusters[dev.device][which][S];
@@ -515,7 +521,7 @@ static int max_clusters(int S, const DeviceInfo& dev, int which) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<kRowsA, kQ>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, decode_kernel<kRowsA, kOut>, &cfg) != cudaSuccess) {
       cudaGetLastError();
       n = 0;
     }
@@ -525,10 +531,10 @@ static int max_clusters(int S, const DeviceInfo& dev, int which) {
   return cached;
 }
 
-template <int kRowsA, bool kQ>
+template <int kRowsA, int kOut>
 static cudaError_t launch_rows(DecodeArgs a, const DeviceInfo& dev, cudaStream_t s, int which) {
   using C = Cfg<kRowsA>;
-  cudaError_t e = prepare<kRowsA, kQ>(dev, which);
+  cudaError_t e = prepare<kRowsA, kOut>(dev, which);
   if (e != cudaSuccess) return e;
   // Split: with fewer tiles than SMs, S CTAs per tile (a cluster), S as
   // large as the SMs allow (at most 8 and at most one k-step per CTA) with
@@ -538,7 +544,7 @@ static cudaError_t launch_rows(DecodeArgs a, const DeviceInfo& dev, cudaStream_t
     split = dev.sm_count / a.n_tiles;
     if (split > 8) split = 8;
     if (split > a.KT) split = a.KT;
-    while (split > 1 && max_clusters<kRowsA, kQ>(split, dev, which) < a.n_tiles) --split;
+    while (split > 1 && max_clusters<kRowsA, kOut>(split, dev, which) < a.n_tiles) --split;
   }
   a.split = split;
   const int grid = split > 1 ? a.n_tiles * split : (a.n_tiles < dev.sm_count ? a.n_tiles : dev.sm_count);
@@ -557,7 +563,7 @@ static cudaError_t launch_rows(DecodeArgs a, const DeviceInfo& dev, cudaStream_t
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = split > 1 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, decode_kernel<kRowsA, kQ>, a);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<kRowsA, kOut>, a);
 }
 
 cudaError_t launch_decode(const DecodeProblem& p, const DeviceInfo& dev, cudaStream_t s) {
@@ -575,6 +581,13 @@ cudaError_t launch_decode(const DecodeProblem& p, const DeviceInfo& dev, cudaStr
   a.o.N = p.N;
   a.o.qcodes = p.qcodes;
   a.o.qscales = p.qscales;
+  a.o.cat = static_cast<__nv_bfloat16*>(p.cat);
+  a.o.split = static_cast<__nv_bfloat16*>(p.split);
+  a.o.z = static_cast<const __nv_bfloat16*>(p.z);
+  a.o.s1 = p.s1;
+  a.o.s2 = p.s2;
+  a.o.s3 = p.s3;
+  a.o.splitcat = p.splitcat ? 1 : 0;
   a.M = p.M;
   a.K = p.K;
   a.KT = static_cast<int>(padded_k(p.K) / kKTile);
@@ -584,15 +597,22 @@ cudaError_t launch_decode(const DecodeProblem& p, const DeviceInfo& dev, cudaStr
 #endif
   if (p.qcodes != nullptr) {
     switch (gemm_rows_a(p.M)) {
-      case 16: return launch_rows<16, true>(a, dev, s, 3);
-      case 32: return launch_rows<32, true>(a, dev, s, 4);
-      default: return launch_rows<64, true>(a, dev, s, 5);
+      case 16: return launch_rows<16, 1>(a, dev, s, 3);
+      case 32: return launch_rows<32, 1>(a, dev, s, 4);
+      default: return launch_rows<64, 1>(a, dev, s, 5);
+    }
+  }
+  if (p.splitcat) {
+    switch (gemm_rows_a(p.M)) {
+      case 16: return launch_rows<16, 2>(a, dev, s, 6);
+      case 32: return launch_rows<32, 2>(a, dev, s, 7);
+      default: return launch_rows<64, 2>(a, dev, s, 8);
     }
   }
   switch (gemm_rows_a(p.M)) {
-    case 16: return launch_rows<16, false>(a, dev, s, 0);
-    case 32: return launch_rows<32, false>(a, dev, s, 1);
-    default: return launch_rows<64, false>(a, dev, s, 2);
+    case 16: return launch_rows<16, 0>(a, dev, s, 0);
+    case 32: return launch_rows<32, 0>(a, dev, s, 1);
+    default: return launch_rows<64, 0>(a, dev, s, 2);
   }
 }
 

@@ -354,7 +354,7 @@ __global__ void __launch_bounds__(256, 4) gemm_fixup_kernel(const __grid_constan
 #pragma unroll
   for (int j = 0; j < 2; ++j) {
     const int gi = g0 + 256 * j;
-    if (gi < groups) store_quad(g.o, mt * 128 + gi / (kTileN / 4), nt * kTileN + 4 * (gi % (kTileN / 4)), acc[j]);
+    if (gi < groups) store_quad_any(g.o, mt * 128 + gi / (kTileN / 4), nt * kTileN + 4 * (gi % (kTileN / 4)), acc[j]);
   }
 }
 
@@ -385,6 +385,13 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
   a.o.N = p.N;
   a.o.qcodes = p.qcodes;
   a.o.qscales = p.qscales;
+  a.o.cat = static_cast<__nv_bfloat16*>(p.cat);
+  a.o.split = static_cast<__nv_bfloat16*>(p.split);
+  a.o.z = static_cast<const __nv_bfloat16*>(p.z);
+  a.o.s1 = p.s1;
+  a.o.s2 = p.s2;
+  a.o.s3 = p.s3;
+  a.o.splitcat = p.splitcat ? 1 : 0;
   a.M = p.M;
   a.KT = static_cast<int>(Kp / kKTile);
   a.n_tiles = static_cast<int>(ceil_div(p.N, kTileN));

@@ -75,16 +75,51 @@ __device__ __forceinline__ int sk_owner(int it, int total, int grid) {
   return c;
 }
 
-// Where the results go: bf16 [M][ldo], or (qcodes != null) the MXFP4
+// Where the results go: bf16 [M][ldo]; or (qcodes != null) the MXFP4
 // quantization of those bf16 values, row-major codes [M][N/2] and scales
-// [M][ceil(N/32)] (N even).
+// [M][ceil(N/32)] (N even); or (splitcat set) the split + cat form: the
+// columns are H = N / (s1 + s2) groups of s1 + s2, the first s1 of group h
+// go to cat[m][h][0, s1) and the other s2 to split[m][h][0, s2), and z[m][h]
+// (s3 values) is copied to cat[m][h][s1, s1 + s3).  s1, s2, s3 are
+// multiples of 8 and cat, split, z 16-byte aligned.
 struct OutView {
   __nv_bfloat16* out;
   const __nv_bfloat16* bias;   // [N] or null
   int ldo, N;
   uint8_t* qcodes;
   uint8_t* qscales;
+  __nv_bfloat16* cat;          // [M][H][s1 + s3]
+  __nv_bfloat16* split;        // [M][H][s2]
+  const __nv_bfloat16* z;      // [M][H][s3]
+  int s1, s2, s3;
+  int splitcat;
 };
+
+// Split + cat form: the bf16 results of row m, columns n .. n + w - 1 (w = 4
+// or 8, never crossing a group part since n, s1 and s2 are multiples of 8
+// or n % 8 + w <= 8), to their place in cat or split; with them, the z
+// values of the same row and group at offsets j, j + G, j + 2G, ... (j the
+// columns' offset in the group, G = s1 + s2) are copied into cat, so the
+// groups' columns together copy all of z[m][h].
+template <int W>
+__device__ __forceinline__ void store_sc(const OutView& o, int m, int n, const uint32_t (&w)[W / 2]) {
+  const int G = o.s1 + o.s2, H = o.N / G;
+  const int h = n / G, j = n - h * G;
+  const size_t gi = static_cast<size_t>(m) * H + h;
+  __nv_bfloat16* dst = j < o.s1 ? o.cat + gi * (o.s1 + o.s3) + j : o.split + gi * o.s2 + (j - o.s1);
+  if constexpr (W == 8)
+    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+  else
+    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+  for (int jz = j; jz < o.s3; jz += G) {
+    const __nv_bfloat16* src = o.z + gi * o.s3 + jz;
+    __nv_bfloat16* d2 = o.cat + gi * (o.s1 + o.s3) + o.s1 + jz;
+    if constexpr (W == 8)
+      *reinterpret_cast<uint4*>(d2) = __ldg(reinterpret_cast<const uint4*>(src));
+    else
+      *reinterpret_cast<uint2*>(d2) = __ldg(reinterpret_cast<const uint2*>(src));
+  }
+}
 
 // MXFP4 output: the 32 outputs of row m from column n (a multiple of 32) +
 // bias, rounded to bf16 exactly as the bf16 store rounds them, then
@@ -141,16 +176,43 @@ __device__ __forceinline__ void store_chunk_bf16(const OutView& o, int m, int n,
   }
 }
 
+// 32 consecutive outputs of row m from column n (a multiple of 8): + bias,
+// bf16, to the split + cat outputs, 8 columns at a time.
+__device__ __forceinline__ void store_chunk_sc(const OutView& o, int m, int n, const float (&v)[32]) {
+  const uint16_t* bias = reinterpret_cast<const uint16_t*>(o.bias);
+#pragma unroll
+  for (int c = 0; c < 32; c += 8) {
+    if (n + c >= o.N) break;
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      w[i] = pack_bf16x2(with_bias(bias, n + c + 2 * i, v[c + 2 * i]), with_bias(bias, n + c + 2 * i + 1, v[c + 2 * i + 1]));
+    store_sc<8>(o, m, n + c, w);
+  }
+}
+
 // The same, or for MXFP4 output (o.qcodes set) its quantization (n is then a
-// multiple of 32).
+// multiple of 32), or the split + cat form (o.splitcat set).
 __device__ __forceinline__ void store_chunk(const OutView& o, int m, int n, const float (&v)[32]) {
   if (o.qcodes != nullptr)
     store_chunk_q(o, m, n, v);
+  else if (o.splitcat)
+    store_chunk_sc(o, m, n, v);
   else
     store_chunk_bf16(o, m, n, v);
 }
 
 // 4 consecutive outputs of row m starting at column n: + bias, bf16, store.
+// 4 consecutive outputs of row m from column n (a multiple of 4): + bias,
+// bf16, to the split + cat outputs.
+__device__ __forceinline__ void store_quad_sc(const OutView& o, int m, int n, float4 v) {
+  if (n >= o.N) return;
+  const uint16_t* bias = reinterpret_cast<const uint16_t*>(o.bias);
+  const uint32_t w[2] = {pack_bf16x2(with_bias(bias, n, v.x), with_bias(bias, n + 1, v.y)),
+                         pack_bf16x2(with_bias(bias, n + 2, v.z), with_bias(bias, n + 3, v.w))};
+  store_sc<4>(o, m, n, w);
+}
+
 __device__ __forceinline__ void store_quad(const OutView& o, int m, int n, float4 v) {
   if (n >= o.N) return;
   __nv_bfloat16* dst = o.out + static_cast<size_t>(m) * o.ldo + n;
@@ -166,6 +228,13 @@ __device__ __forceinline__ void store_quad(const OutView& o, int m, int n, float
     for (int i = 0; i < 4; ++i)
       if (n + i < o.N) dst[i] = __float2bfloat16_rn(x[i]);
   }
+}
+
+__device__ __forceinline__ void store_quad_any(const OutView& o, int m, int n, float4 v) {
+  if (o.splitcat)
+    store_quad_sc(o, m, n, v);
+  else
+    store_quad(o, m, n, v);
 }
 
 // One stage of the MMA pipeline: the tcgen05.cp copies of its scales into

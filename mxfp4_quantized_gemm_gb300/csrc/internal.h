@@ -86,6 +86,11 @@ struct GemmProblem {
   int ldo, M, N, K;
   uint8_t* qcodes;          // MXFP4 output (row-major codes [M][N/2], scales [M][ceil(N/32)]) or null
   uint8_t* qscales;
+  bool splitcat;            // split + cat output (see OutView) instead of `out`
+  void* cat;                // bf16 [M][H][s1 + s3]
+  void* split;              // bf16 [M][H][s2]
+  const void* z;            // bf16 [M][H][s3]
+  int s1, s2, s3;
   void* workspace;          // stream-K partial sums
   size_t workspace_bytes;
 };
@@ -109,6 +114,11 @@ struct DecodeProblem {
   int ldo, M, N, K;
   uint8_t* qcodes;          // MXFP4 output or null (as GemmProblem)
   uint8_t* qscales;
+  bool splitcat;            // split + cat output (as GemmProblem)
+  void* cat;
+  void* split;
+  const void* z;
+  int s1, s2, s3;
 };
 cudaError_t launch_decode(const DecodeProblem& p, const DeviceInfo& dev, cudaStream_t s);
 uint32_t decode_read_clear_error();

@@ -17,6 +17,7 @@ including the pages' flattening of 3-D activations to 2-D for the GEMM.
     torch.ops.mxfp4.linear(x, w_packed, bias, N) -> out          # x [..., K] bf16
     torch.ops.mxfp4.linear_prequant(codes, scales, layout, w_packed, bias, M, N, K) -> out
     torch.ops.mxfp4.linear_mxfp4_out(x, w_packed, bias, N) -> (codes, scales)   # next layer's input
+    torch.ops.mxfp4.linear_split_cat(x, w_packed, bias, z, s1, s2) -> (cat, split)   # per-group split + cat
     torch.ops.mxfp4.a16wfp4_bmm(x, w_packed, N, batch_major) -> out
 """
 
@@ -284,6 +285,49 @@ def _(x, w_packed, bias, N):
     torch._check(N % 2 == 0, lambda: f"mxfp4::linear_mxfp4_out: N = {N} must be even")
     M = x.numel() // x.shape[-1]
     return x.new_empty(M, N // 2, dtype=torch.uint8), x.new_empty(M, _cdiv(N, 32), dtype=torch.uint8)
+
+
+def _check_split_cat(where: str, x: Tensor, w_packed: Tensor, bias: Optional[Tensor], z: Tensor, s1: int,
+                     s2: int) -> tuple[int, int, int]:
+    _check_args(where, x, w_packed, bias, z, dtypes=(torch.bfloat16, torch.uint8, torch.bfloat16, torch.bfloat16))
+    torch._check(s1 >= 0 and s2 >= 0 and s1 + s2 > 0 and s1 % 8 == 0 and s2 % 8 == 0,
+                 lambda: f"{where}: s1 = {s1}, s2 = {s2} must be multiples of 8, not both 0")
+    torch._check(z.dim() == 3, lambda: f"{where}: z must be [M, H, s3]")
+    M, H, s3 = z.shape
+    torch._check(M == x.numel() // x.shape[-1], lambda: f"{where}: z has {M} rows, x {x.numel() // x.shape[-1]}")
+    torch._check(s3 % 8 == 0, lambda: f"{where}: s3 = {s3} must be a multiple of 8")
+    N = H * (s1 + s2)
+    _check_weights(where, w_packed, 1, N, x.shape[-1])
+    _check_bias(where, bias, N)
+    return M, H, s3
+
+
+@custom_op("mxfp4::linear_split_cat", mutates_args=())
+def linear_split_cat(x: Tensor, w_packed: Tensor, bias: Optional[Tensor], z: Tensor, s1: int,
+                     s2: int) -> tuple[Tensor, Tensor]:
+    """linear() with the split + cat epilogue: the output's N = H (s1 + s2)
+    columns as H groups; returns cat [M, H, s1 + s3] (each group's first s1
+    columns, then z[m, h]) and split [M, H, s2] (its other s2 columns), with
+    z [M, H, s3]."""
+    M, H, s3 = _check_split_cat("mxfp4::linear_split_cat", x, w_packed, bias, z, s1, s2)
+    c = _capi()
+    K = x.shape[-1]
+    N = H * (s1 + s2)
+    x2 = x.reshape(-1, K).contiguous()
+    cat = torch.empty(M, H, s1 + s3, dtype=torch.bfloat16, device=x.device)
+    split = torch.empty(M, H, s2, dtype=torch.bfloat16, device=x.device)
+    ws, nbytes = _workspace(M, N, K, x.device)
+    b = bias.contiguous() if bias is not None else None
+    zc = z.contiguous() if s3 else None
+    c.mxfp4_gemm_split_cat(x2, K, None, None, LAYOUT_ROWMAJOR, w_packed, b, M, N, K, s1, s2, zc, s3,
+                           cat if s1 + s3 else None, split if s2 else None, ws, nbytes, _stream(x))
+    return cat, split
+
+
+@linear_split_cat.register_fake
+def _(x, w_packed, bias, z, s1, s2):
+    M, H, s3 = _check_split_cat("mxfp4::linear_split_cat", x, w_packed, bias, z, s1, s2)
+    return x.new_empty(M, H, s1 + s3), x.new_empty(M, H, s2)
 
 
 @custom_op("mxfp4::a16wfp4_bmm", mutates_args=())

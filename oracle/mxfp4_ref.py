@@ -39,7 +39,13 @@ Readings where the pages are silent:
   input's sign bit (so -0.0 encodes as 0x8);
 * a block holding Inf or NaN gets scale 0xFF and codes 0;
 * when K is not a multiple of 32, the missing elements of the last block are
-  zeros.
+  zeros;
+* the split + cat epilogue, which the pages only name (blog analysis,
+  section 2: a 5-tuple input requests the Triton-only fused "split + cat"
+  epilogue, ``fused_gemm_afp4wfp4_split_cat``): the GEMM's bf16 result is
+  viewed as H groups of s1 + s2 columns; each group's first s1 columns,
+  followed by a caller tensor's s3 values for that row and group, form one
+  output, its last s2 columns the other (``split_cat``).
 """
 
 from __future__ import annotations
@@ -221,3 +227,29 @@ def a16wfp4_bmm(x, w_codes, w_scales, K: int, batch_major: bool = False) -> np.n
     acc, _ = a16wfp4_bmm_f64(x, w_codes, w_scales, K)
     bits = f64_to_bf16_bits(acc)
     return np.ascontiguousarray(bits.transpose(1, 0, 2)) if batch_major else bits
+
+
+def split_cat(y_bits, z_bits, s1: int, s2: int):
+    """The split + cat epilogue on the GEMM's bf16 result (a reading: the pages
+    give only the name, blog analysis section 2).
+
+    ``y_bits`` [M, H * (s1 + s2)] bf16 bits, ``z_bits`` [M, H, s3] bf16 bits.
+    Returns (cat [M, H, s1 + s3], split [M, H, s2]): for every row m and group
+    h, cat[m, h] = y[m, h-th group's first s1 columns] followed by z[m, h],
+    split[m, h] = the group's last s2 columns.  Pure data movement.
+    """
+    y = np.asarray(y_bits, dtype=np.uint16)
+    z = np.asarray(z_bits, dtype=np.uint16)
+    M, N = y.shape
+    G = s1 + s2
+    H = N // G
+    assert H * G == N and z.shape[:2] == (M, H)
+    s3 = z.shape[2]
+    cat = np.empty((M, H, s1 + s3), dtype=np.uint16)
+    split = np.empty((M, H, s2), dtype=np.uint16)
+    for h in range(H):
+        group = y[:, h * G:(h + 1) * G]
+        cat[:, h, :s1] = group[:, :s1]
+        cat[:, h, s1:] = z[:, h, :]
+        split[:, h, :] = group[:, s1:]
+    return cat, split

@@ -173,3 +173,18 @@ def test_noalloc_gemm_argument_checks(capi):
     # fake addresses must never reach a kernel)
     if not torch.cuda.is_available():
         assert f(A, 64, A, None, A, 8, 4, 8, 64, None) in (capi.ERR_NO_DEVICE, capi.ERR_CUDA)
+
+
+def test_split_cat_argument_checks(capi):
+    # checked on the host before any device work: group sizes and the outputs the groups need
+    f = capi.lib.mxfp4_gemm_split_cat
+    p = 1 << 20   # a 16-byte aligned stand-in address; the checks below return before using it
+    common = (p, 64, None, None, 0, p, None, 4, 256, 64)
+    assert f(*common, 0, 0, None, 0, p, p, p, 1 << 20, None) == capi.ERR_INVALID_ARG      # s1 + s2 == 0
+    assert f(*common, -8, 16, None, 0, p, p, p, 1 << 20, None) == capi.ERR_INVALID_ARG    # negative
+    assert f(*common, 8, 8, None, 8, p, p, p, 1 << 20, None) == capi.ERR_INVALID_ARG      # s3 > 0 without z
+    assert f(*common, 8, 8, p, 8, None, p, p, 1 << 20, None) == capi.ERR_INVALID_ARG      # no cat output
+    assert f(*common, 8, 8, None, 0, p, None, p, 1 << 20, None) == capi.ERR_INVALID_ARG   # no split output
+    assert f(*common, 4, 12, None, 0, p, p, p, 1 << 20, None) == capi.ERR_UNSUPPORTED_SHAPE   # not multiples of 8
+    assert f(*common, 48, 48, None, 0, p, p, p, 1 << 20, None) == capi.ERR_UNSUPPORTED_SHAPE  # N % 96 != 0
+    assert f(*common, 8, 8, p + 8, 8, p, p, p, 1 << 20, None) == capi.ERR_MISALIGNED     # z misaligned

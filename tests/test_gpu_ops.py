@@ -156,6 +156,11 @@ def test_opcheck_schema_and_fake(capi):
                           (xd, dev_bf16(synth.norm_gamma(K, seed=9)), 1e-6, 0, dev_bf16(synth.residual(M, K, seed=9))),
                           test_utils=utils)
     torch.library.opcheck(torch.ops.mxfp4.pack_weights.default, (dev_u8(wc), dev_u8(ws), K), test_utils=utils)
+    # split + cat: 10 groups of 16 + 16 columns, z of 24 values per group
+    Ns = 10 * 32
+    ps = pack_weights(capi, synth.weight_codes(Ns, K, seed=10), synth.weight_scales(Ns, K, -6, 0, seed=10), K)
+    zd = dev_bf16(synth.activations(M, 10 * 24, seed=10)).reshape(M, 10, 24)
+    torch.library.opcheck(torch.ops.mxfp4.linear_split_cat.default, (xd, ps, None, zd, 16, 16), test_utils=utils)
     B = 2
     xb = dev_bf16(synth.bmm_activations(B, 7, 192, seed=9))
     pb = pack_weights(capi, synth.weight_codes(256, 192, seed=9, batch=B),
@@ -197,3 +202,17 @@ def test_graph_captured_ops_replay(capi):
     torch.cuda.synchronize()
     assert torch.equal(y, want)
     assert capi.mxfp4_get_device_error() == capi.OK
+
+
+def test_split_cat_op_matches_capi(capi):
+    M, H, s1, s2, s3, K = 6, 12, 16, 48, 8, 512
+    N = H * (s1 + s2)
+    x, wc, ws, b = problem(M, N, K, seed=13)
+    packed = pack_weights(capi, wc, ws, K)
+    z = dev_bf16(synth.activations(M, H * s3, seed=14)).reshape(M, H, s3)
+    cat, split = torch.ops.mxfp4.linear_split_cat(dev_bf16(x), packed, dev_bf16(b), z, s1, s2)
+    y = torch.ops.mxfp4.linear(dev_bf16(x), packed, dev_bf16(b), N)
+    torch.cuda.synchronize()
+    yg = y.reshape(M, H, s1 + s2)
+    assert torch.equal(cat, torch.cat([yg[:, :, :s1], z], dim=2))
+    assert torch.equal(split, yg[:, :, s1:])

@@ -60,6 +60,19 @@ def test_linear_mxfp4_out_shapes():
         torch.ops.mxfp4.linear_mxfp4_out(meta(2, 1024), packed_meta(1, 999, 1024), None, 999)
 
 
+def test_linear_split_cat_shapes():
+    cat, split = torch.ops.mxfp4.linear_split_cat(meta(3, 512), packed_meta(1, 16 * 256, 512), None,
+                                                  meta(3, 16, 64), 128, 128)
+    assert cat.shape == (3, 16, 192) and split.shape == (3, 16, 128) and cat.dtype == BF
+    cat, split = torch.ops.mxfp4.linear_split_cat(meta(2, 4, 256), packed_meta(1, 5 * 16, 256), None,
+                                                  meta(8, 5, 0), 8, 8)
+    assert cat.shape == (8, 5, 8) and split.shape == (8, 5, 8)
+    with pytest.raises(RuntimeError, match="multiples of 8"):
+        torch.ops.mxfp4.linear_split_cat(meta(3, 512), packed_meta(1, 16 * 20, 512), None, meta(3, 16, 8), 4, 16)
+    with pytest.raises(RuntimeError, match="rows"):
+        torch.ops.mxfp4.linear_split_cat(meta(3, 512), packed_meta(1, 16 * 16, 512), None, meta(4, 16, 8), 8, 8)
+
+
 def test_pack_weights_shape():
     w = torch.ops.mxfp4.pack_weights(meta(3, 300, 256, dtype=U8), meta(3, 300, 16, dtype=U8), 512)
     assert w.numel() == 3 * 2 * 2 * 34816
