@@ -190,10 +190,18 @@ __global__ void __launch_bounds__(kBmmThreads, 1) a16wfp4_bmm_kernel(const __gri
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      // ---- MMA issuer
-      uint32_t ls = 0;
+      // ---- MMA issuer.  Its MMAs are small (128 x BN x 16), so the scalar
+      // work between them matters: the ring slot and phase advance by
+      // counters, and the shared-memory descriptors by their address field
+      // (an operand's address >> 4 sits in the low bits; every operand here
+      // lies below 256 KiB, so the sums never carry out of the field).
       const uint32_t idesc = idesc_bf16(128, BN);
-      const uint32_t wbase = smem_u32(wsm);
+      const uint64_t xdesc0 = sdesc_sw128(smem_u32(xsm));
+      const uint64_t wdesc0 = sdesc_sw128(smem_u32(wsm));
+      constexpr uint64_t kSlabStep = kSlabBytes >> 4, kKStep = 32 >> 4;
+      const uint64_t wslab_step = static_cast<uint64_t>(BN) * 128 >> 4;
+      int s = 0;
+      uint32_t ph = 0;
       int i = 0;
       for (int mt = mt0; mt < mt1 && !abort; ++mt, ++i) {
         const int buf = i & 1;
@@ -201,17 +209,20 @@ __global__ void __launch_bounds__(kBmmThreads, 1) a16wfp4_bmm_kernel(const __gri
         if (!mbar_wait(&acc_empty[buf], (use & 1) ^ 1, abort)) break;
         tc_fence_after();
         const uint32_t acc = tmem + buf * BN;
-        for (int ks = 0; ks < g.KS; ++ks, ++ls) {
-          const int s = ls % stages;
-          const uint32_t ph = (ls / stages) & 1;
+        uint64_t wdesc = wdesc0;
+        for (int ks = 0; ks < g.KS; ++ks) {
           if (!mbar_wait(&full[s], ph, abort)) break;
           tc_fence_after();
-          const uint32_t xs = smem_u32(xsm + s * kSlabBytes);
-          const uint32_t wsl = wbase + static_cast<uint32_t>(ks) * BN * 128;
+          const uint64_t xdesc = xdesc0 + static_cast<uint64_t>(s) * kSlabStep;
+          mma_bf16(acc, xdesc, wdesc, idesc, ks != 0);
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            mma_bf16(acc, sdesc_sw128(xs + 32 * j), sdesc_sw128(wsl + 32 * j), idesc, (ks | j) != 0);
+          for (int j = 1; j < 4; ++j) mma_bf16(acc, xdesc + j * kKStep, wdesc + j * kKStep, idesc, 1u);
           mma_commit(&empty[s]);
+          wdesc += wslab_step;
+          if (++s == stages) {
+            s = 0;
+            ph ^= 1u;
+          }
         }
         mma_commit(&acc_full[buf]);
       }
