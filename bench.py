@@ -955,7 +955,12 @@ def run_timeline(args):
         a = stamps[seq % 64].astype(np.uint64)
         live = (a[:, 0] >> np.uint64(48)) == np.uint64(seq & 0xFFFF)
         a = a[live].copy()
-        a[:, 0] &= np.uint64(0xFFFFFFFFFFFF)
+        # point 0 keeps only the timer's low 48 bits: take the high bits from
+        # point 1 (stamped by every CTA shortly after), one 2^48 period back
+        # if the low bits wrapped in between
+        low = a[:, 0] & np.uint64(0xFFFFFFFFFFFF)
+        p0 = (a[:, 1] & ~np.uint64(0xFFFFFFFFFFFF)) | low
+        a[:, 0] = np.where(p0 > a[:, 1], p0 - np.uint64(1 << 48), p0)
         a = a.astype(np.int64)
         raw[cases[j]] = a
         t0 = a[:, 0].min()

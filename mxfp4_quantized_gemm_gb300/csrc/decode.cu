@@ -476,6 +476,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const __grid_consta
     }
     cluster_sync_all();
   }
+#ifdef MXFP4_STAMPS
+  __syncthreads();   // "done" = the whole CTA has finished (no thread returns early)
+#endif
   if (threadIdx.x == 0) MX_STAMP(7);
   if (abort) atomicOr(&g_decode_error, kErrTimeout);
 }
