@@ -62,12 +62,13 @@ def test_bmm_small_shapes(capi, B, M, N, K, batch_major):
     check_close(got_bmn, acc, mag, -(-K // 16) + 2, what=f"bmm B={B} M={M} N={N} K={K}", K=K)
 
 
-@pytest.mark.parametrize("B,M,N,K", [(185, 600, 128, 64), (89, 700, 300, 192)])
+@pytest.mark.parametrize("B,M,N,K", [(185, 600, 128, 64), (89, 700, 300, 192), (80, 300, 200, 320)])
 @pytest.mark.parametrize("batch_major", [False, True])
 def test_bmm_more_pairs_than_sms(capi, B, M, N, K, batch_major):
-    """More (batch, weight tile) pairs than a GB300 has SMs (178 and 185
-    against 152), several M tiles each, ragged M and N: the grid runs in two
-    waves of one-CTA-per-SM blocks.  Every output is compared."""
+    """More (batch, weight tile) pairs than a GB300 has SMs (185, 178 and 160
+    against 152; the last with its weight tiles in TMEM), several M tiles
+    each, ragged M and N: the grid runs in two waves of one-CTA-per-SM
+    blocks.  Every output is compared."""
     x = synth.bmm_activations(B, M, K, seed=B + M)
     wc = synth.weight_codes(N, K, seed=N + 1, batch=B)
     ws = synth.weight_scales(N, K, -8, 2, seed=N + 1, batch=B)
@@ -109,11 +110,13 @@ def test_bmm_weight_scales_at_the_e8m0_extremes(capi, band, batch_major):
     check_close(got_bmn, acc, mag, -(-K // 16) + 2, what=f"bmm {band} scales", K=K)
 
 
+@pytest.mark.parametrize("K", [192, 384])
 @pytest.mark.parametrize("batch_major", [False, True])
-def test_bmm_nan_weight_scale_poisons_its_output_column(capi, batch_major):
+def test_bmm_nan_weight_scale_poisons_its_output_column(capi, batch_major, K):
     """A live 0xFF (NaN) weight scale makes that batch's weight row's outputs
-    NaN for every activation row, and nothing else."""
-    B, M, N, K = 2, 70, 200, 192
+    NaN for every activation row, and nothing else (weight tile in shared
+    memory at K = 192, in TMEM at K = 384)."""
+    B, M, N = 2, 70, 200
     x = synth.bmm_activations(B, M, K, seed=13)
     wc = synth.weight_codes(N, K, seed=14, batch=B)
     ws = synth.weight_scales(N, K, -6, 0, seed=14, batch=B).copy()
