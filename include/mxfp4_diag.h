@@ -38,9 +38,10 @@ MXFP4_API int mxfp4_diag_max_units(void);
  * accumulators of N <= 128 columns each).
  *
  * Each unit (one CTA per SM, or one 2-CTA cluster) issues `steps` steps back
- * to back after 16 untimed ones: the copies, then the MMAs of shape
- * M x mma_n x K into the issuer's accumulator, each step committed to an
- * mbarrier, with a wait on the commit of the step `depth` back before the
+ * to back after 16 untimed ones: the copies and the MMAs of shape
+ * M x mma_n x K into the issuer's accumulator, in groups of four MMAs each
+ * after its share of the step's copies (one group per 256-wide k-step of
+ * the GEMMs), each step committed to an mbarrier, with a wait on the commit of the step `depth` back before the
  * next step is issued (depth 4: the round trip of a 4-stage pipeline ring;
  * depth 32: nearly free issue).  Operands are zero bytes.
  *

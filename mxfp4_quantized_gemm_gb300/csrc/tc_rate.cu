@@ -131,12 +131,17 @@ __device__ __forceinline__ void rate_commit(uint64_t* bar) {
 }
 
 // One instruction mix, fully unrolled: kMmas MMAs of kind kKind (0: mxf4,
-// 1: bf16, 2: the mxf4 product issued as kind::mxf4nvf4) after kCopies scale copies of form kForm per step, issued by
+// 1: bf16, 2: the mxf4 product issued as kind::mxf4nvf4) and kCopies scale
+// copies of form kForm per step (groups of four MMAs, each after its share
+// of the copies), issued by
 // kIssuers threads of the CTA (lane 0 of warps 0 and 1), each into its own
 // accumulator (columns 0.. and 128.. ; N <= 128 with two issuers) and its
 // own scale columns (256.. and 384..).
 template <bool kPair, int kKind, int kMmas, int kCopies, int kForm, int kIssuers>
 __global__ void __launch_bounds__(128, 1) tc_rate_kernel(const RateArgs a) {
+  constexpr int kGroups = kMmas >= 4 ? kMmas / 4 : 1;
+  constexpr int kMmasPerGroup = kMmas >= 4 ? 4 : kMmas;
+  static_assert(kCopies % kGroups == 0, "copies split evenly over the groups of four MMAs");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
   __shared__ uint64_t ring[kIssuers][kRateRing];
@@ -191,18 +196,24 @@ __global__ void __launch_bounds__(128, 1) tc_rate_kernel(const RateArgs a) {
       tc_fence_after();
       if (s == kRateWarm) t0 = globaltimer();
       const uint32_t scol = scbase + static_cast<uint32_t>(s & 3) * 32u;   // four rotating slots (values unused)
+      // In groups of four MMAs (a 256-wide k-step of the GEMMs), each after
+      // its share of the step's copies.
 #pragma unroll
-      for (int c = 0; c < kCopies; ++c) {
-        if (kForm == 0)
-          rate_copy<kPair, 0>(scol + 4u * (c & 7), sdesc_scales(sc_s + 512u * (c & 7)));
-        else
-          rate_copy<kPair, 1>(scol + 8u * (c & 3), sdesc_scales_128x256b(sc_s + 4096u * (c & 3)));
-      }
+      for (int grp = 0; grp < kGroups; ++grp) {
 #pragma unroll
-      for (int j = 0; j < kMmas; ++j) {
-        const uint32_t q = static_cast<uint32_t>(j & 3);
-        rate_mma<kPair, kKind>(dcol, sdesc_sw128(a_s + 32u * q), sdesc_sw128(b_s + 32u * q), id[q & 1],
-                               scol + 4u * (q >> 1), scol + 16u + 8u * (q >> 1));
+        for (int c0 = 0; c0 < kCopies / kGroups; ++c0) {
+          const int c = grp * (kCopies / kGroups) + c0;
+          if (kForm == 0)
+            rate_copy<kPair, 0>(scol + 4u * (c & 7), sdesc_scales(sc_s + 512u * (c & 7)));
+          else
+            rate_copy<kPair, 1>(scol + 8u * (c & 3), sdesc_scales_128x256b(sc_s + 4096u * (c & 3)));
+        }
+#pragma unroll
+        for (int j = 0; j < kMmasPerGroup; ++j) {
+          const uint32_t q = static_cast<uint32_t>(j & 3);
+          rate_mma<kPair, kKind>(dcol, sdesc_sw128(a_s + 32u * q), sdesc_sw128(b_s + 32u * q), id[q & 1],
+                                 scol + 4u * (q >> 1), scol + 16u + 8u * (q >> 1));
+        }
       }
       rate_commit<kPair>(&ring[issuer][s % kRateRing]);
     }
@@ -312,6 +323,9 @@ static const RateVariant kRateVariants[] = {
     MX_RATE(1, 0, 4, 4, 0, 1),  MX_RATE(1, 0, 16, 0, 0, 1), MX_RATE(0, 1, 4, 0, 0, 1),
     MX_RATE(1, 1, 4, 0, 0, 1),  MX_RATE(0, 1, 16, 0, 0, 1), MX_RATE(0, 1, 16, 0, 0, 2),
     MX_RATE(0, 2, 16, 0, 0, 1), MX_RATE(0, 2, 4, 4, 0, 1),  MX_RATE(1, 2, 16, 0, 0, 1),
+    // several k-steps per commit
+    MX_RATE(0, 0, 8, 8, 0, 1),  MX_RATE(0, 0, 16, 16, 0, 1), MX_RATE(0, 0, 8, 4, 1, 1),
+    MX_RATE(0, 0, 8, 12, 0, 1), MX_RATE(0, 1, 8, 0, 0, 1),
 };
 #undef MX_RATE
 constexpr int kNumRateVariants = static_cast<int>(sizeof(kRateVariants) / sizeof(kRateVariants[0]));
