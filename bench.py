@@ -468,7 +468,7 @@ def measured_mxf4_peak(torch, capi, dev):
     on every SM (mxfp4_diag_tensor_rate, 16 per step, depth 32), median of three launches."""
     var = next(v for v in range(capi.mxfp4_diag_tensor_rate_variants())
                if capi.mxfp4_diag_tensor_rate_info(v) == {"pair": 0, "kind": 0, "mmas": 16, "copies": 0, "form": 0,
-                                                           "issuers": 1})
+                                                           "issuers": 1, "split": 0})
     ns = torch.zeros(capi.mxfp4_diag_max_units(), dtype=torch.int64, device=dev)
     steps, meds = 2000, []
     for _ in range(3):
@@ -859,11 +859,12 @@ def run_tc_rates(args):
         if only is not None and var not in only:
             continue
         info = capi.mxfp4_diag_tensor_rate_info(var)
-        pair, kind, mmas, copies, form, issuers = (info[k] for k in ("pair", "kind", "mmas", "copies", "form",
-                                                                    "issuers"))
+        pair, kind, mmas, copies, form, issuers, split = (info[k] for k in ("pair", "kind", "mmas", "copies", "form",
+                                                                           "issuers", "split"))
         name = (f"{('mxf4', 'bf16', 'mxf4nvf4')[kind]} {'2cta' if pair else '1cta'} {mmas} mma"
                 + (f" + {copies} cp{'128x256b' if form else ''}" if copies else "")
-                + (f" x{issuers} issuers" if issuers > 1 else ""))
+                + (f" x{issuers} issuers" if issuers > 1 else "")
+                + ({1: ", copies first, a commit per 4 mma", 2: ", commit after the next copies"}.get(split, "")))
         for n, depth in TC_RATE_POINTS:
             if (pair and n < 64) or (issuers > 1 and n > 128) or (mmas == 0 and n != 256):
                 continue

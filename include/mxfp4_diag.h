@@ -28,14 +28,18 @@ MXFP4_API int mxfp4_diag_max_units(void);
 /* Tensor-pipe issue rate of one of mxfp4_diag_tensor_rate_variants()
  * instruction mixes, on every SM at once.
  *
- * mxfp4_diag_tensor_rate_info(variant, info) fills info[0..5] with the mix:
+ * mxfp4_diag_tensor_rate_info(variant, info) fills info[0..6] with the mix:
  * pair (1: cta_group::2 over a 2-CTA cluster, M = 256; 0: one CTA, M = 128),
  * kind (0: kind::mxf4.block_scale.scale_vec::2X, E2M1 x E2M1 with UE8M0
  * scales, K = 64; 1: kind::f16, bf16 x bf16, K = 16; 2: the kind 0 product
  * issued as kind::mxf4nvf4.block_scale.scale_vec::2X), MMAs per step, scale
  * copies per step, copy form (0: tcgen05.cp.32x128b.warpx4, 1:
  * tcgen05.cp.128x256b), issuing threads per CTA (1, or 2 with separate
- * accumulators of N <= 128 columns each).
+ * accumulators of N <= 128 columns each), commit placement (0: the step's
+ * groups of four MMAs each after its share of the copies, one commit per
+ * step; 1: all the step's copies first, then each group's MMAs followed by
+ * a commit of its own; 2: as 0, with each step's commit issued after the
+ * next step's copies, just before its MMAs).
  *
  * Each unit (one CTA per SM, or one 2-CTA cluster) issues `steps` steps back
  * to back after 16 untimed ones: the copies and the MMAs of shape
@@ -50,7 +54,8 @@ MXFP4_API int mxfp4_diag_max_units(void);
  * two-issuer CTA) land in ns_dev[u], or 0 if a bounded wait gave up.  *units
  * (host) receives the number of units launched.  Arguments: mma_n a multiple
  * of 16 in [16, 256] ([64, 256] for a pair, at most 128 with two issuers),
- * 1 <= steps <= 10^6, 1 <= depth <= 32; otherwise MXFP4_ERR_INVALID_ARG. */
+ * 1 <= steps <= 10^6, 1 <= depth <= 32 (2 <= depth for placement 2); otherwise
+ * MXFP4_ERR_INVALID_ARG. */
 MXFP4_API int mxfp4_diag_tensor_rate_variants(void);
 MXFP4_API mxfp4_status mxfp4_diag_tensor_rate_info(int variant, int* info);
 MXFP4_API mxfp4_status mxfp4_diag_tensor_rate(int variant, int mma_n, int steps, int depth,

@@ -194,9 +194,9 @@ def mxfp4_diag_tensor_rate_variants() -> int:
 
 def mxfp4_diag_tensor_rate_info(variant: int) -> dict:
     """The instruction mix of one measurement variant."""
-    info = (_i * 6)()
+    info = (_i * 7)()
     _check(lib.mxfp4_diag_tensor_rate_info(variant, info), "mxfp4_diag_tensor_rate_info")
-    return dict(zip(("pair", "kind", "mmas", "copies", "form", "issuers"), list(info)))
+    return dict(zip(("pair", "kind", "mmas", "copies", "form", "issuers", "split"), list(info)))
 
 
 def mxfp4_diag_tensor_rate(variant: int, mma_n: int, steps: int, depth: int, ns_dev, stream=None) -> int:

@@ -33,7 +33,7 @@ constexpr int kRateWarm = 16;                  // untimed steps before the timed
 constexpr int kRateSmem = 200 * 1024;          // keeps one CTA per SM
 constexpr int kRateOperandBytes = 80 * 1024;   // A 16 KiB, B 32 KiB, scale sources 32 KiB
 constexpr uint32_t kRateTmemCols = 512;
-constexpr int kRateRing = 32;                  // commit barriers; the deepest wait is 32 steps back
+constexpr int kRateRing = 128;                 // commit barriers: 32 steps back of up to 4 commits each
 
 struct RateArgs {
   int mma_n;       // N of each MMA (M is 128, or 256 for a pair)
@@ -137,11 +137,14 @@ __device__ __forceinline__ void rate_commit(uint64_t* bar) {
 // kIssuers threads of the CTA (lane 0 of warps 0 and 1), each into its own
 // accumulator (columns 0.. and 128.. ; N <= 128 with two issuers) and its
 // own scale columns (256.. and 384..).
-template <bool kPair, int kKind, int kMmas, int kCopies, int kForm, int kIssuers>
+template <bool kPair, int kKind, int kMmas, int kCopies, int kForm, int kIssuers, int kMode>
 __global__ void __launch_bounds__(128, 1) tc_rate_kernel(const RateArgs a) {
   constexpr int kGroups = kMmas >= 4 ? kMmas / 4 : 1;
+  constexpr bool kSplitCommit = kMode == 1;
+  constexpr int kCommits = kSplitCommit ? kGroups : 1;   // commits per step
   constexpr int kMmasPerGroup = kMmas >= 4 ? 4 : kMmas;
   static_assert(kCopies % kGroups == 0, "copies split evenly over the groups of four MMAs");
+  static_assert(32 * kCommits <= kRateRing, "the deepest wait's commit still has its own barrier");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
   __shared__ uint64_t ring[kIssuers][kRateRing];
@@ -190,33 +193,44 @@ __global__ void __launch_bounds__(128, 1) tc_rate_kernel(const RateArgs a) {
     for (int h = 0; h < 2; ++h) id[h] = kKind != 1 ? idesc_mxf4(M, a.mma_n, h * 2, h * 2) : idesc_bf16(M, a.mma_n);
     for (int s = 0; s < total; ++s) {
       if (s >= a.depth) {
-        const int w = s - a.depth;
+        const int w = (s - a.depth) * kCommits + kCommits - 1;   // the last commit of that step
         if (!mbar_wait(&ring[issuer][w % kRateRing], static_cast<uint32_t>(w / kRateRing) & 1u, abort)) break;
       }
       tc_fence_after();
       if (s == kRateWarm) t0 = globaltimer();
       const uint32_t scol = scbase + static_cast<uint32_t>(s & 3) * 32u;   // four rotating slots (values unused)
       // In groups of four MMAs (a 256-wide k-step of the GEMMs), each after
-      // its share of the step's copies.
+      // its share of the step's copies and one commit per step; or
+      // (kSplitCommit) every group's copies first, then each group's MMAs
+      // followed by a commit of its own.
 #pragma unroll
       for (int grp = 0; grp < kGroups; ++grp) {
 #pragma unroll
-        for (int c0 = 0; c0 < kCopies / kGroups; ++c0) {
-          const int c = grp * (kCopies / kGroups) + c0;
+        for (int c0 = 0; c0 < (kSplitCommit ? kCopies : kCopies / kGroups); ++c0) {
+          if (kSplitCommit && grp != 0) break;
+          const int c = kSplitCommit ? c0 : grp * (kCopies / kGroups) + c0;
           if (kForm == 0)
             rate_copy<kPair, 0>(scol + 4u * (c & 7), sdesc_scales(sc_s + 512u * (c & 7)));
           else
             rate_copy<kPair, 1>(scol + 8u * (c & 3), sdesc_scales_128x256b(sc_s + 4096u * (c & 3)));
         }
+        // kMode 2: the previous step's commit between this step's copies and
+        // its MMAs, so that no copy directly follows a commit
+        if (kMode == 2 && grp == 0 && s > 0) rate_commit<kPair>(&ring[issuer][(s - 1) % kRateRing]);
 #pragma unroll
         for (int j = 0; j < kMmasPerGroup; ++j) {
           const uint32_t q = static_cast<uint32_t>(j & 3);
           rate_mma<kPair, kKind>(dcol, sdesc_sw128(a_s + 32u * q), sdesc_sw128(b_s + 32u * q), id[q & 1],
                                  scol + 4u * (q >> 1), scol + 16u + 8u * (q >> 1));
         }
+        if (kSplitCommit) {
+          const int c = s * kCommits + grp;
+          rate_commit<kPair>(&ring[issuer][c % kRateRing]);
+        }
       }
-      rate_commit<kPair>(&ring[issuer][s % kRateRing]);
+      if (kMode == 0) rate_commit<kPair>(&ring[issuer][s % kRateRing]);
     }
+    if (kMode == 2 && total > 0 && !abort) rate_commit<kPair>(&ring[issuer][(total - 1) % kRateRing]);
     // Arrives (in both CTAs of a pair) once every instruction issued above is done.
     rate_commit<kPair>(&done[issuer]);
   }
@@ -308,13 +322,17 @@ extern "C" mxfp4_status mxfp4_diag_pair_alloc_probe(uint32_t* addr_dev, void* st
 namespace mx {
 
 // The measured instruction mixes: pair, kind, MMAs and scale copies per
-// step, copy form, issuing threads.
+// step, copy form, issuing threads, commit placement (0: after the step's
+// MMAs; 1: the step's copies all first, a commit after every group of four
+// MMAs; 2: the step's commit deferred past the next step's copies).
 struct RateVariant {
-  int pair, kind, mmas, copies, form, issuers;
+  int pair, kind, mmas, copies, form, issuers, split;   // split: the commit placement
   void* kernel;
 };
 #define MX_RATE(P, K, MM, C, F, I) \
-  { P, K, MM, C, F, I, reinterpret_cast<void*>(tc_rate_kernel<P != 0, K, MM, C, F, I>) }
+  { P, K, MM, C, F, I, 0, reinterpret_cast<void*>(tc_rate_kernel<P != 0, K, MM, C, F, I, 0>) }
+#define MX_RATE_MODE(MM, C, F, MODE) \
+  { 0, 0, MM, C, F, 1, MODE, reinterpret_cast<void*>(tc_rate_kernel<false, 0, MM, C, F, 1, MODE>) }
 static const RateVariant kRateVariants[] = {
     MX_RATE(0, 0, 4, 0, 0, 1),  MX_RATE(0, 0, 4, 6, 0, 1),  MX_RATE(0, 0, 4, 4, 0, 1),
     MX_RATE(0, 0, 4, 2, 1, 1),  MX_RATE(0, 0, 8, 0, 0, 1),  MX_RATE(0, 0, 16, 0, 0, 1),
@@ -326,8 +344,14 @@ static const RateVariant kRateVariants[] = {
     // several k-steps per commit
     MX_RATE(0, 0, 8, 8, 0, 1),  MX_RATE(0, 0, 16, 16, 0, 1), MX_RATE(0, 0, 8, 4, 1, 1),
     MX_RATE(0, 0, 8, 12, 0, 1), MX_RATE(0, 1, 8, 0, 0, 1),
+    // copies of two or four k-steps issued ahead, a commit after each k-step's MMAs
+    MX_RATE_MODE(8, 8, 0, 1),   MX_RATE_MODE(16, 16, 0, 1), MX_RATE_MODE(8, 12, 0, 1),
+    MX_RATE_MODE(8, 4, 1, 1),
+    // each step's commit deferred past the next step's copies
+    MX_RATE_MODE(4, 4, 0, 2),   MX_RATE_MODE(4, 6, 0, 2),   MX_RATE_MODE(4, 2, 1, 2),
 };
 #undef MX_RATE
+#undef MX_RATE_MODE
 constexpr int kNumRateVariants = static_cast<int>(sizeof(kRateVariants) / sizeof(kRateVariants[0]));
 
 }  // namespace mx
@@ -343,6 +367,7 @@ extern "C" mxfp4_status mxfp4_diag_tensor_rate_info(int variant, int* info) {
   info[3] = v.copies;
   info[4] = v.form;
   info[5] = v.issuers;
+  info[6] = v.split;
   return MXFP4_OK;
 }
 
@@ -354,7 +379,9 @@ extern "C" mxfp4_status mxfp4_diag_tensor_rate(int variant, int mma_n, int steps
   // N: a multiple of 16 in [16, 256] (one CTA), [64, 256] (a pair), at most 128 with two issuers
   if (mma_n % 16 != 0 || mma_n > (v.issuers == 2 ? 128 : 256) || mma_n < (v.pair ? 64 : 16))
     return MXFP4_ERR_INVALID_ARG;
-  if (steps < 1 || steps > 1000000 || depth < 1 || depth > kRateRing) return MXFP4_ERR_INVALID_ARG;
+  // a deferred commit (placement 2) is issued one step late: waiting on the step just before
+  // would wait on a commit not yet issued
+  if (steps < 1 || steps > 1000000 || depth < (v.split == 2 ? 2 : 1) || depth > 32) return MXFP4_ERR_INVALID_ARG;
   DeviceInfo dev;
   if (current_device_info(&dev) != cudaSuccess || !dev.ok) return MXFP4_ERR_NO_DEVICE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
