@@ -58,7 +58,15 @@ struct GemmArgs {
   int grid;
   int rows_a;                      // activation rows per tile that are loaded (128)
   float* partials;                 // 2 slots per CTA, rows_a x 256 floats each
+  int whole_tiles;                 // 1: each CTA takes whole tiles (no part is published)
 };
+
+// First iteration of CTA c: the balanced stream-K split of the (tile,
+// k-step) space, or, with whole tiles, the balanced split of the tiles.
+__device__ __forceinline__ int cta_begin(const GemmArgs& g, int c) {
+  if (g.whole_tiles) return static_cast<int>((static_cast<long long>(c) * (g.total / g.KT)) / g.grid) * g.KT;
+  return sk_begin(c, g.total, g.grid);
+}
 
 // One CTA per SM (the ring takes the shared memory), so the full register
 // budget of a 320-thread block is available: the epilogue holds a whole
@@ -77,8 +85,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs g) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int KT = g.KT;
   const int cta = blockIdx.x;
-  const int it0 = sk_begin(cta, g.total, g.grid);
-  const int it1 = sk_begin(cta + 1, g.total, g.grid);
+  const int it0 = cta_begin(g, cta);
+  const int it1 = cta_begin(g, cta + 1);
   bool abort = false;
 
   if (threadIdx.x == 0) {
@@ -402,6 +410,14 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
   a.grid = grid;
   a.rows_a = gemm_rows_a(p.M);
   a.partials = static_cast<float*>(p.workspace);
+  // Whole tiles per CTA when the last wave's idle share is below 3% of the
+  // work: the tiles cut by CTA boundaries then cost more (their fp32 parts
+  // written and read back, and the fix-up launch) than the idle SMs do.
+  {
+    const double waves = static_cast<double>(tiles) / grid;
+    const double idle = (static_cast<double>(ceil_div(tiles, static_cast<int64_t>(grid))) - waves) / waves;
+    a.whole_tiles = tiles >= grid && idle < 0.03 ? 1 : 0;
+  }
   if (a.rows_a != 128) return cudaErrorInvalidValue;   // M <= 64 runs in decode.cu
   using C = Cfg<128>;
   if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
@@ -416,7 +432,7 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
   FixupArgs f;
   f.g = a;
   int n_split = 0, prev = -1;
-  for (int c = 1; c < grid; ++c) {
+  for (int c = 1; c < grid && !a.whole_tiles; ++c) {
     const int b = static_cast<int>((static_cast<long long>(c) * a.total) / grid);
     if (b % a.KT == 0) continue;
     const int t = b / a.KT;
