@@ -67,7 +67,7 @@ def launches_per_call(M, N, K):
     (quantization, GEMM and split-tile sums in one kernel); 8 < M <= 64: the
     quantizer, then the decode GEMM.  Larger M: quantizer, GEMM, and the fix-up
     when a CTA boundary cuts a tile (none when the GEMM takes whole tiles per
-    CTA, as it does when that leaves under 3% of the last wave idle)."""
+    CTA, as it does when that leaves under 8% of the last wave idle)."""
     import torch
     kt = ceil_div(K, 256)
     if M <= 64:
@@ -77,7 +77,7 @@ def launches_per_call(M, N, K):
     total = tiles * kt
     grid = min(grid, total)
     waves = tiles / grid
-    if tiles >= grid and (ceil_div(tiles, grid) - waves) / waves < 0.03:
+    if tiles >= grid and (ceil_div(tiles, grid) - waves) / waves < 0.08:
         return 2                                   # whole tiles per CTA: no fix-up
     split = any(((c * total) // grid) % kt for c in range(1, grid))
     return 2 + (1 if split else 0)
