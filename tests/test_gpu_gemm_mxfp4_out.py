@@ -82,7 +82,8 @@ def test_decode_paths(capi, M, N, K):
     check(capi, M, N, K, seed=M + N + K)
 
 
-@pytest.mark.parametrize("M,N,K", [(65, 1000, 2048), (300, 5120, 5120), (2048, 1024, 5120), (1000, 3000, 1536)])
+@pytest.mark.parametrize("M,N,K", [(65, 1000, 2048), (300, 5120, 5120), (2048, 1024, 5120), (1000, 3000, 1536),
+                                   (2432, 2040, 512)])     # 152 tiles: whole tiles per CTA, no fix-up
 def test_prefill_paths(capi, M, N, K):
     check(capi, M, N, K, seed=M + N, oracle_rows=np.array([0, 1, M // 2, M - 1]))
 

@@ -67,7 +67,7 @@ def test_decode_mla_shape(capi, M):
     run(capi, M, 16, 128, 128, 64, 512, seed=M)
 
 
-@pytest.mark.parametrize("M", [300, 2048])
+@pytest.mark.parametrize("M", [300, 2048, 2432])   # 2432: 152 tiles, whole tiles per CTA (no fix-up)
 def test_prefill_mla_shape(capi, M):
     run(capi, M, 16, 128, 128, 64, 512, seed=M)
 
