@@ -84,7 +84,8 @@ typedef enum {
     MXFP4_OUT_MBN = 1   /* out[m][b][n]  (V-up projection, batch-major write) */
 } mxfp4_bmm_out_layout;
 
-/* Version of this ABI (increments on incompatible change). */
+/* Version of this ABI (increments on incompatible change; 3: the diagnostic
+ * mxfp4_diag_tensor_rate_info of mxfp4_diag.h fills seven ints, not six). */
 MXFP4_API int mxfp4_abi_version(void);
 
 /* Human-readable name of a status code (static string, never NULL). */

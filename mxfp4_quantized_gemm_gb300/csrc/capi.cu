@@ -86,7 +86,7 @@ using namespace mx;
 
 extern "C" {
 
-int mxfp4_abi_version(void) { return 2; }
+int mxfp4_abi_version(void) { return 3; }
 
 const char* mxfp4_status_string(mxfp4_status s) {
   switch (s) {

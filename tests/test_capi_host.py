@@ -47,7 +47,7 @@ def test_every_declared_symbol_has_a_binding(capi):
 
 
 def test_abi_version_and_status_strings(capi):
-    assert capi.mxfp4_abi_version() == 2
+    assert capi.mxfp4_abi_version() == 3
     for s in range(8):
         assert capi.mxfp4_status_string(s).startswith("MXFP4_")
     assert capi.mxfp4_status_string(99) == "MXFP4_ERR_UNKNOWN"
