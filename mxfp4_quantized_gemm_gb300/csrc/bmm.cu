@@ -533,6 +533,18 @@ __global__ void __launch_bounds__(kBmmThreads, 1) a16wfp4_bmm_ts_kernel(const __
 }
 
 // ------------------------------------------------------------------ host
+// The calling host thread's device context, made current if the runtime has
+// not bound it in this thread yet: cuTensorMapEncodeTiled is a driver call
+// and runs in the thread's current context, which the runtime binds lazily
+// (cudaFree(nullptr) binds it and frees nothing).
+static cudaError_t bind_device_context() {
+  static thread_local bool bound = false;
+  if (bound) return cudaSuccess;
+  const cudaError_t e = cudaFree(nullptr);
+  if (e == cudaSuccess) bound = true;
+  return e;
+}
+
 // The driver's tensor-map encoder, looked up once (thread-safe static init).
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
@@ -554,6 +566,8 @@ cudaError_t launch_bmm(const void* x, const uint8_t* w_packed, void* out, int B,
                        bool batch_major, const DeviceInfo& dev, cudaStream_t s) {
   auto encode = tensor_map_encoder();
   if (encode == nullptr) return cudaErrorNotSupported;
+  cudaError_t ce = bind_device_context();
+  if (ce != cudaSuccess) return ce;
 
   BmmArgs a{};
   a.w_packed = w_packed;

@@ -127,3 +127,44 @@ def test_bmm_nan_weight_scale_poisons_its_output_column(capi, batch_major, K):
     assert np.isnan(acc[1, :, 77]).all() and np.isfinite(acc[0]).all()
     got_bmn = got.transpose(1, 0, 2) if batch_major else got
     check_close(got_bmn, acc, mag, -(-K // 16) + 2, what="bmm NaN scale", K=K)
+
+
+def test_bmm_from_new_host_threads(capi):
+    """Calls from host threads that have made no CUDA call before (the x
+    tensor map is encoded in the calling thread's device context): two
+    threads, each its own stream, K-up and V-up shapes, the bits of the same
+    calls made on the main thread."""
+    import threading
+
+    jobs = []
+    for i, (B, M, N, K, bm) in enumerate([(4, 300, 512, 192, False), (4, 300, 256, 512, True)]):
+        x = synth.bmm_activations(B, M, K, seed=70 + i)
+        wc = synth.weight_codes(N, K, seed=71 + i, batch=B)
+        ws = synth.weight_scales(N, K, -8, 2, seed=71 + i, batch=B)
+        packed = pack_weights(capi, wc, ws, K)
+        want = run_bmm(capi, x, packed, B, M, N, K, bm)
+        jobs.append(dict(B=B, M=M, N=N, K=K, layout=capi.OUT_MBN if bm else capi.OUT_BMN, x=dev_bf16(x),
+                         packed=packed, want=want, stream=torch.cuda.Stream(),
+                         out=torch.zeros(B * M * N, dtype=torch.bfloat16, device="cuda")))
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(j):
+        try:
+            for _ in range(5):
+                capi.a16wfp4_bmm(j["x"], j["packed"], j["out"], j["B"], j["M"], j["N"], j["K"], j["layout"],
+                                 j["stream"])
+        except Exception as e:   # reported below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=worker, args=(j,)) for j in jobs]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    assert capi.mxfp4_get_device_error() == capi.OK
+    for j in jobs:
+        got = host_bits(j["out"])
+        assert np.array_equal(got.reshape(j["want"].shape), j["want"]), (j["M"], j["N"], j["K"])
