@@ -327,8 +327,8 @@ MXFP4_API mxfp4_status a16wfp4_bmm(const void* x_dev, const void* w_packed_dev, 
  * mxfp4_gemm_workspace_bytes(M, N, K) exceeds that size is rejected with
  * MXFP4_ERR_WORKSPACE.  Nothing is allocated or freed.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress); make that first call before any stream capture.
- *     The address is kept for the process: resetting the device
+ *     (cudaGetSymbolAddress).  The address is kept for the process:
+ *     resetting the device
  *     (cudaDeviceReset) while the library is in use is not supported.
  *   - All calls share the one array and it keeps the last call's contents
  *     (no call needs it cleared); calls that overlap on the GPU — on
