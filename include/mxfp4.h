@@ -328,8 +328,8 @@ MXFP4_API mxfp4_status a16wfp4_bmm(const void* x_dev, const void* w_packed_dev, 
  * MXFP4_ERR_WORKSPACE.  Nothing is allocated or freed.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress).  The address is kept for the process:
- *     resetting the device
- *     (cudaDeviceReset) while the library is in use is not supported.
+ *     resetting the device (cudaDeviceReset) while the library is in use is
+ *     not supported.
  *   - All calls share the one array and it keeps the last call's contents
  *     (no call needs it cleared); calls that overlap on the GPU — on
  *     different streams, or from several host threads without ordering —
