@@ -850,6 +850,61 @@ def run_single(args):
     print(f"single {M},{N},{K}{' (MXFP4 out)' if args.mxfp4_out else ''}: {args.calls} calls ok")
 
 
+def run_prefill_pairs(args):
+    """The prefill sweep's calls timed on the library's GEMM path and on the CTA-pair kernel
+    (mxfp4_diag_gemm_pair) where that applies: one JSON line of per-call microseconds."""
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from mxfp4_quantized_gemm_gb300 import capi, synth
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=dev)
+    sptr = stream.cuda_stream
+    cases = {}
+    for (N, K) in DECODE_NK:
+        wc = synth.weight_codes(N, K, seed=0, tensor_id=2)
+        ws = synth.weight_scales(N, K, *W_SCALE_PREFILL, seed=0, tensor_id=3)
+        packed = torch.empty(capi.mxfp4_packed_weight_bytes(1, N, K), dtype=torch.uint8, device=dev)
+        capi.mxfp4_pack_weights(torch.from_numpy(wc).to(dev), torch.from_numpy(ws).to(dev), 1, N, K, packed)
+        bias = synth.bf16_tensor(synth.bias(N, seed=0)).to(dev)
+        for M in PREFILL_MS:
+            x = synth.bf16_tensor(synth.activations(M, K, seed=M, tensor_id=1)).to(dev)
+            out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            wsb = capi.mxfp4_gemm_workspace_bytes(M, N, K)
+            work = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+            row = {}
+            for name, fn in (("library_us", capi.mxfp4_gemm), ("pair_us", capi.mxfp4_diag_gemm_pair)):
+                def call():
+                    fn(x, K, None, None, 0, packed, bias, out, N, M, N, K, work, wsb, sptr)
+                try:
+                    with torch.cuda.stream(stream):
+                        for _ in range(3):
+                            call()
+                except capi.Mxfp4Error as e:
+                    if e.status != capi.ERR_UNSUPPORTED_SHAPE:
+                        raise
+                    row[name] = None
+                    continue
+                stream.synchronize()
+                reps = 20
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    a.record(stream)
+                    for _ in range(reps):
+                        call()
+                    b.record(stream)
+                stream.synchronize()
+                row[name] = round(a.elapsed_time(b) / reps * 1e3, 1)
+            cases[f"M{M}_N{N}_K{K}"] = row
+        del packed
+    assert capi.mxfp4_get_device_error() == capi.OK
+    print(json.dumps({"prefill_pairs": cases,
+                      "note": "quantizer + GEMM (+ fix-up) per call, back-to-back calls on one weight copy; "
+                              "pair_us null where the CTA-pair kernel does not apply"}), flush=True)
+
+
 # (N of each MMA, depth) pairs measured for every instruction mix of mxfp4_diag_tensor_rate: a
 # k-step of the 1-CTA GEMM kernels is "mxf4 1cta 4 mma + 6 cp" at N = 256; depth 4 is the round trip
 # of a 4-stage ring, depth 32 leaves the tensor pipe's throughput.
@@ -1038,11 +1093,16 @@ def main():
                     help="with --timeline: also save every CTA's stamps (ns) to this .npz file")
     ap.add_argument("--timeline", action="store_true",
                     help="per-call timeline of the decode sweep from the library's timeline build (one JSON line)")
+    ap.add_argument("--prefill-pairs", action="store_true",
+                    help="time the prefill sweep's calls on the library path and on the CTA-pair kernel")
     ap.add_argument("--calls", type=int, default=6)
     ap.add_argument("--copies", type=int, default=4)
     args = ap.parse_args()
     if args.tc_rates:
         run_tc_rates(args)
+        return
+    if args.prefill_pairs:
+        run_prefill_pairs(args)
         return
     if args.timeline:
         run_timeline(args)

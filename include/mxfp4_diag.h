@@ -96,6 +96,29 @@ MXFP4_API mxfp4_status mxfp4_diag_set_wait_cycles(long long cycles);
  * launches still running are partial. */
 MXFP4_API mxfp4_status mxfp4_diag_decode_timeline(unsigned long long* host, size_t host_bytes, int* next_call);
 
+/* mxfp4_gemm run on the CTA-pair kernel: 256 x 256 output tiles, each
+ * computed by a 2-CTA cluster with tcgen05 cta_group::2 MMAs (each CTA holds
+ * 128 activation rows and 128 of the tile's 256 weight rows; six 35 KiB
+ * pipeline stages per CTA instead of four of 51 KiB), whole tiles per pair.
+ *
+ * Same operation, arguments, layouts, workspace and results as mxfp4_gemm
+ * with a bf16 output (sglang PR #39598 "[AMD] Add opt-in AITER ASM FP4 GEMM
+ * for Quark dense linear", blog analysis section 2, apply_weights: the
+ * per-1x32 activation quantization, the W4A4 GEMM with fp32 accumulation,
+ * the bias).  It applies where M > 64, the 128-row activation tiles pair up
+ * (an even count, or at least 16) and the last wave of 256 x 256 tiles over
+ * the device's co-resident CTA pairs is at most 8% idle; elsewhere it
+ * returns MXFP4_ERR_UNSUPPORTED_SHAPE before any launch.  mxfp4_gemm never
+ * takes this kernel: on the prefill shapes it measured at the single-CTA
+ * kernel's speed, not faster (per SM a pair's k-step costs the tensor pipe
+ * what a single CTA's does).  It is here so that the comparison can be
+ * repeated (python bench.py --prefill-pairs). */
+MXFP4_API mxfp4_status mxfp4_diag_gemm_pair(const void* a_bf16_dev, int lda, const uint8_t* a_codes_dev,
+                                            const uint8_t* a_scales_dev, mxfp4_layout a_layout,
+                                            const void* w_packed_dev, const void* bias_dev, void* out_dev, int ldo,
+                                            int M, int N, int K, void* workspace_dev, size_t workspace_bytes,
+                                            void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -57,6 +57,7 @@ _SIGNATURES = {
     "mxfp4_diag_pair_alloc_probe": (_i, [_p, _p]),
     "mxfp4_diag_set_wait_cycles": (_i, [ctypes.c_longlong]),
     "mxfp4_diag_decode_timeline": (_i, [_p, _sz, ctypes.POINTER(_i)]),
+    "mxfp4_diag_gemm_pair": (_i, [_p, _i, _p, _p, _i, _p, _p, _p, _i, _i, _i, _i, _p, _sz, _p]),
 }
 for _name, (_res, _args) in _SIGNATURES.items():
     _fn = getattr(lib, _name)
@@ -215,6 +216,16 @@ def mxfp4_diag_pair_alloc_probe(addr_dev, stream=None) -> None:
 
 def mxfp4_diag_set_wait_cycles(cycles: int) -> None:
     _check(lib.mxfp4_diag_set_wait_cycles(cycles), "mxfp4_diag_set_wait_cycles")
+
+
+def mxfp4_diag_gemm_pair(a_bf16, lda: int, a_codes, a_scales, a_layout: int, w_packed, bias, out, ldo: int,
+                         M: int, N: int, K: int, workspace, workspace_bytes: int, stream=None) -> None:
+    """mxfp4_gemm on the CTA-pair kernel; raises Mxfp4Error (MXFP4_ERR_UNSUPPORTED_SHAPE) where it
+    does not apply."""
+    _check(lib.mxfp4_diag_gemm_pair(_ptr(a_bf16), lda, _ptr(a_codes), _ptr(a_scales), a_layout, _ptr(w_packed),
+                                    _ptr(bias), _ptr(out), ldo, M, N, K, _ptr(workspace), workspace_bytes,
+                                    _stream(stream)),
+           "mxfp4_diag_gemm_pair")
 
 
 def mxfp4_diag_decode_timeline():

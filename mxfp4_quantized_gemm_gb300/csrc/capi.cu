@@ -194,7 +194,8 @@ struct SplitCat {
 static mxfp4_status gemm_any(const void* a_bf16, int lda, const uint8_t* a_codes, const uint8_t* a_scales,
                              mxfp4_layout a_layout, const void* w_packed, const void* bias, void* out, int ldo,
                              uint8_t* qcodes, uint8_t* qscales, int M, int N, int K, void* workspace,
-                             size_t workspace_bytes, void* stream, const SplitCat& sc = SplitCat{}) {
+                             size_t workspace_bytes, void* stream, const SplitCat& sc = SplitCat{},
+                             bool cta_pairs = false) {
   const bool quant_out = qcodes != nullptr || sc.on;   // no bf16 [M][ldo] output
   if (w_packed == nullptr || (!quant_out && out == nullptr) || (qcodes != nullptr && qscales == nullptr))
     return MXFP4_ERR_INVALID_ARG;
@@ -228,6 +229,7 @@ static mxfp4_status gemm_any(const void* a_bf16, int lda, const uint8_t* a_codes
   if (st != MXFP4_OK) return st;
   const GemmWorkspace wl = gemm_workspace_layout(M, N, K, gemm_grid(dev));
   if (workspace_bytes < wl.total) return MXFP4_ERR_WORKSPACE;
+  if (cta_pairs && gemm_pair_count(M, N, dev) <= 0) return MXFP4_ERR_UNSUPPORTED_SHAPE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
 
@@ -308,6 +310,7 @@ static mxfp4_status gemm_any(const void* a_bf16, int lda, const uint8_t* a_codes
   p.s3 = sc.s3;
   p.workspace = ws + wl.streamk_off;
   p.workspace_bytes = wl.total - wl.streamk_off;
+  p.cta_pairs = cta_pairs;
   return from_cuda(launch_gemm(p, dev, s));
 }
 
@@ -316,6 +319,13 @@ mxfp4_status mxfp4_gemm(const void* a_bf16, int lda, const uint8_t* a_codes, con
                         int N, int K, void* workspace, size_t workspace_bytes, void* stream) {
   return gemm_any(a_bf16, lda, a_codes, a_scales, a_layout, w_packed, bias, out, ldo, nullptr, nullptr, M, N, K,
                   workspace, workspace_bytes, stream);
+}
+
+mxfp4_status mxfp4_diag_gemm_pair(const void* a_bf16, int lda, const uint8_t* a_codes, const uint8_t* a_scales,
+                                  mxfp4_layout a_layout, const void* w_packed, const void* bias, void* out, int ldo,
+                                  int M, int N, int K, void* workspace, size_t workspace_bytes, void* stream) {
+  return gemm_any(a_bf16, lda, a_codes, a_scales, a_layout, w_packed, bias, out, ldo, nullptr, nullptr, M, N, K,
+                  workspace, workspace_bytes, stream, SplitCat{}, true);
 }
 
 mxfp4_status mxfp4_gemm_mxfp4_out(const void* a_bf16, int lda, const uint8_t* a_codes, const uint8_t* a_scales,

@@ -144,15 +144,34 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs g) {
       a_load(it0 + lane, st, &full[lane]);
     }
     __syncwarp();
-    if (lane == 0) {
+    if (lane == 0 && npre < n_iter) {
+      // The stage's tile and k-step advance one iteration at a time, so no
+      // division sits between a stage's release and its copies.  The
+      // producer's time per stage is on the kernel's critical path: this
+      // measured 0.8% faster than dividing.
+      int t = (it0 + npre) / KT, kt = (it0 + npre) - t * KT;
+      int mt = t / g.n_tiles, nt = t - mt * g.n_tiles;
       for (int i = npre; i < n_iter; ++i) {
         const int s = i % C::kStages;
         const uint32_t ph = (i / C::kStages) & 1;
         if (!mbar_wait(&empty[s], ph ^ 1, abort)) break;
         uint8_t* st = smem + s * C::kStageBytes;
         mbar_arrive_expect_tx(&full[s], stage_bytes(it0 + i));
-        w_load(it0 + i, st, &full[s]);
-        a_load(it0 + i, st, &full[s]);
+        bulk_g2s(st, g.w_packed + static_cast<size_t>(nt * KT + kt) * kWeightBlockBytes, kWeightBlockBytes, &full[s]);
+        const size_t ai = static_cast<size_t>(mt * KT + kt);
+        if (g.a_blocked) {
+          bulk_g2s(st + C::kW, g.a_codes + ai * (C::kALoad + C::kSA), C::kALoad + C::kSA, &full[s]);
+        } else {
+          bulk_g2s(st + C::kW, g.a_codes + (ai << 14), C::kALoad, &full[s]);
+          bulk_g2s(st + C::kW + C::kA, g.a_scales + (ai << 10), 1024, &full[s]);
+        }
+        if (++kt == KT) {
+          kt = 0;
+          if (++nt == g.n_tiles) {
+            nt = 0;
+            ++mt;
+          }
+        }
       }
     }
     __syncwarp();   // whole warp reaches the final barrier converged
@@ -269,6 +288,243 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs g) {
   if (abort) atomicOr(&g_gemm_error, kErrTimeout);
 }
 
+// ================================================================ CTA pairs
+// The same GEMM on 256 x 256 output tiles, each computed by a 2-CTA cluster
+// with the cta_group::2 MMA: CTA r of the pair holds activation rows
+// 128 r .. 128 r + 127 of the tile and weight rows 128 r .. 128 r + 127 (its
+// half of the MMA's B operand), plus the scales of all 256 weight rows.  A
+// stage is 35 KiB per CTA instead of 51, so the ring holds six stages
+// instead of four, and each SM reads 31% fewer operand bytes.  CTA 0 issues
+// the scale copies, MMAs and commits for both; CTA 1 tells it when its half
+// of a stage has landed (its MMA warp relays its own stage barrier).  Each
+// CTA drains its own 128 accumulator rows.  Whole tiles only.
+//
+// Measured on the prefill shapes it runs at the single-CTA kernel's speed
+// (0.3-1.5% slower): per SM the pair's k-step costs the tensor pipe what the
+// single CTA's does, and both kernels' producers spend most of a stage
+// issuing its bulk copies.  So mxfp4_gemm never takes it; it runs only
+// behind the diagnostic entry point mxfp4_diag_gemm_pair.
+struct CfgPair {
+  static constexpr int kWOff = 0;                            // this CTA's 128 weight rows: one code tile
+  static constexpr int kSBOff = kTileBytes;                  // scales of the tile's 256 weight rows (4 atoms)
+  static constexpr int kAOff = kTileBytes + 4 * kAtomBytes;  // activation codes, 128 rows
+  static constexpr int kSAOff = kAOff + kTileBytes;          // activation scale atoms (2)
+  static constexpr int kStageBytes = kSAOff + 2 * kAtomBytes;
+  static constexpr int kStages = 6;
+  static constexpr int kRing = kStages * kStageBytes;
+  static constexpr int kSmem = kRing + 1024 + 512;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kSfBase = 256, kSfSlot = 32, kSfbOff = 8;
+};
+static_assert(CfgPair::kSmem <= kMaxSmem, "pair ring exceeds shared memory");
+static_assert(CfgPair::kAOff % 1024 == 0 && CfgPair::kStageBytes % 1024 == 0, "swizzled tiles need 1 KiB alignment");
+static_assert(CfgPair::kSfBase + CfgPair::kStages * CfgPair::kSfSlot <= CfgPair::kTmemCols, "scale slots exceed TMEM");
+
+__global__ void __launch_bounds__(kThreads, 1) gemm_pair_kernel(const GemmArgs g) {
+  using C = CfgPair;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align_1024(smem_raw);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kRing);   // this CTA's half of the stage landed
+  uint64_t* pfull = full + C::kStages;                              // (CTA 0) CTA 1's half landed
+  uint64_t* empty = pfull + C::kStages;
+  uint64_t* acc_full = empty + C::kStages;
+  uint64_t* acc_empty = acc_full + 1;                               // (CTA 0) both CTAs drained
+  uint64_t* done = acc_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int KT = g.KT;
+  const int pair = static_cast<int>(blockIdx.x >> 1);
+  const int it0 = cta_begin(g, pair);
+  const int it1 = cta_begin(g, pair + 1);
+  const int n_iter = it1 - it0;
+  const int last_mt = (g.M - 1) >> 7;   // last 128-row activation tile that exists
+  bool abort = false;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&pfull[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 2 * (kEpiThreads / 32));   // one arrival per epilogue warp of either CTA
+    mbar_init(done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, C::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();   // both CTAs' barriers and TMEM exist before any remote arrival or MMA
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) griddep_launch_dependents();
+
+  if (warp == 0) {
+    // ---- producer: this CTA's half of each stage
+    auto w_load = [&](int it, uint8_t* st, uint64_t* bar) {
+      const int t = it / KT, kt = it - t * KT;
+      const int nt = t % g.n_tiles;
+      const uint8_t* blk = g.w_packed + static_cast<size_t>(nt * KT + kt) * kWeightBlockBytes;
+      if (rank == 0) {
+        bulk_g2s(st + C::kWOff, blk, kTileBytes, bar);
+        bulk_g2s(st + C::kSBOff, blk + 2 * kTileBytes, 4 * kAtomBytes, bar);
+      } else {   // the second code tile and the scales are contiguous in the packed block
+        bulk_g2s(st + C::kWOff, blk + kTileBytes, kTileBytes + 4 * kAtomBytes, bar);
+      }
+    };
+    auto a_load = [&](int it, uint8_t* st, uint64_t* bar) {
+      const int t = it / KT, kt = it - t * KT;
+      int mt = 2 * (t / g.n_tiles) + static_cast<int>(rank);
+      mt = mt < last_mt ? mt : last_mt;   // rows past M: any existing tile (never stored)
+      if (g.a_blocked) {
+        bulk_g2s(st + C::kAOff, g.a_codes + static_cast<size_t>(mt * KT + kt) * (kTileBytes + 2 * kAtomBytes),
+                 kTileBytes + 2 * kAtomBytes, bar);
+      } else {
+        bulk_g2s(st + C::kAOff, g.a_codes + (static_cast<size_t>(mt * KT + kt) << 14), kTileBytes, bar);
+        bulk_g2s(st + C::kSAOff, g.a_scales + (static_cast<size_t>(mt * KT + kt) << 10), 2 * kAtomBytes, bar);
+      }
+    };
+    const int npre = n_iter < C::kStages ? n_iter : C::kStages;
+    if (lane < npre) {
+      uint8_t* st = smem + lane * C::kStageBytes;
+      mbar_arrive_expect_tx(&full[lane], C::kStageBytes);
+      w_load(it0 + lane, st, &full[lane]);
+      griddep_wait();
+      a_load(it0 + lane, st, &full[lane]);
+    }
+    __syncwarp();
+    if (lane == 0) {
+      for (int i = npre; i < n_iter; ++i) {
+        const int s = i % C::kStages;
+        const uint32_t ph = (i / C::kStages) & 1;
+        if (!mbar_wait_cluster(&empty[s], ph ^ 1, abort)) break;
+        uint8_t* st = smem + s * C::kStageBytes;
+        mbar_arrive_expect_tx(&full[s], C::kStageBytes);
+        w_load(it0 + i, st, &full[s]);
+        a_load(it0 + i, st, &full[s]);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---- MMA issuer for the pair.  Activation scales stay in TMEM across
+      // the tiles of one activation row tile when they fit (as in gemm_kernel).
+      constexpr uint32_t kSfaRes = C::kSfBase + C::kStages * 16u;
+      const bool resident = kSfaRes + 8u * static_cast<uint32_t>(KT) <= C::kTmemCols;
+      int cur_mt = -1;
+      uint32_t have = 0;
+      int i = 0;
+      for (int seg = 0; seg * KT < n_iter && !abort; ++seg) {
+        const int mt = ((it0 / KT) + seg) / g.n_tiles;
+        if (mt != cur_mt) {
+          cur_mt = mt;
+          have = 0;
+        }
+        for (int k = 0; k < KT; ++k, ++i) {
+          const int s = i % C::kStages;
+          const uint32_t ph = (i / C::kStages) & 1;
+          if (!mbar_wait(&full[s], ph, abort)) break;
+          if (!mbar_wait_cluster(&pfull[s], ph, abort)) break;
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + s * C::kStageBytes);
+          const uint32_t sfa_col = resident ? kSfaRes + 8u * k : C::kSfBase + s * C::kSfSlot;
+          const uint32_t sfb_col = resident ? C::kSfBase + 16u * s : sfa_col + C::kSfbOff;
+          const uint32_t sfa = tmem + sfa_col, sfb = tmem + sfb_col;
+          if (!resident || ((have >> k) & 1u) == 0) {
+            tmem_cp_scales_pair(sfa + 0, sdesc_scales(st + C::kSAOff));
+            tmem_cp_scales_pair(sfa + 4, sdesc_scales(st + C::kSAOff + kAtomBytes));
+          }
+          if (resident) have |= 1u << k;
+#pragma unroll
+          for (int a = 0; a < 2; ++a)
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+              tmem_cp_scales_pair(sfb + a * 8 + q * 4, sdesc_scales(st + C::kSBOff + q * 2 * kAtomBytes + a * kAtomBytes));
+          if (k == 0) {
+            if (!mbar_wait_cluster(acc_empty, (seg & 1) ^ 1, abort)) break;
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t id = idesc_mxf4(256, kTileN, (q & 1) * 2, (q & 1) * 2);
+            mma_mxf4_pair(tmem, sdesc_sw128(st + C::kAOff + 32 * q), sdesc_sw128(st + C::kWOff + 32 * q), id,
+                          sfa + 4 * (q >> 1), sfb + 8 * (q >> 1), (k != 0 || q != 0) ? 1u : 0u);
+          }
+          mma_commit_pair(&empty[s]);
+        }
+        mma_commit_pair(acc_full);
+      }
+      mma_commit_pair(done);   // arrives in both CTAs once every MMA above has completed
+    } else if (lane == 0) {
+      // ---- CTA 1: pass each landed stage on to CTA 0's issuer
+      const uint32_t pf0 = mapa_shared(smem_u32(pfull), 0);
+      for (int i = 0; i < n_iter; ++i) {
+        const int s = i % C::kStages;
+        if (!mbar_wait(&full[s], (i / C::kStages) & 1, abort)) break;
+        mbar_arrive_cluster_relaxed(pf0 + 8u * static_cast<uint32_t>(s));
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue: warp w drains this CTA's accumulator rows 32*(w%4).., columns 128*h..
+    griddep_wait();
+    const int q = warp & 3;
+    const int h = (warp - 2) >> 2;
+    const int rl = q * 32 + lane;
+    const uint32_t ae0 = mapa_shared(smem_u32(acc_empty), 0);
+    for (int seg = 0; seg * KT < n_iter; ++seg) {
+      const int t = it0 / KT + seg;
+      const int mt = 2 * (t / g.n_tiles) + static_cast<int>(rank), nt = t % g.n_tiles;
+      const bool ok = mbar_wait_cluster(acc_full, seg & 1, abort);
+      tc_fence_after();
+      const int m = mt * 128 + rl;
+      const int n0 = nt * kTileN + h * 128;
+      uint32_t r[128];
+#pragma unroll
+      for (int c0 = 0; c0 < 128; c0 += 16)
+        tmem_ld16(tmem + (static_cast<uint32_t>(q * 32) << 16) + h * 128 + c0,
+                  *reinterpret_cast<uint32_t(*)[16]>(&r[c0]));
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster_relaxed(ae0);   // this warp's part of the accumulator is free
+      if (m < g.M) {
+        if (!ok) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c) r[c] = 0u;
+        }
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          float chunk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) chunk[c] = __uint_as_float(r[c0 + c]);
+          store_chunk(g.o, m, n0 + c0, chunk);
+        }
+      }
+    }
+  }
+  // No MMA of the pair is in flight when the TMEM is freed: both CTAs wait
+  // for the issuer's last commit.
+  if (warp == 1 && lane == 0) {
+    bool late = false;
+    mbar_wait_cluster(done, 0, late);
+    abort = abort || late;
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, C::kTmemCols);
+  }
+  if (abort) atomicOr(&g_gemm_error, kErrTimeout);
+}
+
 // ===================================================================== fix-up
 // Tiles split between CTAs, summed after the GEMM.  Block (x, y) takes
 // split tile x, float4 groups [512 y, 512 y + 512) of it (group gi = row
@@ -368,6 +624,55 @@ __global__ void __launch_bounds__(256, 4) gemm_fixup_kernel(const __grid_constan
 
 // ===================================================================== host
 static std::atomic<bool> g_attr_set[64];   // kernel attribute set on this device
+static std::atomic<int> g_pairs[64];       // co-resident CTA pairs of gemm_pair_kernel (0: not yet known)
+
+// How many CTA pairs of gemm_pair_kernel the device holds at once (its
+// shared-memory attribute set first), or -1 if that cannot be determined.
+static int resident_pairs(const DeviceInfo& dev) {
+  int n = g_pairs[dev.device].load(std::memory_order_acquire);
+  if (n != 0) return n;
+  if (cudaFuncSetAttribute(gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgPair::kSmem) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    n = -1;
+  } else {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = CfgPair::kSmem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = -1;
+    }
+  }
+  g_pairs[dev.device].store(n, std::memory_order_release);
+  return n;
+}
+
+// Idle share of the last wave when `units` of work go to `slots` workers.
+static double last_wave_idle(int64_t units, int slots) {
+  const double waves = static_cast<double>(units) / slots;
+  return (static_cast<double>(ceil_div(units, static_cast<int64_t>(slots))) - waves) / waves;
+}
+
+int gemm_pair_count(int M, int N, const DeviceInfo& dev) {
+  if (M <= kDecodeMaxM || dev.device < 0 || dev.device >= 64) return 0;
+  const int64_t n_mt = ceil_div(M, 128);
+  const int64_t tiles2 = ceil_div(M, 256) * ceil_div(N, kTileN);
+  int pairs = resident_pairs(dev);
+  const int grid = gemm_grid(dev);
+  if (pairs > grid / 2) pairs = grid / 2;
+  if (pairs <= 0) return 0;
+  if (pairs > tiles2) pairs = static_cast<int>(tiles2);
+  return (n_mt % 2 == 0 || n_mt >= 16) && last_wave_idle(tiles2, pairs) < 0.08 ? pairs : 0;
+}
 
 
 size_t gemm_streamk_workspace_bytes(int M, int N, int K, int grid) {
@@ -414,14 +719,34 @@ cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_
   // work: the tiles cut by CTA boundaries then cost more (their fp32 parts
   // written and read back, and the fix-up launch) than the idle SMs do
   // (measured: 3% and 8% against 50%, the latter slower at 2.1 waves).
-  {
-    const double waves = static_cast<double>(tiles) / grid;
-    const double idle = (static_cast<double>(ceil_div(tiles, static_cast<int64_t>(grid))) - waves) / waves;
-    a.whole_tiles = tiles >= grid && idle < 0.08 ? 1 : 0;
-  }
+  a.whole_tiles = tiles >= grid && last_wave_idle(tiles, grid) < 0.08 ? 1 : 0;
   if (a.rows_a != 128) return cudaErrorInvalidValue;   // M <= 64 runs in decode.cu
   using C = Cfg<128>;
   if (dev.device < 0 || dev.device >= 64) return cudaErrorInvalidDevice;
+  if (p.cta_pairs) {
+    // the CTA-pair kernel on 256-row tiles, whole tiles per pair, or nothing
+    const int pairs = gemm_pair_count(p.M, p.N, dev);
+    if (pairs <= 0) return cudaErrorNotSupported;
+    GemmArgs b = a;
+    b.total = static_cast<int>(ceil_div(p.M, 256) * a.n_tiles * a.KT);
+    b.grid = pairs;
+    b.whole_tiles = 1;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = CfgPair::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, gemm_pair_kernel, b);
+  }
   if (!g_attr_set[dev.device].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;

@@ -93,12 +93,17 @@ struct GemmProblem {
   int s1, s2, s3;
   void* workspace;          // stream-K partial sums
   size_t workspace_bytes;
+  bool cta_pairs;           // the CTA-pair kernel (a diagnostic), or cudaErrorNotSupported where it does not apply
 };
 // Stream-K CTAs of the GEMM on this device, and the partial-sum + ticket
 // workspace it needs for that grid.
 int gemm_grid(const DeviceInfo& dev);
 size_t gemm_streamk_workspace_bytes(int M, int N, int K, int grid);
 cudaError_t launch_gemm(const GemmProblem& p, const DeviceInfo& dev, cudaStream_t s);
+// CTA pairs the pair kernel runs an M x N problem on, or 0 where it does not
+// apply (M <= kDecodeMaxM, an odd count of 128-row activation tiles below
+// 16, or a last wave of 256 x 256 tiles more than 8% idle).
+int gemm_pair_count(int M, int N, const DeviceInfo& dev);
 uint32_t gemm_read_clear_error();
 
 // decode.cu: M <= kDecodeMaxM in one launch.
