@@ -112,11 +112,6 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 __device__ __forceinline__ void bulk_prefetch_l2(const void* gsrc, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gsrc), "r"(bytes) : "memory");
 }
-__device__ __forceinline__ uint64_t policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
 
 // ------------------------------------------------------------------ TMEM
 // Warp-wide.  Writes the allocated TMEM base address to *smem_slot.
@@ -245,9 +240,6 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 }
 
 // ---------------------------------------------------------------- misc
-__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -256,7 +248,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
-__device__ __forceinline__ bool elect_lane0() { return (threadIdx.x & 31) == 0; }
 
 // --------------------------------------------------------------- clusters
 // Barrier over every thread of every CTA of the cluster; shared-memory writes
