@@ -843,11 +843,14 @@ def run_single(args):
     for i in range(args.calls):
         if args.mxfp4_out:
             capi.mxfp4_gemm_mxfp4_out(x, K, None, None, 0, pks[i % len(pks)], None, codes, scales, M, N, K, work, wsb)
+        elif args.pairs:
+            capi.mxfp4_diag_gemm_pair(x, K, None, None, 0, pks[i % len(pks)], None, out, N, M, N, K, work, wsb)
         else:
             capi.mxfp4_gemm(x, K, None, None, 0, pks[i % len(pks)], None, out, N, M, N, K, work, wsb)
     torch.cuda.synchronize()
     assert capi.mxfp4_get_device_error() == capi.OK
-    print(f"single {M},{N},{K}{' (MXFP4 out)' if args.mxfp4_out else ''}: {args.calls} calls ok")
+    form = " (MXFP4 out)" if args.mxfp4_out else (" (CTA pairs)" if args.pairs else "")
+    print(f"single {M},{N},{K}{form}: {args.calls} calls ok")
 
 
 def run_prefill_pairs(args):
@@ -1093,6 +1096,8 @@ def main():
                     help="with --timeline: also save every CTA's stamps (ns) to this .npz file")
     ap.add_argument("--timeline", action="store_true",
                     help="per-call timeline of the decode sweep from the library's timeline build (one JSON line)")
+    ap.add_argument("--pairs", action="store_true",
+                    help="with --single: run the shape on the CTA-pair kernel (mxfp4_diag_gemm_pair)")
     ap.add_argument("--prefill-pairs", action="store_true",
                     help="time the prefill sweep's calls on the library path and on the CTA-pair kernel")
     ap.add_argument("--calls", type=int, default=6)
