@@ -19,7 +19,9 @@ import numpy as np
 import pytest
 import torch
 
-from helpers import check_close, dev_bf16, gemm_workspace, host_bits, oracle_gemm_rows, pack_weights, sample_rows
+from oracle import mxfp4_ref as ref
+from helpers import (check_close, dev_bf16, dev_u8, gemm_workspace, host_bits, oracle_gemm_rows, pack_weights,
+                     sample_rows, tiled_from_oracle)
 from test_gpu_gemm import make_problem, n_acc, run_gemm
 
 pytestmark = pytest.mark.gpu
@@ -31,12 +33,12 @@ def capi():
     return c
 
 
-def run_pair(capi, x_bits, packed, bias_bits, M, N, K):
+def run_pair(capi, x_bits, packed, bias_bits, M, N, K, pre=None):
     out = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
     wsb = capi.mxfp4_gemm_workspace_bytes(M, N, K)
     bias = dev_bf16(bias_bits) if bias_bits is not None else None
-    capi.mxfp4_diag_gemm_pair(dev_bf16(x_bits), K, None, None, 0, packed, bias, out, N, M, N, K,
-                              gemm_workspace(capi, wsb), wsb)
+    a = (dev_bf16(x_bits), K, None, None, 0) if pre is None else (None, 0) + pre
+    capi.mxfp4_diag_gemm_pair(*a, packed, bias, out, N, M, N, K, gemm_workspace(capi, wsb), wsb)
     torch.cuda.synchronize()
     assert capi.mxfp4_get_device_error() == capi.OK
     return host_bits(out)
@@ -81,6 +83,22 @@ def test_pair_tiles_every_output(capi, M, N, K):
 ])
 def test_pair_tiles_sampled_rows(capi, M, N, K):
     check(capi, M, N, K, seed=M + 3, rows=sample_rows(M, seed=M, n_random=32, boundary_stride=1))
+
+
+@pytest.mark.parametrize("M", [200, 512])
+def test_pair_prequantized_inputs_match_bf16_input(capi, M):
+    """The two pre-quantized input forms (row-major, re-laid out into the workspace, and the TILED
+    layout read in place) give the bits of the bf16 input quantized by the library."""
+    N, K = 19456, 1024
+    x, wc, ws, b = make_problem(M, N, K, seed=13, edge=True, with_bias=True)
+    packed = pack_weights(capi, wc, ws, K)
+    fused = run_pair(capi, x, packed, b, M, N, K)
+    c_ref, s_ref = ref.quantize_mxfp4(ref.bf16_bits_to_f64(x))
+    rm = run_pair(capi, x, packed, b, M, N, K, pre=(dev_u8(c_ref), dev_u8(s_ref), capi.LAYOUT_ROWMAJOR))
+    tc, ts = tiled_from_oracle(c_ref, s_ref, K)
+    tiled = run_pair(capi, x, packed, b, M, N, K, pre=(dev_u8(tc), dev_u8(ts), capi.LAYOUT_TILED))
+    assert np.array_equal(fused, rm)
+    assert np.array_equal(fused, tiled)
 
 
 @pytest.mark.parametrize("M,N,K", [(64, 1024, 512), (300, 1024, 512), (2048, 5120, 14336)])
