@@ -300,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const GemmArgs g) {
 // CTA drains its own 128 accumulator rows.  Whole tiles only.
 //
 // Measured on the prefill shapes it runs at the single-CTA kernel's speed
-// (0.3-1.5% slower): per SM the pair's k-step costs the tensor pipe what the
+// (within 0.6% per shape): per SM the pair's k-step costs the tensor pipe what the
 // single CTA's does, and both kernels' producers spend most of a stage
 // issuing its bulk copies.  So mxfp4_gemm never takes it; it runs only
 // behind the diagnostic entry point mxfp4_diag_gemm_pair.
